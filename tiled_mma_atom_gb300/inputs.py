@@ -1,0 +1,125 @@
+"""Seeded synthetic inputs for the GEMM workloads.
+
+This module only draws random numbers and packs them into the storage
+formats the library accepts; it holds none of the GEMM's arithmetic.  It is
+shared by the tests, the benchmark and the oracle checks so that every side
+reads bit-identical inputs.
+
+Storage formats:
+  * fp32 / bf16 matrices: torch tensors; bf16 values are fp32 draws rounded
+    by torch's own float->bfloat16 conversion.
+  * MXFP4: e2m1 codes packed two per byte, even k in the low nibble, rows
+    K-contiguous, shape (rows, K/2) uint8; e8m0 scales (rows, K/32) uint8.
+
+Seeds: 1000 * workload_index + {0: A, 1: B, 2: scale A, 3: scale B}.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    index: int
+    M: int
+    N: int
+    K: int
+    dtype: str          # "f32", "bf16" or "mxfp4"
+    a_dist: str         # description of the value distribution
+    b_dist: str
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.M * self.N * self.K
+
+
+WORKLOADS = {
+    "fp32_128": Workload("fp32_128", 0, 128, 128, 128, "f32", "U[-1,1]", "U[-1,1]"),
+    "bf16_1024": Workload("bf16_1024", 1, 1024, 1024, 1024, "bf16", "N(0,1)", "N(0,1)"),
+    "bf16_4096": Workload("bf16_4096", 2, 4096, 4096, 4096, "bf16", "N(0,1)", "N(0,1)"),
+    "skinny_16x28672x8192": Workload("skinny_16x28672x8192", 3, 16, 28672, 8192, "bf16",
+                                     "N(0,1)", "N(0,0.02)"),
+    "mxfp4_8192": Workload("mxfp4_8192", 4, 8192, 8192, 8192, "mxfp4",
+                           "e2m1 codes U{0..15}, e8m0 exp U[-4,4]",
+                           "e2m1 codes U{0..15}, e8m0 exp U[-4,4]"),
+}
+
+
+def _gen(seed: int) -> torch.Generator:
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    return g
+
+
+def uniform_f32(rows: int, cols: int, seed: int, lo: float = -1.0, hi: float = 1.0) -> torch.Tensor:
+    g = _gen(seed)
+    return torch.rand((rows, cols), generator=g, dtype=torch.float32) * (hi - lo) + lo
+
+
+def normal_bf16(rows: int, cols: int, seed: int, std: float = 1.0) -> torch.Tensor:
+    g = _gen(seed)
+    x = torch.randn((rows, cols), generator=g, dtype=torch.float32)
+    if std != 1.0:
+        x.mul_(std)
+    return x.to(torch.bfloat16)
+
+
+def integer_valued(rows: int, cols: int, seed: int, lo: int = -2, hi: int = 2,
+                   dtype: torch.dtype = torch.bfloat16) -> torch.Tensor:
+    """Integers uniform in [lo, hi], stored exactly in fp32 or bf16."""
+    g = _gen(seed)
+    return torch.randint(lo, hi + 1, (rows, cols), generator=g, dtype=torch.int32).to(dtype)
+
+
+def random_fp4_codes(rows: int, K: int, seed: int) -> torch.Tensor:
+    """(rows, K/2) bytes; each nibble an independent uniform e2m1 code."""
+    if K % 2:
+        raise ValueError("K must be even for packed fp4")
+    g = _gen(seed)
+    return torch.randint(0, 256, (rows, K // 2), generator=g, dtype=torch.int32).to(torch.uint8)
+
+
+def random_e8m0(rows: int, K: int, seed: int, lo: int = -4, hi: int = 4) -> torch.Tensor:
+    """(rows, K/32) bytes 127 + e, e uniform in [lo, hi]."""
+    if K % 32:
+        raise ValueError("K must be a multiple of 32")
+    g = _gen(seed)
+    e = torch.randint(lo, hi + 1, (rows, K // 32), generator=g, dtype=torch.int32)
+    return (e + 127).to(torch.uint8)
+
+
+def pack_fp4(codes: torch.Tensor) -> torch.Tensor:
+    """Pack a (rows, K) tensor of 4-bit codes, even k into the low nibble."""
+    c = codes.to(torch.int32)
+    return (c[:, 0::2] | (c[:, 1::2] << 4)).to(torch.uint8)
+
+
+def make_inputs(w: Workload):
+    """Inputs of a workload on the CPU.
+
+    Returns (A, B) for f32/bf16 and (A, B, scaleA, scaleB) for mxfp4."""
+    M = w.M
+    s = 1000 * w.index
+    if w.dtype == "f32":
+        return uniform_f32(M, w.K, s + 0), uniform_f32(w.N, w.K, s + 1)
+    if w.dtype == "bf16":
+        std_b = 0.02 if w.name.startswith("skinny") else 1.0
+        return normal_bf16(M, w.K, s + 0), normal_bf16(w.N, w.K, s + 1, std=std_b)
+    if w.dtype == "mxfp4":
+        return (random_fp4_codes(M, w.K, s + 0), random_fp4_codes(w.N, w.K, s + 1),
+                random_e8m0(M, w.K, s + 2), random_e8m0(w.N, w.K, s + 3))
+    raise ValueError(w.dtype)
+
+
+def bits_of(t: torch.Tensor):
+    """numpy view of a CPU tensor's raw bits (uint32 for f32, uint16 for bf16)."""
+    if t.dtype == torch.float32:
+        return t.contiguous().view(torch.int32).numpy().view("uint32")
+    if t.dtype == torch.bfloat16:
+        return t.contiguous().view(torch.int16).numpy().view("uint16")
+    if t.dtype == torch.uint8:
+        return t.contiguous().numpy()
+    raise TypeError(t.dtype)
