@@ -1,0 +1,441 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 tiled GEMM library (D = A·Bᵀ, fp32 accumulate).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference] [--no-extra]
+
+One step is one GEMM of the chosen workload through the library's C ABI
+(default: bf16 4096³, the compute-bound headline).  Inputs are seeded
+synthetic data resident in HBM; L2 is flushed (a 512 MiB write) before every
+timed step and the step itself is timed with CUDA events on the launching
+stream.  Rank 0 prints ONE JSON line.  Unless --no-extra is given, the line
+also carries a measurement of every other workload ("workloads"), each with
+its own roofline entry.
+
+--impl reference times the CPU oracle (oracle/, fp64, OpenMP on the host
+cores) on bounded row samples of the same workload: the reference arm.
+Under torchrun (N > 1) every rank runs its own replica of the workload on
+its own GPU (weak scaling, no data-path collective); a gloo group is used
+only for the barrier and the max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOP/s and % of GB300 dense tensor (or HBM) roofline, 1 GPU"
+HEADLINE = "bf16_4096"
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# nominal dense ratio fp4 : bf16 on GB300 (13.5 : 2.25 PFLOP/s)
+FP4_OVER_BF16 = 13.5 / 2.25
+# fp32 FFMA peak: 152 SMs x 128 FMA/clk x 2 flop x 2.07 GHz
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+L2_FLUSH_BYTES = 512 << 20
+KERNEL_OF = {"fp32_128": "ffma_gemm_kernel", "bf16_1024": "tc_bf16_kernel",
+             "bf16_4096": "tc_bf16_kernel", "skinny_16x28672x8192": "skinny_tc_kernel",
+             "mxfp4_8192": "mxfp4_kernel"}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, "measured"
+    except Exception:
+        return dict(FALLBACK), "fallback"
+
+
+def load_traffic():
+    """Per-launch DRAM bytes from committed ncu summaries, keyed by workload;
+    dropped when the kernel source changed since the capture."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            rec = json.load(f)
+    except Exception:
+        return {}
+    from tiled_mma_atom_gb300 import build as tb
+    out = {}
+    for wl, r in rec.items():
+        if r.get("source_hash") == tb.source_hash(r.get("source", "")):
+            out[wl] = r.get("dram_bytes_per_launch")
+    return out
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[3:7]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ workloads
+
+def device_inputs(w, dev):
+    import torch
+    from tiled_mma_atom_gb300 import inputs
+    host = inputs.make_inputs(w)
+    return host, [t.to(dev) for t in host]
+
+
+def make_call(w, dev_in, out, stream):
+    import tiled_mma_atom_gb300 as tmg
+    if w.dtype == "mxfp4":
+        A, B, sA, sB = dev_in
+        return lambda: tmg.gemm_mxfp4(A, B, sA, sB, out, stream=stream)
+    A, B = dev_in
+    return lambda: tmg.gemm(A, B, out, stream=stream)
+
+
+def roofline(w, ms_per_launch, peaks, peak_kind, traffic):
+    t = ms_per_launch * 1e-3
+    if w.name.startswith("skinny"):
+        alg = (w.M * w.K + w.N * w.K + w.M * w.N) * 2
+        ach = alg / t / 1e9
+        peak = peaks["hbm_gbs"]
+        r = {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
+             "algorithmic_bytes": alg}
+    elif w.dtype == "f32":
+        ach = w.flops / t / 1e12
+        peak = FP32_ALU_TFLOPS
+        r = {"bound": "alu", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+             "peak_source": "152 SMs x 128 FP32 FMA/clk x 2 x 2.07 GHz"}
+    else:
+        ach = w.flops / t / 1e12
+        peak = peaks["bf16_tflops"]
+        src = f"{peak_kind} bf16 burst"
+        if w.dtype == "mxfp4":
+            peak = peak * FP4_OVER_BF16
+            src = f"{peak_kind} bf16 burst x nominal fp4/bf16 ratio 6"
+        r = {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+             "peak_source": src}
+    r["frac"] = r["achieved"] / r["peak"]
+    r["traffic"] = traffic.get(w.name)
+    r["kernel"] = KERNEL_OF[w.name]
+    return r
+
+
+def time_device(w, steps, warmup, dev, stream, flush):
+    """Per-step CUDA-event time of one library call (inputs in HBM)."""
+    import torch
+    import tiled_mma_atom_gb300 as tmg
+    host, dev_in = device_inputs(w, dev)
+    dt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+    out = torch.empty((w.M, w.N), dtype=dt, device=dev)
+    call = make_call(w, dev_in, out, stream)
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            flush.zero_()
+            call()
+    tmg.check(stream)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    n0 = tmg.launch_count()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            flush.zero_()
+            starts[i].record(stream)
+            call()
+            ends[i].record(stream)
+    torch.cuda.synchronize()
+    launches = tmg.launch_count() - n0
+    tmg.check(stream)
+    ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    return ms, launches, host, dev_in, out
+
+
+def time_e2e(w, steps, dev, stream):
+    """Same metric through the public API with host buffers: H2D of the
+    inputs from pinned memory, the GEMM, D2H of D — all inside the timing."""
+    import torch
+    import tiled_mma_atom_gb300 as tmg
+    from tiled_mma_atom_gb300 import inputs
+    host = [t.pin_memory() for t in inputs.make_inputs(w)]
+    dev_in = [torch.empty_like(t, device=dev) for t in host]
+    dt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+    out = torch.empty((w.M, w.N), dtype=dt, device=dev)
+    out_host = torch.empty((w.M, w.N), dtype=dt).pin_memory()
+    call = make_call(w, dev_in, out, stream)
+
+    def step():
+        for h, d in zip(host, dev_in):
+            d.copy_(h, non_blocking=True)
+        call()
+        out_host.copy_(out, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for _ in range(steps):
+            step()
+    stream.synchronize()
+    dt_s = (time.perf_counter() - t0) / steps
+    tmg.check(stream)
+    h2d = sum(t.numel() * t.element_size() for t in host)
+    d2h = out_host.numel() * out_host.element_size()
+    return dt_s, h2d, d2h
+
+
+def unit_value(w, seconds):
+    return w.flops / seconds / 1e12     # TFLOP/s
+
+
+# ------------------------------------------------------------ CPU oracle
+
+def oracle_sample(w, budget_s):
+    """Time the fp64 oracle on the first r rows of D, r chosen so the run
+    takes about budget_s.  Returns (TFLOP/s, seconds, rows, threads)."""
+    import numpy as np
+    import oracle
+    from tiled_mma_atom_gb300 import inputs
+    host = inputs.make_inputs(w)
+    threads = oracle.max_threads()
+
+    def run(rows):
+        if w.dtype == "mxfp4":
+            A, B, sA, sB = [t.numpy() for t in host]
+            t0 = time.perf_counter()
+            oracle.gemm_mxfp4(A[:rows], B, sA[:rows], sB, rows, w.N, w.K)
+            return time.perf_counter() - t0
+        A, B = host
+        dtype = oracle.F32 if w.dtype == "f32" else oracle.BF16
+        a = inputs.bits_of(A[:rows])
+        b = inputs.bits_of(B)
+        t0 = time.perf_counter()
+        oracle.gemm(a, oracle.row_major(rows, w.K), b, oracle.row_major(w.N, w.K), dtype,
+                    rows, w.N, w.K)
+        return time.perf_counter() - t0
+
+    probe_rows = min(w.M, max(1, threads))
+    t = run(probe_rows)
+    rows = probe_rows
+    if t < budget_s and rows < w.M:
+        rows = int(min(w.M, max(probe_rows, probe_rows * budget_s / max(t, 1e-6))))
+        t = run(rows)
+    flops = 2.0 * rows * w.N * w.K
+    return flops / t / 1e12, t, rows, threads
+
+
+# ------------------------------------------------------------------- main
+
+def dist_setup(n):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("gloo", rank=rank, world_size=world)
+        pg = dist
+    return world, rank, local, pg
+
+
+def barrier(pg):
+    if pg is not None:
+        pg.barrier()
+
+
+def max_over_ranks(pg, x):
+    if pg is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_reference(args, world, rank, pg):
+    from tiled_mma_atom_gb300 import inputs
+    w = inputs.WORKLOADS[args.workload]
+    if rank != 0:
+        return
+    per_step = max(0.3, 90.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_sample(w, per_step)
+    vals, secs, rows, thr = [], [], 0, 0
+    t_all = time.perf_counter()
+    for _ in range(args.steps):
+        v, s, rows, thr = oracle_sample(w, per_step)
+        vals.append(v)
+        secs.append(s)
+    total = time.perf_counter() - t_all
+    value = statistics.median(vals)
+    sample = f"first {rows} of {w.M} rows of D ({rows}x{w.N}x{w.K}), fp64 oracle, median of {args.steps}"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * statistics.median(secs), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "wall_s": total}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world, rank, local, pg = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, world, rank, pg)
+        return
+
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import tiled_mma_atom_gb300 as tmg
+    from tiled_mma_atom_gb300 import inputs
+
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    peaks, peak_kind = load_peaks()
+    traffic = load_traffic()
+    w = inputs.WORKLOADS[args.workload]
+
+    # ---- timed region (headline) ----
+    clocks = ClockSampler(torch.cuda.current_device() if world == 1 else local)
+    barrier(pg)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.05)
+    t_wall = time.perf_counter()
+    ms, launches, host, dev_in, out = time_device(w, args.steps, args.warmup, dev, stream, flush)
+    wall = time.perf_counter() - t_wall
+    torch.cuda.synchronize()
+    barrier(pg)
+    clk = clocks.stop()
+    kernel_ms = sum(ms)
+    kernel_ms_max = max_over_ranks(pg, kernel_ms)
+    ms_per_step = kernel_ms_max / args.steps
+    value = world * w.flops * args.steps / (kernel_ms_max * 1e-3) / 1e12
+    rl = roofline(w, kernel_ms / args.steps, peaks, peak_kind, traffic)
+
+    e2e_s, h2d, d2h = time_e2e(w, max(3, min(20, args.steps)), dev, stream)
+    e2e_s = max_over_ranks(pg, e2e_s)
+
+    extra = {}
+    if not args.no_extra:
+        for name, ow in inputs.WORKLOADS.items():
+            if name == w.name:
+                continue
+            try:
+                steps = 400 if ow.flops < 1e11 else 100
+                oms, ol, _, _, _ = time_device(ow, steps, 5, dev, stream, flush)
+                per = statistics.mean(oms)
+                extra[name] = {"value": unit_value(ow, per * 1e-3), "unit": "TFLOP/s",
+                               "ms_median": statistics.median(oms), "ms_mean": per,
+                               "launches_per_step": ol / steps,
+                               "roofline": roofline(ow, per, peaks, peak_kind, traffic)}
+            except Exception as e:  # report, do not hide
+                extra[name] = {"unavailable": f"{type(e).__name__}: {e}"}
+
+    cpu = None
+    if rank == 0 and world == 1:
+        v, s, rows, thr = oracle_sample(w, args.cpu_budget)
+        cpu = {"value": v, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+               "sample": f"first {rows} of {w.M} rows of D ({rows}x{w.N}x{w.K}) in {s:.1f} s, fp64"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if w.dtype == "bf16" else w.dtype, "data": "synthetic",
+            "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
+                       "a": w.a_dist, "b": w.b_dist, "accumulate": "fp32",
+                       "l2": f"flushed before every timed step ({L2_FLUSH_BYTES >> 20} MiB write)",
+                       "timing": "CUDA events around each library call on its stream",
+                       "ms_median": statistics.median(ms), "ms_min": min(ms),
+                       "parallelism": f"{world} independent replica(s)"},
+            "roofline": rl,
+            "cpu_baseline": cpu,
+            "e2e": {"value": unit_value(w, e2e_s) * world, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": int(launches),
+            "clocks": clk,
+            "peaks": {"source": peak_kind, **peaks},
+            "timed_wall_s": wall,
+            "workloads": extra,
+        }
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

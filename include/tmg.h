@@ -1,0 +1,160 @@
+/*
+ * tmg.h — C ABI of the GB300 tiled GEMM library (libtmg.so).
+ *
+ * The library computes D = A·Bᵀ with fp32 accumulation on one NVIDIA GB300
+ * (sm_103a) GPU.  All compute runs in the library's own CUDA kernels; there
+ * is no CPU fallback: a call either launches GPU work or returns an error.
+ *
+ * Operation, as the FlyDSL pages state it:
+ *   - Operand convention A = (M,K), B = (N,K), C/D = (M,N): "add-target-atom-op"
+ *     (skillsmp.com), §1.4 "ThrVal layouts describe the per-thread register
+ *     footprint" and §1.5.3 "Reference coordinate system is column-major".
+ *   - Layouts are (Shape, Stride) pairs; element (i,j) lives at
+ *     crd2idx((i,j)) = i*stride_0 + j*stride_1: "FlyDSL Kernel Authoring
+ *     Skill", §2 "Layout System", "Core Types" and "Coordinate Mapping".
+ *     A top-level mode may be nested one level, e.g. (9,(4,8)) ("Construction"
+ *     in the same section); a scalar coordinate of a nested mode is split
+ *     colexicographically (first sub-mode fastest), the order idx2crd uses
+ *     in the worked example of "Coordinate Mapping".
+ *   - fp32 accumulation: the f32-accumulating MFMA atoms of §6 "MFMA
+ *     Integration" (e.g. 16x16x4 f32 and 16x16x16 f16/bf16 -> f32).
+ *   - bf16 output is the f32 accumulator rounded to nearest even (the pages
+ *     write `.to(fx.BFloat16)`, §3 "Internal Types", without a mode).
+ *   - MXFP4: e2m1 values with one e8m0 scale per 32 consecutive K elements:
+ *     §6, "gfx1250 WMMA (wave32)", MX-scaled WMMA (block_size=32), and
+ *     "Kernel authoring guide" (rocm.github.io), §4.3 GFX950 scaled MFMA.
+ *   - Calls are asynchronous on a caller-supplied stream: "Kernel authoring
+ *     guide", §2.4 `fx.Stream`.
+ *
+ * Ownership: the caller owns every buffer passed in (device memory, e.g.
+ * torch tensors).  The library never frees or retains them beyond the
+ * call.  The library owns only: a device error word (static device memory),
+ * a host cache of TMA descriptors, and per-(device, stream) split-K scratch
+ * for the skinny path, grown on demand and released by tmg_shutdown().
+ *
+ * Errors: nothing is allowed to fault.  Bad arguments return
+ * TMG_ERR_INVALID_ARG, valid but unhandled requests TMG_ERR_UNSUPPORTED,
+ * CUDA launch/runtime failures TMG_ERR_CUDA.  Every wait inside a kernel is
+ * bounded; a wait that runs out sets the device error word and the kernel
+ * returns early — tmg_check() then reports TMG_ERR_TIMEOUT.
+ * tmg_last_error() gives a message for the calling thread's last failure.
+ */
+#ifndef TMG_H
+#define TMG_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TMG_OK = 0,
+    TMG_ERR_INVALID_ARG = 1,
+    TMG_ERR_UNSUPPORTED = 2,
+    TMG_ERR_CUDA = 3,
+    TMG_ERR_TIMEOUT = 4
+} tmg_status;
+
+/* Element type of A, B and D (identical); accumulation is always fp32. */
+typedef enum { TMG_F32 = 0, TMG_BF16 = 1 } tmg_dtype;
+
+/* Which kernel family runs a gemm.  AUTO picks by dtype, layout and shape:
+ *   FFMA   — CUDA-core fp32 FMA, any layout (the fp32 path, and the general
+ *            layout path for bf16);
+ *   TC     — persistent tcgen05 tensor-core GEMM, bf16, K-major operands;
+ *   SKINNY — tensor-core swap-AB split-K GEMM for M <= 64, bf16, K-major;
+ *   SKINNY_FFMA — CUDA-core split-K dot products for M <= 16, bf16, K-major.
+ * Forcing a family that cannot take the arguments returns UNSUPPORTED. */
+typedef enum {
+    TMG_PATH_AUTO = 0,
+    TMG_PATH_FFMA = 1,
+    TMG_PATH_TC = 2,
+    TMG_PATH_SKINNY = 3,
+    TMG_PATH_SKINNY_FFMA = 4
+} tmg_path;
+
+/* A rank-2 layout over logical coordinates (row, col).  Mode t (0 = rows,
+ * 1 = columns) has depth[t] sub-modes (1 or 2) with shapes shape[t][0..] and
+ * strides stride[t][0..], counted in elements.  Unused entries are ignored.
+ * The product of the sub-shapes of mode t must equal the logical extent.
+ * Example: a row-major M x K matrix with leading dimension ld is
+ * {depth={1,1}, shape={{M,1},{K,1}}, stride={{ld,0},{1,0}}}. */
+typedef struct {
+    int32_t depth[2];
+    int64_t shape[2][2];
+    int64_t stride[2][2];
+} tmg_layout;
+
+/* D[m,n] = sum_k A(m,k) * B(n,k), fp32 accumulation.
+ *   A, B, D  device pointers to the element type `dtype`.
+ *   M, N, K  logical extents, each >= 0.  M == 0 or N == 0 is a no-op;
+ *            K == 0 writes zeros to D.
+ *   layoutA  over (m,k); NULL means row-major (M,K):(K,1).
+ *   layoutB  over (n,k); NULL means row-major (N,K):(K,1).
+ *   layoutD  over (m,n); NULL means row-major (M,N):(N,1).  D's layout must
+ *            map distinct (m,n) to distinct elements (strides > 0).
+ *   stream   a cudaStream_t (NULL = the legacy default stream).
+ * Asynchronous: returns after the launch.  Input strides may be 0
+ * (broadcast).  Offsets must fit in int64. */
+tmg_status tmg_gemm(const void *A, const void *B, void *D, int64_t M, int64_t N,
+                    int64_t K, tmg_dtype dtype, const tmg_layout *layoutA,
+                    const tmg_layout *layoutB, const tmg_layout *layoutD,
+                    void *stream);
+
+/* tmg_gemm with an explicit kernel family (see tmg_path). */
+tmg_status tmg_gemm_ex(const void *A, const void *B, void *D, int64_t M,
+                       int64_t N, int64_t K, tmg_dtype dtype,
+                       const tmg_layout *layoutA, const tmg_layout *layoutB,
+                       const tmg_layout *layoutD, tmg_path path, void *stream);
+
+/* MXFP4 GEMM: D[m,n] = sum_k a(m,k) * b(n,k) with
+ *   a(m,k) = e2m1(code of A at (m,k)) * 2^(scaleA[m, k/32] - 127), same for b.
+ *   A       device, (M, K/2) bytes row-major: two e2m1 codes per byte, the
+ *           even k in the low nibble (bits 0-3), the odd k in bits 4-7.
+ *   B       device, (N, K/2) bytes, same packing.
+ *   scaleA  device, (M, K/32) e8m0 bytes row-major; scaleB (N, K/32).
+ *           Byte 0xFF (NaN) propagates NaN.
+ *   D       device, bf16 (M, N) row-major.
+ * K must be a positive multiple of 32 (else INVALID_ARG); the tensor-core
+ * kernel additionally needs K % 256 == 0 and 16-byte aligned rows
+ * (else UNSUPPORTED).  E2M1/E8M0 follow the OCP MX v1.0 definitions. */
+tmg_status tmg_gemm_mxfp4(const void *A, const void *B, const void *scaleA,
+                          const void *scaleB, void *D, int64_t M, int64_t N,
+                          int64_t K, void *stream);
+
+/* Synchronise `stream`, then report: TMG_ERR_CUDA for a sticky or pending
+ * CUDA error, TMG_ERR_TIMEOUT if a kernel's bounded wait ran out since the
+ * last check (the device error word is cleared and the skinny-path scratch
+ * counters are reset), else TMG_OK. */
+tmg_status tmg_check(void *stream);
+
+/* Message for the calling thread's last non-OK status ("" if none).  The
+ * pointer stays valid until the thread's next library call. */
+const char *tmg_last_error(void);
+
+/* Budget of every bounded wait inside the kernels, in nanoseconds
+ * (default 2 s).  Applies to launches made after the call. */
+void tmg_set_wait_budget_ns(uint64_t ns);
+
+/* Launch one tiny kernel that waits on a barrier nothing will ever signal,
+ * with the given budget; it must give up and set the device error word, so
+ * that the next tmg_check() returns TMG_ERR_TIMEOUT.  Exercises the bounded
+ * wait of every kernel without any GPU fault or hang. */
+tmg_status tmg_debug_wait_timeout(uint64_t budget_ns, void *stream);
+
+/* Number of kernels the library has launched in this process. */
+uint64_t tmg_launch_count(void);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int tmg_version(void);
+
+/* Free library-owned device scratch and host caches.  Calls already queued
+ * must have finished.  The library stays usable afterwards. */
+void tmg_shutdown(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TMG_H */

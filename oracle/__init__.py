@@ -103,6 +103,8 @@ def lib():
         L.orc_decode_e8m0.restype = ctypes.c_double
         L.orc_round_bf16.argtypes = [ctypes.c_double]
         L.orc_round_bf16.restype = ctypes.c_uint16
+        L.orc_round_bf16_array.argtypes = [P, I64, P]
+        L.orc_round_bf16_array.restype = None
         L.orc_read_matrix.argtypes = [P, LP, I32, I64, I64, P]
         L.orc_read_matrix.restype = I32
         L.orc_gemm.argtypes = [P, LP, P, LP, I32, I64, I64, I64, P, I32]
@@ -169,9 +171,11 @@ def round_bf16(x: float) -> int:
 
 
 def round_bf16_array(x: np.ndarray) -> np.ndarray:
-    f = lib().orc_round_bf16
-    flat = np.asarray(x, dtype=np.float64).ravel()
-    return np.array([f(float(v)) for v in flat], dtype=np.uint16).reshape(np.shape(x))
+    """orc_round_bf16 applied to every element (bf16 bit patterns)."""
+    flat = np.ascontiguousarray(np.asarray(x, dtype=np.float64).ravel())
+    out = np.empty(flat.shape[0], dtype=np.uint16)
+    lib().orc_round_bf16_array(_ptr(flat), flat.shape[0], _ptr(out))
+    return out.reshape(np.shape(x))
 
 
 def read_matrix(x: np.ndarray, layout: Layout, dtype: int, rows: int, cols: int) -> np.ndarray:

@@ -161,6 +161,13 @@ uint16_t orc_round_bf16(double x)
     return sign | (uint16_t)(u >> 16);
 }
 
+/* orc_round_bf16 over an array. */
+void orc_round_bf16_array(const double *x, int64_t n, uint16_t *out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = orc_round_bf16(x[i]);
+}
+
 /* Element (r, c) of a matrix with the given layout and element type. */
 static double fetch(const void *X, const orc_layout *L, int dtype,
                     int64_t r, int64_t c)

@@ -1,7 +1,138 @@
 """tiled_mma_atom_gb300 — tiled GEMM D = A·Bᵀ (fp32 accumulate) for GB300.
 
 The compute path is a C-ABI shared library of hand-written sm_103a CUDA
-(``csrc/``, built into ``libtmg.so``); this package only marshals torch
-tensors into that library's calls.  Importing the package does not load the
-library; the first call does, and fails loudly if it is missing.
+(``csrc/``, built into ``libtmg.so``; ABI in ``include/tmg.h``).  This
+package marshals torch tensors into that library's calls and nothing else.
+Importing the package does not load the library; the first call does, and
+raises ``TmgError`` if it is missing.
+
+Layouts.  A torch tensor's (shape, stride) already is a (Shape, Stride)
+layout in the FlyDSL sense ("FlyDSL Kernel Authoring Skill", §2 Layout
+System): by default each operand's layout is taken from its tensor —
+A over (m,k), B over (n,k), D over (m,n).  Pass an explicit layout
+(``make_layout(shape, stride)``, modes nested at most one level) to read a
+buffer any other way; the buffer is then addressed through crd2idx from
+the tensor's data pointer.
 """
+from __future__ import annotations
+
+import torch
+
+from . import _native
+from ._native import (BF16, F32, PATHS, Layout, TmgError, make_layout)  # noqa: F401
+
+__all__ = ["gemm", "gemm_mxfp4", "check", "make_layout", "Layout", "TmgError",
+           "set_wait_budget_ns", "debug_wait_timeout", "launch_count", "version",
+           "shutdown", "PATHS"]
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _layout_of(t: torch.Tensor, rows: int, cols: int) -> Layout:
+    if t.dim() != 2 or tuple(t.shape) != (rows, cols):
+        raise ValueError(f"tensor of shape {tuple(t.shape)} is not ({rows}, {cols}); "
+                         "pass an explicit layout")
+    return make_layout((rows, cols), (t.stride(0), t.stride(1)))
+
+
+def _as_layout(spec, t: torch.Tensor, rows: int, cols: int) -> Layout:
+    if spec is None:
+        return _layout_of(t, rows, cols)
+    if isinstance(spec, Layout):
+        return spec
+    shape, stride = spec
+    return make_layout(shape, stride)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError(f"unsupported dtype {t.dtype}: use float32 or bfloat16")
+
+
+def gemm(A: torch.Tensor, B: torch.Tensor, D: torch.Tensor | None = None, *,
+         M: int | None = None, N: int | None = None, K: int | None = None,
+         layoutA=None, layoutB=None, layoutD=None, path: str = "auto",
+         stream=None) -> torch.Tensor:
+    """D = A·Bᵀ on the GPU, fp32 accumulation.  A is (M,K), B is (N,K), D is
+    (M,N); all three share dtype float32 or bfloat16 and live on the GPU.
+    Returns D (allocated row-major if not given).  Asynchronous on `stream`
+    (default: torch's current stream)."""
+    if M is None:
+        M = A.shape[0] if layoutA is None else None
+    if K is None:
+        K = A.shape[1] if layoutA is None else None
+    if N is None:
+        N = B.shape[0] if layoutB is None else None
+    if M is None or N is None or K is None:
+        raise ValueError("give M, N and K when passing explicit layouts")
+    if D is None:
+        D = torch.empty((M, N), dtype=A.dtype, device=A.device)
+    dt = _dtype_code(A)
+    if B.dtype != A.dtype or D.dtype != A.dtype:
+        raise TypeError("A, B and D must share one dtype")
+    if not (A.is_cuda and B.is_cuda and D.is_cuda):
+        raise ValueError("A, B and D must be CUDA tensors")
+    la = _as_layout(layoutA, A, M, K)
+    lb = _as_layout(layoutB, B, N, K)
+    ld = _as_layout(layoutD, D, M, N)
+    L = _native.lib()
+    st = L.tmg_gemm_ex(A.data_ptr(), B.data_ptr(), D.data_ptr(), M, N, K, dt,
+                       la, lb, ld, PATHS[path], _stream_handle(stream))
+    _native.raise_on(st)
+    return D
+
+
+def gemm_mxfp4(A: torch.Tensor, B: torch.Tensor, scaleA: torch.Tensor, scaleB: torch.Tensor,
+               D: torch.Tensor | None = None, *, stream=None) -> torch.Tensor:
+    """MXFP4 GEMM.  A: (M, K/2) uint8, two e2m1 codes per byte (even k in the
+    low nibble); B: (N, K/2); scaleA: (M, K/32) uint8 e8m0; scaleB: (N, K/32).
+    D: (M, N) bfloat16.  All contiguous on the GPU."""
+    M, K2 = A.shape
+    N = B.shape[0]
+    K = 2 * K2
+    for name, t, shape in (("A", A, (M, K2)), ("B", B, (N, K2)), ("scaleA", scaleA, (M, K // 32)),
+                           ("scaleB", scaleB, (N, K // 32))):
+        if t.dtype != torch.uint8 or tuple(t.shape) != shape or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError(f"{name} must be a contiguous CUDA uint8 tensor of shape {shape}")
+    if D is None:
+        D = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    if D.dtype != torch.bfloat16 or tuple(D.shape) != (M, N) or not D.is_contiguous():
+        raise ValueError("D must be a contiguous bfloat16 tensor of shape (M, N)")
+    st = _native.lib().tmg_gemm_mxfp4(A.data_ptr(), B.data_ptr(), scaleA.data_ptr(),
+                                      scaleB.data_ptr(), D.data_ptr(), M, N, K,
+                                      _stream_handle(stream))
+    _native.raise_on(st)
+    return D
+
+
+def check(stream=None) -> None:
+    """Synchronise and raise TmgError if a kernel reported a timeout or a CUDA
+    error occurred."""
+    _native.raise_on(_native.lib().tmg_check(_stream_handle(stream)))
+
+
+def set_wait_budget_ns(ns: int) -> None:
+    _native.lib().tmg_set_wait_budget_ns(int(ns))
+
+
+def debug_wait_timeout(budget_ns: int, stream=None) -> None:
+    _native.raise_on(_native.lib().tmg_debug_wait_timeout(int(budget_ns), _stream_handle(stream)))
+
+
+def launch_count() -> int:
+    return int(_native.lib().tmg_launch_count())
+
+
+def version() -> int:
+    return int(_native.lib().tmg_version())
+
+
+def shutdown() -> None:
+    _native.lib().tmg_shutdown()

@@ -1,0 +1,585 @@
+// api.cu — the library's C ABI (include/tmg.h): argument validation, layout
+// classification, TMA descriptor encoding, kernel-family dispatch and error
+// reporting.
+//
+// Layout handling follows "FlyDSL Kernel Authoring Skill", §2 "Layout
+// System": a layout is a (Shape, Stride) pair and element (i,j) sits at
+// crd2idx((i,j)) = Σ coordinate × stride.  The host classifies each operand
+// layout:
+//   K-major dense   (rows, K):(ld, 1)  -> TMA tiles, tcgen05 K-major operand
+//   anything else (MN-major, nested, strided, broadcast) -> the CUDA-core
+//                   path, which evaluates crd2idx per element.
+// D given column-major, (M,N):(1,ld), is computed as Dᵀ = B·Aᵀ with the
+// operand roles swapped, so it also reaches the tensor-core kernels.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <utility>
+
+#include "internal.h"
+#include "tmg.h"
+
+namespace tmg {
+
+__device__ uint32_t g_err_word;
+
+namespace {
+
+thread_local std::string t_last_error;
+std::atomic<uint64_t> g_budget_ns{2000000000ull};
+std::atomic<uint64_t> g_launches{0};
+std::mutex g_mu;
+
+struct DeviceState {
+    bool ready = false;
+    int num_sms = 0;
+    int cc_major = 0, cc_minor = 0;
+    uint32_t *err_word = nullptr;
+};
+std::map<int, DeviceState> g_dev;
+
+struct Scratch {
+    float *partials = nullptr;
+    size_t partials_bytes = 0;
+    uint32_t *counters = nullptr;
+    size_t counters_bytes = 0;
+};
+std::map<std::pair<int, uintptr_t>, Scratch> g_scratch;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+tmg_status fail(tmg_status st, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+tmg_status fail(tmg_status st, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    t_last_error = buf;
+    return st;
+}
+
+tmg_status cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(TMG_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// Per-device set-up, with that device current.
+tmg_status device_state(DeviceState **out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDevice");
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState &ds = g_dev[dev];
+    if (!ds.ready) {
+        if ((e = cudaDeviceGetAttribute(&ds.num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute");
+        cudaDeviceGetAttribute(&ds.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&ds.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (ds.cc_major != 10 || ds.cc_minor != 3)
+            return fail(TMG_ERR_UNSUPPORTED,
+                        "device %d is sm_%d%d; this library is built for sm_103a (GB300)", dev,
+                        ds.cc_major, ds.cc_minor);
+        void *p = nullptr;
+        if ((e = cudaGetSymbolAddress(&p, g_err_word)) != cudaSuccess)
+            return cuda_fail(e, "cudaGetSymbolAddress(error word)");
+        ds.err_word = static_cast<uint32_t *>(p);
+        if ((e = cudaMemset(ds.err_word, 0, sizeof(uint32_t))) != cudaSuccess)
+            return cuda_fail(e, "cudaMemset(error word)");
+        if (!g_encode) {
+            void *fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                 cudaEnableDefault, &q);
+            if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+                return fail(TMG_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+        }
+        ds.ready = true;
+    }
+    *out = &ds;
+    return TMG_OK;
+}
+
+ErrCtx err_ctx(const DeviceState &ds)
+{
+    return ErrCtx{ds.err_word, g_budget_ns.load()};
+}
+
+// ------------------------------------------------------------- layouts
+
+int64_t mode_size(const tmg_layout &L, int t)
+{
+    return L.depth[t] == 2 ? L.shape[t][0] * L.shape[t][1] : L.shape[t][0];
+}
+
+tmg_layout row_major(int64_t rows, int64_t cols)
+{
+    tmg_layout L;
+    std::memset(&L, 0, sizeof L);
+    L.depth[0] = L.depth[1] = 1;
+    L.shape[0][0] = rows;
+    L.shape[1][0] = cols;
+    L.stride[0][0] = cols;
+    L.stride[1][0] = 1;
+    L.shape[0][1] = L.shape[1][1] = 1;
+    return L;
+}
+
+// Checks depth, shapes and extents; strides >= 0 (> 0 when `output`);
+// the largest offset must fit in int64.
+tmg_status check_layout(const tmg_layout &L, int64_t rows, int64_t cols, bool output, const char *name)
+{
+    const int64_t ext[2] = {rows, cols};
+    __int128 max_off = 0;
+    for (int t = 0; t < 2; ++t) {
+        if (L.depth[t] != 1 && L.depth[t] != 2)
+            return fail(TMG_ERR_INVALID_ARG, "%s: mode %d depth %d (must be 1 or 2)", name, t, L.depth[t]);
+        for (int j = 0; j < L.depth[t]; ++j) {
+            if (L.shape[t][j] < 1)
+                return fail(TMG_ERR_INVALID_ARG, "%s: mode %d shape %lld < 1", name, t, (long long)L.shape[t][j]);
+            if (L.stride[t][j] < 0 || (output && L.stride[t][j] == 0 && L.shape[t][j] > 1))
+                return fail(TMG_ERR_INVALID_ARG, "%s: mode %d stride %lld not allowed", name, t,
+                            (long long)L.stride[t][j]);
+            max_off += static_cast<__int128>(L.shape[t][j] - 1) * L.stride[t][j];
+        }
+        if (mode_size(L, t) != ext[t])
+            return fail(TMG_ERR_INVALID_ARG, "%s: mode %d has size %lld, expected %lld", name, t,
+                        (long long)mode_size(L, t), (long long)ext[t]);
+    }
+    if (max_off > static_cast<__int128>(INT64_MAX / 2))
+        return fail(TMG_ERR_INVALID_ARG, "%s: offsets overflow int64", name);
+    return TMG_OK;
+}
+
+// Returns the row stride if L is (rows, cols):(ld, 1) with flat modes, else -1.
+int64_t row_stride_if_rowmajor(const tmg_layout &L, int64_t rows, int64_t cols)
+{
+    if (L.depth[0] != 1 || L.depth[1] != 1)
+        return -1;
+    if (cols > 1 && L.stride[1][0] != 1)
+        return -1;
+    if (rows == 1)
+        return L.stride[0][0] > 0 ? L.stride[0][0] : cols;
+    return L.stride[0][0] > 0 ? L.stride[0][0] : -1;
+}
+
+// Column stride if L is (rows, cols):(1, ld) with flat modes, else -1.
+int64_t col_stride_if_colmajor(const tmg_layout &L, int64_t rows, int64_t cols)
+{
+    if (L.depth[0] != 1 || L.depth[1] != 1)
+        return -1;
+    if (rows > 1 && L.stride[0][0] != 1)
+        return -1;
+    if (cols == 1)
+        return L.stride[1][0] > 0 ? L.stride[1][0] : rows;
+    return L.stride[1][0] > 0 ? L.stride[1][0] : -1;
+}
+
+DevLayout to_dev(const tmg_layout &L)
+{
+    DevLayout d;
+    std::memcpy(&d, &L, sizeof d);
+    static_assert(sizeof(DevLayout) == sizeof(tmg_layout), "layout struct mismatch");
+    return d;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// 2-D TMA descriptor over a row-major (rows, inner) matrix of `elem` bytes
+// with row stride `ld` elements: box {box_inner, box_rows}, 128-byte swizzle,
+// out-of-range elements read as zero.
+tmg_status encode_2d(CUtensorMap *map, CUtensorMapDataType dt, int elem, const void *base,
+                     int64_t inner, int64_t rows, int64_t ld, int box_inner, int box_rows)
+{
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * elem};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(TMG_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled failed (%d) for %lldx%lld ld=%lld", (int)r,
+                    (long long)rows, (long long)inner, (long long)ld);
+    return TMG_OK;
+}
+
+// TMA limits: 16-byte aligned base, row stride a multiple of 16 bytes and
+// below 2^40, dimensions below 2^31 (kernel coordinates are int32).
+bool tma_ok(const void *p, int64_t ld, int elem, int64_t rows, int64_t inner)
+{
+    return aligned16(p) && (ld * elem) % 16 == 0 && ld * elem < (int64_t(1) << 40) && rows < (int64_t(1) << 31) &&
+           inner < (int64_t(1) << 31) && ld >= 1;
+}
+
+// Tensor-core plan: operands after a possible swap, all K-major.
+struct TcPlan {
+    bool ok = false;
+    const void *A, *B;
+    int64_t M, N, lda, ldb, ldd;
+};
+
+TcPlan plan_tc(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, const tmg_layout &la,
+               const tmg_layout &lb, const tmg_layout &ld)
+{
+    TcPlan p;
+    const int64_t lda = row_stride_if_rowmajor(la, M, K);
+    const int64_t ldb = row_stride_if_rowmajor(lb, N, K);
+    if (lda < 0 || ldb < 0)
+        return p;
+    int64_t ldd = row_stride_if_rowmajor(ld, M, N);
+    if (ldd > 0 && (N == 1 || ldd >= N)) {
+        p = TcPlan{true, A, B, M, N, lda, ldb, ldd};
+    } else {
+        ldd = col_stride_if_colmajor(ld, M, N);
+        if (ldd > 0 && (M == 1 || ldd >= M))
+            p = TcPlan{true, B, A, N, M, ldb, lda, ldd};
+    }
+    if (!p.ok)
+        return p;
+    if (!tma_ok(p.A, p.lda, 2, p.M, K) || !tma_ok(p.B, p.ldb, 2, p.N, K) || p.M > INT32_MAX ||
+        p.N > INT32_MAX || K > INT32_MAX)
+        p.ok = false;
+    (void)D;
+    return p;
+}
+
+Scratch *skinny_scratch(int dev, cudaStream_t s, size_t pbytes, size_t cbytes, tmg_status *st)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    Scratch &sc = g_scratch[{dev, reinterpret_cast<uintptr_t>(s)}];
+    cudaError_t e;
+    if (sc.partials_bytes < pbytes) {
+        if (sc.partials)
+            cudaFree(sc.partials);
+        sc.partials = nullptr;
+        sc.partials_bytes = 0;
+        if ((e = cudaMalloc(&sc.partials, pbytes)) != cudaSuccess) {
+            *st = cuda_fail(e, "cudaMalloc(skinny partials)");
+            return nullptr;
+        }
+        sc.partials_bytes = pbytes;
+    }
+    if (sc.counters_bytes < cbytes) {
+        if (sc.counters)
+            cudaFree(sc.counters);
+        sc.counters = nullptr;
+        sc.counters_bytes = 0;
+        if ((e = cudaMalloc(&sc.counters, cbytes)) != cudaSuccess) {
+            *st = cuda_fail(e, "cudaMalloc(skinny counters)");
+            return nullptr;
+        }
+        if ((e = cudaMemsetAsync(sc.counters, 0, cbytes, s)) != cudaSuccess) {
+            *st = cuda_fail(e, "cudaMemsetAsync(skinny counters)");
+            return nullptr;
+        }
+        sc.counters_bytes = cbytes;
+    }
+    *st = TMG_OK;
+    return &sc;
+}
+
+tmg_status run_tc(const DeviceState &ds, const TcPlan &p, void *D, int64_t K, cudaStream_t s)
+{
+    TcArgs a;
+    std::memset(&a, 0, sizeof a);
+    const int tiles256 = static_cast<int>(((p.M + 127) / 128) * ((p.N + 255) / 256));
+    a.bn = tiles256 >= ds.num_sms ? 256 : 128;
+    tmg_status st;
+    if ((st = encode_2d(&a.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.A, K, p.M, p.lda, 64, 128)) != TMG_OK)
+        return st;
+    if ((st = encode_2d(&a.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.B, K, p.N, p.ldb, 64, a.bn)) != TMG_OK)
+        return st;
+    a.D = D;
+    a.ldd = p.ldd;
+    a.M = static_cast<int>(p.M);
+    a.N = static_cast<int>(p.N);
+    a.K = static_cast<int>(K);
+    cudaError_t e = launch_tc_bf16(a, ds.num_sms, err_ctx(ds), s);
+    return e == cudaSuccess ? TMG_OK : cuda_fail(e, "tc_bf16 launch");
+}
+
+tmg_status run_skinny(const DeviceState &ds, const TcPlan &p, void *D, int64_t K, cudaStream_t s)
+{
+    SkinnyTcArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.mp = static_cast<int>((p.M + 15) / 16 * 16);
+    tmg_status st;
+    if ((st = encode_2d(&a.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.B, K, p.N, p.ldb, 64, 128)) != TMG_OK)
+        return st;
+    if ((st = encode_2d(&a.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.A, K, p.M, p.lda, 64, a.mp)) != TMG_OK)
+        return st;
+    const int64_t units = ((p.N + 127) / 128) * ((K + 63) / 64);
+    a.grid = static_cast<int>(units < ds.num_sms ? units : ds.num_sms);
+    int dev = 0;
+    cudaGetDevice(&dev);
+    Scratch *sc = skinny_scratch(dev, s, skinny_partials_bytes(a.grid, a.mp), skinny_counters_bytes(p.N), &st);
+    if (!sc)
+        return st;
+    a.partials = sc->partials;
+    a.counters = sc->counters;
+    a.D = D;
+    a.ldd = p.ldd;
+    a.M = static_cast<int>(p.M);
+    a.N = static_cast<int>(p.N);
+    a.K = static_cast<int>(K);
+    cudaError_t e = launch_skinny_tc(a, err_ctx(ds), s);
+    return e == cudaSuccess ? TMG_OK : cuda_fail(e, "skinny_tc launch");
+}
+
+}  // namespace
+
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+namespace {
+
+__global__ void wait_probe_kernel(ErrCtx err)
+{
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0)
+        mbar_wait(&bar, 0, err, nullptr, kSiteProbe);   // nothing ever arrives
+}
+
+}  // namespace
+
+cudaError_t launch_wait_probe(const ErrCtx &err, cudaStream_t s)
+{
+    note_launch();
+    wait_probe_kernel<<<1, 32, 0, s>>>(err);
+    return cudaGetLastError();
+}
+
+}  // namespace tmg
+
+using namespace tmg;
+
+extern "C" {
+
+tmg_status tmg_gemm_ex(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K,
+                       tmg_dtype dtype, const tmg_layout *layoutA, const tmg_layout *layoutB,
+                       const tmg_layout *layoutD, tmg_path path, void *stream)
+{
+    t_last_error.clear();
+    if (dtype != TMG_F32 && dtype != TMG_BF16)
+        return fail(TMG_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+    if (path < TMG_PATH_AUTO || path > TMG_PATH_SKINNY_FFMA)
+        return fail(TMG_ERR_INVALID_ARG, "unknown path %d", (int)path);
+    if (M < 0 || N < 0 || K < 0)
+        return fail(TMG_ERR_INVALID_ARG, "negative extent M=%lld N=%lld K=%lld", (long long)M, (long long)N,
+                    (long long)K);
+    if (M == 0 || N == 0)
+        return TMG_OK;
+    if (!D || (K > 0 && (!A || !B)))
+        return fail(TMG_ERR_INVALID_ARG, "null operand pointer");
+    const tmg_layout la = layoutA ? *layoutA : row_major(M, K);
+    const tmg_layout lb = layoutB ? *layoutB : row_major(N, K);
+    const tmg_layout ld = layoutD ? *layoutD : row_major(M, N);
+    tmg_status st;
+    if (K > 0) {
+        if ((st = check_layout(la, M, K, false, "layoutA")) != TMG_OK)
+            return st;
+        if ((st = check_layout(lb, N, K, false, "layoutB")) != TMG_OK)
+            return st;
+    }
+    if ((st = check_layout(ld, M, N, true, "layoutD")) != TMG_OK)
+        return st;
+
+    DeviceState *ds = nullptr;
+    if ((st = device_state(&ds)) != TMG_OK)
+        return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int dt = dtype == TMG_F32 ? 0 : 1;
+
+    if (K == 0) {
+        cudaError_t e = launch_zero_fill(D, to_dev(ld), M, N, dt, s);
+        return e == cudaSuccess ? TMG_OK : cuda_fail(e, "zero_fill launch");
+    }
+
+    tmg_path use = path;
+    TcPlan plan;
+    if (dtype == TMG_BF16)
+        plan = plan_tc(A, B, D, M, N, K, la, lb, ld);
+    if (use == TMG_PATH_AUTO) {
+        if (dtype == TMG_F32 || !plan.ok)
+            use = TMG_PATH_FFMA;
+        else
+            use = plan.M <= 64 ? TMG_PATH_SKINNY : TMG_PATH_TC;
+    }
+
+    switch (use) {
+    case TMG_PATH_FFMA: {
+        FfmaArgs a;
+        a.A = A;
+        a.B = B;
+        a.D = D;
+        a.la = to_dev(la);
+        a.lb = to_dev(lb);
+        a.ld = to_dev(ld);
+        a.M = M;
+        a.N = N;
+        a.K = K;
+        cudaError_t e = launch_ffma(a, dt, ds->num_sms, err_ctx(*ds), s);
+        return e == cudaSuccess ? TMG_OK : cuda_fail(e, "ffma launch");
+    }
+    case TMG_PATH_TC:
+        if (dtype != TMG_BF16 || !plan.ok)
+            return fail(TMG_ERR_UNSUPPORTED,
+                        "tensor-core path needs bf16, K-major A and B (unit K stride, 16-byte aligned rows), "
+                        "and row- or column-major D");
+        return run_tc(*ds, plan, D, K, s);
+    case TMG_PATH_SKINNY:
+        if (dtype != TMG_BF16 || !plan.ok || plan.M > 64)
+            return fail(TMG_ERR_UNSUPPORTED,
+                        "skinny path needs bf16, K-major A and B, row- or column-major D, and at most 64 rows "
+                        "on the small side");
+        return run_skinny(*ds, plan, D, K, s);
+    case TMG_PATH_SKINNY_FFMA: {
+        if (dtype != TMG_BF16 || !plan.ok || plan.M > 16 || K % 8 != 0)
+            return fail(TMG_ERR_UNSUPPORTED,
+                        "skinny FFMA path needs bf16, K-major A and B, K %% 8 == 0 and at most 16 rows");
+        SkinnyFfmaArgs a{plan.A, plan.B, D, plan.M, plan.N, K, plan.lda, plan.ldb, plan.ldd};
+        cudaError_t e = launch_skinny_ffma(a, ds->num_sms, s);
+        return e == cudaSuccess ? TMG_OK : cuda_fail(e, "skinny_ffma launch");
+    }
+    default:
+        return fail(TMG_ERR_INVALID_ARG, "unknown path");
+    }
+}
+
+tmg_status tmg_gemm(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, tmg_dtype dtype,
+                    const tmg_layout *layoutA, const tmg_layout *layoutB, const tmg_layout *layoutD, void *stream)
+{
+    return tmg_gemm_ex(A, B, D, M, N, K, dtype, layoutA, layoutB, layoutD, TMG_PATH_AUTO, stream);
+}
+
+tmg_status tmg_gemm_mxfp4(const void *A, const void *B, const void *scaleA, const void *scaleB, void *D, int64_t M,
+                          int64_t N, int64_t K, void *stream)
+{
+    t_last_error.clear();
+    if (M < 0 || N < 0 || K < 0)
+        return fail(TMG_ERR_INVALID_ARG, "negative extent");
+    if (K % 32 != 0)
+        return fail(TMG_ERR_INVALID_ARG, "K=%lld is not a multiple of 32 (one e8m0 scale per 32 elements)",
+                    (long long)K);
+    if (M == 0 || N == 0)
+        return TMG_OK;
+    if (!D || (K > 0 && (!A || !B || !scaleA || !scaleB)))
+        return fail(TMG_ERR_INVALID_ARG, "null operand pointer");
+    DeviceState *ds = nullptr;
+    tmg_status st;
+    if ((st = device_state(&ds)) != TMG_OK)
+        return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (K == 0) {
+        cudaError_t e = launch_zero_fill(D, to_dev(row_major(M, N)), M, N, 1, s);
+        return e == cudaSuccess ? TMG_OK : cuda_fail(e, "zero_fill launch");
+    }
+    if (K % 256 != 0 || !tma_ok(A, K / 2, 1, M, K / 2) || !tma_ok(B, K / 2, 1, N, K / 2) || M > INT32_MAX ||
+        N > INT32_MAX || K > INT32_MAX)
+        return fail(TMG_ERR_UNSUPPORTED, "MXFP4 kernel needs K %% 256 == 0 and 16-byte aligned operand rows");
+    Mxfp4Args a;
+    std::memset(&a, 0, sizeof a);
+    if ((st = encode_2d(&a.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, K / 2, M, K / 2, 128, 128)) != TMG_OK)
+        return st;
+    if ((st = encode_2d(&a.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, K / 2, N, K / 2, 128, 128)) != TMG_OK)
+        return st;
+    a.sA = static_cast<const uint8_t *>(scaleA);
+    a.sB = static_cast<const uint8_t *>(scaleB);
+    a.D = D;
+    a.M = static_cast<int>(M);
+    a.N = static_cast<int>(N);
+    a.K = static_cast<int>(K);
+    cudaError_t e = launch_mxfp4(a, ds->num_sms, err_ctx(*ds), s);
+    return e == cudaSuccess ? TMG_OK : cuda_fail(e, "mxfp4 launch");
+}
+
+tmg_status tmg_check(void *stream)
+{
+    t_last_error.clear();
+    DeviceState *ds = nullptr;
+    tmg_status st;
+    if ((st = device_state(&ds)) != TMG_OK)
+        return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaStreamSynchronize");
+    if ((e = cudaGetLastError()) != cudaSuccess)
+        return cuda_fail(e, "pending CUDA error");
+    uint32_t w = 0;
+    if ((e = cudaMemcpy(&w, ds->err_word, sizeof w, cudaMemcpyDeviceToHost)) != cudaSuccess)
+        return cuda_fail(e, "reading the device error word");
+    if (w != 0) {
+        cudaMemset(ds->err_word, 0, sizeof w);
+        int dev = 0;
+        cudaGetDevice(&dev);
+        {
+            std::lock_guard<std::mutex> lk(g_mu);
+            for (auto &kv : g_scratch)
+                if (kv.first.first == dev && kv.second.counters)
+                    cudaMemset(kv.second.counters, 0, kv.second.counters_bytes);
+        }
+        cudaDeviceSynchronize();
+        return fail(TMG_ERR_TIMEOUT, "a kernel wait ran out of its budget (error word 0x%08x, site %u)", w,
+                    w & 0xFFu);
+    }
+    return TMG_OK;
+}
+
+const char *tmg_last_error(void) { return t_last_error.c_str(); }
+
+void tmg_set_wait_budget_ns(uint64_t ns) { g_budget_ns.store(ns ? ns : 1); }
+
+tmg_status tmg_debug_wait_timeout(uint64_t budget_ns, void *stream)
+{
+    t_last_error.clear();
+    DeviceState *ds = nullptr;
+    tmg_status st;
+    if ((st = device_state(&ds)) != TMG_OK)
+        return st;
+    ErrCtx ctx{ds->err_word, budget_ns};
+    cudaError_t e = launch_wait_probe(ctx, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TMG_OK : cuda_fail(e, "wait probe launch");
+}
+
+uint64_t tmg_launch_count(void) { return g_launches.load(); }
+
+int tmg_version(void) { return 100; }
+
+void tmg_shutdown(void)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    int cur = 0;
+    cudaGetDevice(&cur);
+    for (auto &kv : g_scratch) {
+        cudaSetDevice(kv.first.first);
+        if (kv.second.partials)
+            cudaFree(kv.second.partials);
+        if (kv.second.counters)
+            cudaFree(kv.second.counters);
+    }
+    g_scratch.clear();
+    cudaSetDevice(cur);
+}
+
+}  // extern "C"

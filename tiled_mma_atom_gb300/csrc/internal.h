@@ -1,0 +1,92 @@
+// internal.h — declarations shared by the library's translation units
+// (host launchers of each kernel family and the argument structs they take).
+// Not part of the public ABI; see include/tmg.h for that.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "device.cuh"
+
+namespace tmg {
+
+// A rank-2 layout as the kernels see it (same meaning as tmg_layout).
+struct DevLayout {
+    int32_t depth[2];
+    int64_t shape[2][2];
+    int64_t stride[2][2];
+};
+
+// ---------------------------------------------------------------- FFMA path
+struct FfmaArgs {
+    const void *A;
+    const void *B;
+    void *D;
+    DevLayout la, lb, ld;
+    int64_t M, N, K;
+};
+// dtype: 0 = f32, 1 = bf16.  Returns the launch status.
+cudaError_t launch_ffma(const FfmaArgs &a, int dtype, int num_sms, const ErrCtx &err,
+                        cudaStream_t s);
+
+// Skinny CUDA-core path: A (M,K) and B (N,K) bf16 K-major (row strides lda,
+// ldb), D (M,N) bf16 row-major with leading dimension ldd; M <= 16.
+struct SkinnyFfmaArgs {
+    const void *A;
+    const void *B;
+    void *D;
+    int64_t M, N, K, lda, ldb, ldd;
+};
+cudaError_t launch_skinny_ffma(const SkinnyFfmaArgs &a, int num_sms, cudaStream_t s);
+
+// Fill the (M,N) output with zeros through its layout (K == 0).
+cudaError_t launch_zero_fill(void *D, const DevLayout &ld, int64_t M, int64_t N, int dtype,
+                             cudaStream_t s);
+
+// ------------------------------------------------------ tcgen05 bf16 path
+struct TcArgs {
+    CUtensorMap tmA;   // A (M,K) bf16 K-major, box {64, 128}, 128B swizzle
+    CUtensorMap tmB;   // B (N,K) bf16 K-major, box {64, BN}, 128B swizzle
+    void *D;           // bf16 (M,N), row stride ldd elements, unit column stride
+    int64_t ldd;
+    int M, N, K;
+    int bn;            // 128 or 256
+};
+cudaError_t launch_tc_bf16(const TcArgs &a, int num_sms, const ErrCtx &err, cudaStream_t s);
+
+// ---------------------------------------------------- skinny swap-AB path
+struct SkinnyTcArgs {
+    CUtensorMap tmB;   // B (N,K) bf16 K-major, box {64, 128}  (MMA operand "A")
+    CUtensorMap tmA;   // A (M,K) bf16 K-major, box {64, MP}   (MMA operand "B")
+    void *D;           // bf16 (M,N) row stride ldd
+    int64_t ldd;
+    int M, N, K;
+    int mp;            // M rounded up to a multiple of 16, <= 64
+    float *partials;   // scratch: grid * 2 slots of 128 * mp fp32
+    uint32_t *counters;  // scratch: 4 per 128-row tile of B, zero on entry
+    int grid;          // number of CTAs (persistent)
+};
+cudaError_t launch_skinny_tc(const SkinnyTcArgs &a, const ErrCtx &err, cudaStream_t s);
+// Scratch bytes the skinny path needs for a given problem and grid.
+size_t skinny_partials_bytes(int grid, int mp);
+size_t skinny_counters_bytes(int64_t N);
+
+// ------------------------------------------------------------ MXFP4 path
+struct Mxfp4Args {
+    CUtensorMap tmA;    // A codes (M, K/2) u8, box {128, 128}, 128B swizzle
+    CUtensorMap tmB;    // B codes (N, K/2) u8, box {128, BN}
+    const uint8_t *sA;  // (M, K/32) e8m0
+    const uint8_t *sB;  // (N, K/32) e8m0
+    void *D;            // bf16 (M,N) row-major, ldd = N
+    int M, N, K;
+};
+cudaError_t launch_mxfp4(const Mxfp4Args &a, int num_sms, const ErrCtx &err, cudaStream_t s);
+
+// Probe kernel for the bounded wait (never signalled barrier).
+cudaError_t launch_wait_probe(const ErrCtx &err, cudaStream_t s);
+
+// Counts every kernel launch made through the launchers above.
+void note_launch();
+
+}  // namespace tmg

@@ -1,0 +1,317 @@
+// skinny.cu — decode-shaped GEMM (M <= 64, N and K large) on tcgen05 with
+// the operands swapped: Dᵀ (N x M) = B (N x K) · A (M x K)ᵀ.  The 128-row MMA
+// dimension runs over N (rows of B, the weight matrix streamed from HBM) and
+// the small M becomes the MMA's N (16..64), so no tensor-core lane idles on
+// padding rows.  The work is HBM-bound: the point is to keep enough TMA
+// loads of B in flight on every SM.
+//
+// The pages' preshuffle GEMM takes a runtime M so one kernel serves any
+// batch ("Kernel authoring guide", §11, note under the example); the skinny
+// case is the small-M end of that range.
+//
+// Work split (stream-K): the units are (128-row tile of B, 64-wide K block);
+// CTA c of G takes units [c·U/G, (c+1)·U/G), a contiguous run that covers
+// whole tiles and at most two partial ones.  A CTA that covers a whole tile
+// writes it directly.  Partial tiles write fp32 partial sums to scratch; the
+// last CTA to arrive at a tile (a counter per tile and TMEM lane quarter,
+// so each epilogue warp settles its own 32 rows) adds all partials in CTA
+// order — a fixed order, so results do not depend on timing — rounds to bf16,
+// writes D, and resets the counter to zero for the next call.
+//
+// Roles as in tc_bf16.cu: warp 0 TMA producer, warp 1 MMA issuer (and TMEM
+// owner), warps 2..5 epilogue; 8-stage ring of 16 KB (B) + mp·128 B (A).
+#include <cuda_bf16.h>
+
+#include "internal.h"
+
+namespace tmg {
+namespace {
+
+constexpr int kTileN = 128;        // rows of B per tile (MMA M)
+constexpr int kBK = 64;
+constexpr int kUmmaK = 16;
+constexpr int kStages = 8;
+constexpr int kMaxMP = 64;
+constexpr int kBBytes = kTileN * kBK * 2;        // 16 KB
+constexpr int kABytesMax = kMaxMP * kBK * 2;     // 8 KB
+constexpr int kStageBytes = kBBytes + kABytesMax;
+constexpr int kTmemCols = 2 * kMaxMP;            // 128
+constexpr int kSmem = kStages * kStageBytes + (2 * kStages + 4) * 8 + 32 + 1024;
+constexpr int kThreads = 192;
+
+__device__ __forceinline__ int64_t unit_start(int c, int64_t U, int G)
+{
+    return (static_cast<int64_t>(c) * U) / G;
+}
+
+// End (exclusive) of the K-block run that starts at kb0 with `left` units
+// of the CTA's range remaining.
+__device__ __forceinline__ int seg_end(int kb0, int KB, int64_t left)
+{
+    return left < static_cast<int64_t>(KB - kb0) ? kb0 + static_cast<int>(left) : KB;
+}
+
+// CTA whose run contains unit u.
+__device__ __forceinline__ int unit_owner(int64_t u, int64_t U, int G)
+{
+    return static_cast<int>(((u + 1) * G - 1) / U);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    skinny_tc_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmA,
+                     __nv_bfloat16 *__restrict__ D, int64_t ldd, int M, int N, int K, int mp,
+                     float *__restrict__ partials, uint32_t *__restrict__ counters, ErrCtx err)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * kStageBytes);
+    uint64_t *empty = full + kStages;
+    uint64_t *tfull = empty + kStages;
+    uint64_t *tempty = tfull + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int G = gridDim.x, c = blockIdx.x;
+    const int tiles = (N + kTileN - 1) / kTileN;
+    const int KB = (K + kBK - 1) / kBK;
+    const int64_t U = static_cast<int64_t>(tiles) * KB;
+    const int64_t u_begin = unit_start(c, U, G), u_end = unit_start(c + 1, U, G);
+    const uint32_t a_bytes = static_cast<uint32_t>(mp) * kBK * 2;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 4);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmA);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint64_t keep_a = policy_evict_last();   // A is re-read by every CTA
+            const uint64_t stream_b = policy_evict_first(); // B is read once
+            int stage = 0;
+            uint32_t phase = 0;
+            int64_t issued = 0;
+            bool ok = true;
+            for (int64_t u = u_begin; u < u_end && ok;) {
+                const int tile = static_cast<int>(u / KB);
+                const int kb0 = static_cast<int>(u % KB);
+                const int kb1 = seg_end(kb0, KB, u_end - u);
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, err, abort_flag, kSiteProducerEmpty)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *st = smem + stage * kStageBytes;
+                    mbar_arrive_expect_tx(&full[stage], kBBytes + a_bytes);
+                    tma_load_2d_hint(st, &tmB, &full[stage], kb * kBK, tile * kTileN, stream_b);
+                    tma_load_2d_hint(st + kBBytes, &tmA, &full[stage], kb * kBK, 0, keep_a);
+                    ++issued;
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                u += kb1 - kb0;
+            }
+            for (int i = 0; i < kStages && i < issued; ++i) {
+                int s = stage - 1 - i;
+                uint32_t ph = phase;
+                if (s < 0) {
+                    s += kStages;
+                    ph ^= 1u;
+                }
+                mbar_wait(&full[s], ph, err, nullptr, kSiteDrain);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16_f32(kTileN, mp);
+            int stage = 0;
+            uint32_t phase = 0;
+            int seg = 0;
+            bool ok = true;
+            for (int64_t u = u_begin; u < u_end && ok; ++seg) {
+                const int kb0 = static_cast<int>(u % KB);
+                const int kb1 = seg_end(kb0, KB, u_end - u);
+                const int acc = seg & 1;
+                if (!mbar_wait(&tempty[acc], ((seg >> 1) & 1) ^ 1u, err, abort_flag, kSiteMmaTmemEmpty))
+                    break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * kMaxMP;
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!mbar_wait(&full[stage], phase, err, abort_flag, kSiteMmaFull)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    uint8_t *st = smem + stage * kStageBytes;
+                    const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(st));            // MMA "A": B rows
+                    const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(st + kBBytes));  // MMA "B": A rows
+#pragma unroll
+                    for (int k = 0; k < kBK / kUmmaK; ++k) {
+                        const uint64_t koff = static_cast<uint64_t>((k * kUmmaK * 2) >> 4);
+                        mma_bf16(d_tmem, bdesc + koff, adesc + koff, idesc, (kb != kb0) || (k != 0));
+                    }
+                    mma_commit(&empty[stage]);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok)
+                    break;
+                mma_commit(&tfull[acc]);
+                u += kb1 - kb0;
+            }
+        }
+    } else {
+        // epilogue: thread owns B row n_local = 32 q + lane of the tile
+        const int q = warp & 3;
+        const int n_local = q * 32 + lane;
+        int seg = 0;
+        for (int64_t u = u_begin; u < u_end; ++seg) {
+            const int tile = static_cast<int>(u / KB);
+            const int kb0 = static_cast<int>(u % KB);
+            const int kb1 = seg_end(kb0, KB, u_end - u);
+            u += kb1 - kb0;
+            const int acc = seg & 1;
+            if (!mbar_wait(&tfull[acc], (seg >> 1) & 1, err, abort_flag, kSiteEpiTmemFull))
+                break;
+            tc_fence_after();
+            float v[kMaxMP];
+#pragma unroll
+            for (int ch = 0; ch < kMaxMP / 16; ++ch) {
+                if (ch * 16 < mp) {
+                    uint32_t r[16];
+                    tmem_ld16(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kMaxMP + ch * 16, r);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        v[ch * 16 + j] = __uint_as_float(r[j]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        v[ch * 16 + j] = 0.f;
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&tempty[acc]);
+
+            const int n = tile * kTileN + n_local;
+            if (kb0 == 0 && kb1 == KB) {
+                if (n < N) {
+#pragma unroll
+                    for (int m = 0; m < kMaxMP; ++m)
+                        if (m < M)
+                            D[static_cast<int64_t>(m) * ldd + n] = __float2bfloat16_rn(v[m]);
+                }
+                continue;
+            }
+            // Partial tile: publish this warp's 32 rows; the last warp to
+            // arrive for (tile, quarter) reduces them.  Warps never wait on
+            // one another, so an aborted warp cannot stall the others.
+            const int slot = 2 * c + (seg == 0 ? 0 : 1);
+            float *mine = partials + static_cast<int64_t>(slot) * mp * kTileN;
+#pragma unroll
+            for (int m = 0; m < kMaxMP; ++m)
+                if (m < mp)
+                    mine[m * kTileN + n_local] = v[m];
+            __threadfence();
+            __syncwarp();
+            const int64_t t_first = static_cast<int64_t>(tile) * KB;
+            const int c_first = unit_owner(t_first, U, G);
+            const int c_last = unit_owner(t_first + KB - 1, U, G);
+            uint32_t old = 0;
+            if (lane == 0)
+                old = atomicAdd(&counters[tile * 4 + q], 1u);
+            old = __shfl_sync(0xFFFFFFFFu, old, 0);
+            if (old == static_cast<uint32_t>(c_last - c_first)) {
+                __threadfence();
+                float sum[kMaxMP];
+#pragma unroll
+                for (int m = 0; m < kMaxMP; ++m)
+                    sum[m] = 0.f;
+                for (int cc = c_first; cc <= c_last; ++cc) {
+                    if (cc == c) {
+#pragma unroll
+                        for (int m = 0; m < kMaxMP; ++m)
+                            sum[m] += v[m];
+                    } else {
+                        const int first_tile = static_cast<int>(unit_start(cc, U, G) / KB);
+                        const int s2 = 2 * cc + (first_tile == tile ? 0 : 1);
+                        const float *p = partials + static_cast<int64_t>(s2) * mp * kTileN;
+#pragma unroll
+                        for (int m = 0; m < kMaxMP; ++m)
+                            if (m < mp)
+                                sum[m] += __ldcg(p + m * kTileN + n_local);
+                    }
+                }
+                if (n < N) {
+#pragma unroll
+                    for (int m = 0; m < kMaxMP; ++m)
+                        if (m < M)
+                            D[static_cast<int64_t>(m) * ldd + n] = __float2bfloat16_rn(sum[m]);
+                }
+                __syncwarp();
+                if (lane == 0)
+                    counters[tile * 4 + q] = 0;
+            }
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+}  // namespace
+
+size_t skinny_partials_bytes(int grid, int mp)
+{
+    return static_cast<size_t>(grid) * 2 * mp * kTileN * sizeof(float);
+}
+
+size_t skinny_counters_bytes(int64_t N)
+{
+    return static_cast<size_t>((N + kTileN - 1) / kTileN) * 4 * sizeof(uint32_t);
+}
+
+cudaError_t launch_skinny_tc(const SkinnyTcArgs &a, const ErrCtx &err, cudaStream_t s)
+{
+    static_assert(kSmem <= 232448, "shared memory budget");
+    cudaError_t e = cudaFuncSetAttribute(skinny_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess)
+        return e;
+    note_launch();
+    skinny_tc_kernel<<<a.grid, kThreads, kSmem, s>>>(a.tmB, a.tmA, static_cast<__nv_bfloat16 *>(a.D), a.ldd,
+                                                     a.M, a.N, a.K, a.mp, a.partials, a.counters, err);
+    return cudaGetLastError();
+}
+
+}  // namespace tmg
