@@ -1,0 +1,107 @@
+"""MXFP4 (e2m1 codes, one e8m0 scale per 32 K elements) tensor-core GEMM
+against the CPU oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests import parity
+from tiled_mma_atom_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module")
+def tmg():
+    import __graft_entry__
+    __graft_entry__.build()
+    import tiled_mma_atom_gb300 as t
+    return t
+
+
+def _run(tmg, A, B, sA, sB):
+    D = tmg.gemm_mxfp4(*(t.to(DEV) for t in (A, B, sA, sB)))
+    tmg.check()
+    return D
+
+
+def _ref(A, B, sA, sB, M, N, K):
+    return oracle.gemm_mxfp4(A.numpy(), B.numpy(), sA.numpy(), sB.numpy(), M, N, K)
+
+
+def _amax(X, S, K):
+    return float(np.abs(oracle.read_mxfp4(X.numpy(), S.numpy(), X.shape[0], K)).max())
+
+
+def test_mxfp4_unit_scales_bit_exact(tmg):
+    """Scales 2^0: every product is a multiple of 1/4 and |sum| < 2^15, so the
+    fp32 accumulation is exact and D must be RNE_bf16(exact)."""
+    M, N, K = 256, 384, 512
+    A = inputs.random_fp4_codes(M, K, 1)
+    B = inputs.random_fp4_codes(N, K, 2)
+    sA = torch.full((M, K // 32), 127, dtype=torch.uint8)
+    sB = torch.full((N, K // 32), 127, dtype=torch.uint8)
+    D = _run(tmg, A, B, sA, sB)
+    parity.check_exact_bf16(parity.bf16_bits(D), _ref(A, B, sA, sB, M, N, K))
+
+
+def test_mxfp4_per_block_scales_bit_exact(tmg):
+    """Scales 2^-1..2^1 varying per row and per 32-element block: products
+    are multiples of 2^-4 below 2^8 and sums stay below 2^17, so the result
+    is still exact — any misplaced scale (wrong row, block or half-word)
+    changes it."""
+    M, N, K = 384, 256, 1024
+    A = inputs.random_fp4_codes(M, K, 3)
+    B = inputs.random_fp4_codes(N, K, 4)
+    sA = inputs.random_e8m0(M, K, 5, lo=-1, hi=1)
+    sB = inputs.random_e8m0(N, K, 6, lo=-1, hi=1)
+    D = _run(tmg, A, B, sA, sB)
+    parity.check_exact_bf16(parity.bf16_bits(D), _ref(A, B, sA, sB, M, N, K))
+
+
+def test_mxfp4_one_hot_scale_locates_each_block(tmg):
+    """All codes 1.0; one row of A gets scale 2^1 on a single K block.  Each
+    output of that row must be K + 32, all others K."""
+    M, N, K = 128, 128, 512
+    one = torch.full((M, K), 2, dtype=torch.int32)            # code 2 = 1.0
+    A = inputs.pack_fp4(one)
+    B = inputs.pack_fp4(one[:N])
+    for row, blk in [(0, 0), (37, 5), (127, 15), (64, 9)]:
+        sA = torch.full((M, K // 32), 127, dtype=torch.uint8)
+        sB = torch.full((N, K // 32), 127, dtype=torch.uint8)
+        sA[row, blk] = 128
+        D = _run(tmg, A, B, sA, sB).float().cpu()
+        want = torch.full((M, N), float(K))
+        want[row, :] = K + 32
+        assert torch.equal(D, want), (row, blk)
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 200, 1024), (128, 640, 256)])
+def test_mxfp4_random_vs_oracle(tmg, M, N, K):
+    A = inputs.random_fp4_codes(M, K, 7)
+    B = inputs.random_fp4_codes(N, K, 8)
+    sA = inputs.random_e8m0(M, K, 9)
+    sB = inputs.random_e8m0(N, K, 10)
+    D = _run(tmg, A, B, sA, sB)
+    parity.check_bf16(D, _ref(A, B, sA, sB, M, N, K), K, _amax(A, sA, K), _amax(B, sB, K))
+
+
+def test_mxfp4_workload_8192_sampled(tmg):
+    """8192³ MXFP4 (codes U{0..15}, scale exponents U[-4,4]), the benchmark's
+    launch: sampled outputs vs the oracle."""
+    w = inputs.WORKLOADS["mxfp4_8192"]
+    A, B, sA, sB = inputs.make_inputs(w)
+    D = _run(tmg, A, B, sA, sB)
+    ms, ns = parity.sample_coords(w.M, w.N, 4000, seed=4)
+    ref = oracle.gemm_mxfp4_entries(A.numpy(), B.numpy(), sA.numpy(), sB.numpy(), w.K, ms, ns)
+    parity.check_bf16_values(parity.to_f64(D)[ms, ns], ref, w.K, 6.0 * 16, 6.0 * 16)
+
+
+def test_mxfp4_rejects_unaligned_k(tmg):
+    A = torch.zeros((4, 24), dtype=torch.uint8, device=DEV)       # K = 48
+    s = torch.zeros((4, 1), dtype=torch.uint8, device=DEV)
+    with pytest.raises(tmg.TmgError) as ei:
+        tmg.gemm_mxfp4(A, A, s, s)
+    assert ei.value.status == 1

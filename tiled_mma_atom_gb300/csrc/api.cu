@@ -497,6 +497,8 @@ tmg_status tmg_gemm_mxfp4(const void *A, const void *B, const void *scaleA, cons
     if (K % 256 != 0 || !tma_ok(A, K / 2, 1, M, K / 2) || !tma_ok(B, K / 2, 1, N, K / 2) || M > INT32_MAX ||
         N > INT32_MAX || K > INT32_MAX)
         return fail(TMG_ERR_UNSUPPORTED, "MXFP4 kernel needs K %% 256 == 0 and 16-byte aligned operand rows");
+    if ((reinterpret_cast<uintptr_t>(scaleA) & 7u) || (reinterpret_cast<uintptr_t>(scaleB) & 7u))
+        return fail(TMG_ERR_UNSUPPORTED, "MXFP4 scale arrays must be 8-byte aligned");
     Mxfp4Args a;
     std::memset(&a, 0, sizeof a);
     if ((st = encode_2d(&a.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, K / 2, M, K / 2, 128, 128)) != TMG_OK)

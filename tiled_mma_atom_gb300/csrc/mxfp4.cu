@@ -1,15 +1,344 @@
-// mxfp4.cu — placeholder until the block-scaled tcgen05 kernel lands.
+// mxfp4.cu — block-scaled FP4 GEMM on tcgen05:
+//   D (bf16, M x N) = A·Bᵀ, a(m,k) = e2m1(A code) * 2^(sA[m, k/32] - 127),
+//   b(n,k) likewise, fp32 accumulation in tensor memory.
+//
+// The FlyDSL pages express this product with scaled MFMA/WMMA atoms whose
+// E8M0 scales cover 32 consecutive K elements ("FlyDSL Kernel Authoring
+// Skill", §6, "gfx1250 WMMA (wave32)": MX-scaled WMMA with block_size=32;
+// "Kernel authoring guide", §4.3: the GFX950 scaled MFMA for MXFP4), and name
+// an MXFP4 preshuffle GEMM kernel.  On sm_103a the product is one
+// tcgen05.mma.kind::mxf4.block_scale.scale_vec::2X per 64 K elements
+// (two scales per row per instruction), reading the packed e2m1 codes from
+// 128-byte-swizzled shared memory and the scales from tensor memory.
+//
+// Per K block of 256 elements (128 bytes of codes per row):
+//   producer warp   lane 0: TMA of the A and B code tiles (128 x 128 bytes
+//                   each).  All 32 lanes: load the tile's e8m0 scales (8
+//                   per row) and store them to shared memory in the
+//                   32-row x 16-byte "scale chunk" order the tensor core
+//                   reads (row r0 holds, for rows r0, r0+32, r0+64, r0+96,
+//                   four consecutive K-block scales each), then a proxy fence
+//                   and a second arrive on the stage's `full` barrier.
+//   MMA lane        tcgen05.cp (32x128b, replicated to the four TMEM lane
+//                   quarters) copies each scale chunk to this stage's TMEM
+//                   scale columns; then four MMAs, each selecting its two
+//                   scales inside the 32-bit column with the SF id (0 or 2).
+//   epilogue warps  as in tc_bf16.cu.
+// Tile 128 x 128, double-buffered accumulator (256 TMEM columns) plus
+// 16 scale columns per stage.
+#include <cuda_bf16.h>
+
 #include "internal.h"
 
 namespace tmg {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBN = 128;
+constexpr int kBKBytes = 128;            // 256 e2m1 codes
+constexpr int kBK = 256;                 // elements
+constexpr int kStages = 6;
+constexpr int kTileBytes = kBM * kBKBytes;   // 16 KB (A and B alike)
+constexpr int kSfChunk = 512;            // 32 rows x 16 bytes
+constexpr int kSfBytes = 2 * kSfChunk;   // 8 scales per row, 128 rows
+constexpr int kThreads = 192;
+constexpr int kTmemCols = 512;
+constexpr int kAccCols = kBN;            // per buffer
+constexpr int kSfCol0 = 2 * kAccCols;    // first scale column
+constexpr int kSfColsPerStage = 16;      // A: 2 chunks x 4, B: 2 chunks x 4
+constexpr int kGroupM = 8;
+constexpr int kSmem = kStages * (2 * kTileBytes + 2 * kSfBytes) + (2 * kStages + 4) * 8 + 16 + 1024;
+
+// Shared-memory descriptor without swizzle (8-row x 16-byte core matrices,
+// stride byte offset 128 between consecutive 8-row groups), for tcgen05.cp.
+__device__ __forceinline__ uint64_t sdesc_noswizzle_rows16(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(128 >> 4) << 16;
+    d |= static_cast<uint64_t>(128 >> 4) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    return d;
+}
+
+// Instruction descriptor, kind::mxf4 block-scaled: B scale id (bits 4-5),
+// A format (7-9) = 1 (E2M1), B format (10-12) = 1 (E2M1), K-major A and B,
+// N >> 3 (17-22), scale type (23) = 1 (E8M0), M >> 4 (24-28), A scale id
+// (29-30), K size (31) = 0 (64 dense).
+__device__ __forceinline__ uint32_t idesc_mxf4(int M, int N, uint32_t sf_id)
+{
+    return (sf_id << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (1u << 23) | (static_cast<uint32_t>(M >> 4) << 24) | (sf_id << 29);
+}
+
+__device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                         uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X "
+        "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc)
+{
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int &tm, int &tn)
+{
+    const int group = kGroupM * tiles_n;
+    const int first_m = (t / group) * kGroupM;
+    const int gm = min(tiles_m - first_m, kGroupM);
+    const int r = t % group;
+    tm = first_m + r % gm;
+    tn = r / gm;
+}
+
+// Lane l stores the scales of rows l, l+32, l+64, l+96 (8 K-blocks each,
+// one 8-byte load per row) into the two 512-byte chunks of this K block.
+__device__ __forceinline__ void stage_scales(uint8_t *dst, const uint8_t *__restrict__ S, int rows,
+                                             int row0, int kb, int sf_per_row, int lane)
+{
+    uint32_t lo[4], hi[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = row0 + lane + 32 * i;
+        uint2 v = make_uint2(0u, 0u);
+        if (r < rows)
+            v = __ldg(reinterpret_cast<const uint2 *>(S + static_cast<int64_t>(r) * sf_per_row + kb * 8));
+        lo[i] = v.x;
+        hi[i] = v.y;
+    }
+    *reinterpret_cast<uint4 *>(dst + lane * 16) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    *reinterpret_cast<uint4 *>(dst + kSfChunk + lane * 16) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    mxfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                 const uint8_t *__restrict__ sA, const uint8_t *__restrict__ sB,
+                 __nv_bfloat16 *__restrict__ D, int M, int N, int K, int vec_ok, ErrCtx err)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    uint8_t *tA = smem;                                   // kStages x 16 KB
+    uint8_t *tB = tA + kStages * kTileBytes;              // kStages x 16 KB
+    uint8_t *sfA = tB + kStages * kTileBytes;             // kStages x 1 KB
+    uint8_t *sfB = sfA + kStages * kSfBytes;              // kStages x 1 KB
+    uint64_t *full = reinterpret_cast<uint64_t *>(sfB + kStages * kSfBytes);
+    uint64_t *empty = full + kStages;
+    uint64_t *tfull = empty + kStages;
+    uint64_t *tempty = tfull + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int tiles_m = (M + kBM - 1) / kBM, tiles_n = (N + kBN - 1) / kBN;
+    const int num_tiles = tiles_m * tiles_n;
+    const int num_kb = K / kBK;
+    const int sf_per_row = K / 32;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 2);     // TMA arrive (with bytes) + scales arrive
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 4);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------ producer warp
+        int stage = 0;
+        uint32_t phase = 0;
+        int64_t issued = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+            int tm, tn;
+            tile_coords(t, tiles_m, tiles_n, tm, tn);
+            for (int kb = 0; kb < num_kb; ++kb) {
+                // every lane waits (each then owns the acquire), the warp
+                // leaves together if any lane gave up
+                const bool got = mbar_wait(&empty[stage], phase ^ 1u, err, abort_flag, kSiteProducerEmpty);
+                if (!__all_sync(0xFFFFFFFFu, got)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&full[stage], 2 * kTileBytes);
+                    tma_load_2d(tA + stage * kTileBytes, &tmA, &full[stage], kb * kBKBytes, tm * kBM);
+                    tma_load_2d(tB + stage * kTileBytes, &tmB, &full[stage], kb * kBKBytes, tn * kBN);
+                }
+                stage_scales(sfA + stage * kSfBytes, sA, M, tm * kBM, kb, sf_per_row, lane);
+                stage_scales(sfB + stage * kSfBytes, sB, N, tn * kBN, kb, sf_per_row, lane);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&full[stage]);
+                ++issued;
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        if (lane == 0) {
+            for (int i = 0; i < kStages && i < issued; ++i) {
+                int s = stage - 1 - i;
+                uint32_t ph = phase;
+                if (s < 0) {
+                    s += kStages;
+                    ph ^= 1u;
+                }
+                mbar_wait(&full[s], ph, err, nullptr, kSiteDrain);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------ MMA issuer
+            int stage = 0;
+            uint32_t phase = 0;
+            int local = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++local) {
+                const int acc = local & 1;
+                if (!mbar_wait(&tempty[acc], ((local >> 1) & 1) ^ 1u, err, abort_flag, kSiteMmaTmemEmpty))
+                    break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * kAccCols;
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(&full[stage], phase, err, abort_flag, kSiteMmaFull)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sf_col = tmem_base + kSfCol0 + stage * kSfColsPerStage;
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        tmem_cp_32x128b_x4(sf_col + c * 4,
+                                           sdesc_noswizzle_rows16(smem_u32(sfA + stage * kSfBytes + c * kSfChunk)));
+                        tmem_cp_32x128b_x4(sf_col + 8 + c * 4,
+                                           sdesc_noswizzle_rows16(smem_u32(sfB + stage * kSfBytes + c * kSfChunk)));
+                    }
+                    const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(tA + stage * kTileBytes));
+                    const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(tB + stage * kTileBytes));
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        // 64 codes = 32 bytes per MMA; scales (k/2) chunk, id 0 or 2
+                        const uint64_t koff = static_cast<uint64_t>((k * 32) >> 4);
+                        const int c = k >> 1;
+                        const uint32_t id = (k & 1) ? 2u : 0u;
+                        mma_mxf4(d_tmem, adesc + koff, bdesc + koff, idesc_mxf4(kBM, kBN, id),
+                                 sf_col + c * 4, sf_col + 8 + c * 4, (kb | k) != 0);
+                    }
+                    mma_commit(&empty[stage]);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok)
+                    break;
+                mma_commit(&tfull[acc]);
+            }
+        }
+    } else {
+        // ---------------------------------------------------- epilogue
+        const int q = warp & 3;
+        int local = 0;
+        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++local) {
+            int tm, tn;
+            tile_coords(t, tiles_m, tiles_n, tm, tn);
+            const int acc = local & 1;
+            if (!mbar_wait(&tfull[acc], (local >> 1) & 1, err, abort_flag, kSiteEpiTmemFull))
+                break;
+            tc_fence_after();
+            const int row = tm * kBM + q * 32 + lane;
+            __nv_bfloat16 *drow = D + static_cast<int64_t>(row) * N;
+#pragma unroll 1
+            for (int c = 0; c < kBN / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccCols + c * 32, v);
+                const int col0 = tn * kBN + c * 32;
+                if (row < M) {
+                    if (vec_ok && col0 + 32 <= N) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(drow + col0);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            uint4 w;
+                            w.x = pack_bf16x2(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1]));
+                            w.y = pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3]));
+                            w.z = pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5]));
+                            w.w = pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7]));
+                            dst[j] = w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (col0 + j < N)
+                                drow[col0 + j] = __float2bfloat16_rn(__uint_as_float(v[j]));
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&tempty[acc]);
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+}  // namespace
 
 cudaError_t launch_mxfp4(const Mxfp4Args &a, int num_sms, const ErrCtx &err, cudaStream_t s)
 {
-    (void)a;
-    (void)num_sms;
-    (void)err;
-    (void)s;
-    return cudaErrorNotSupported;
+    static_assert(kSmem <= 232448, "shared memory budget");
+    static_assert(kSfCol0 + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
+    cudaError_t e = cudaFuncSetAttribute(mxfp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess)
+        return e;
+    const int tiles = ((a.M + kBM - 1) / kBM) * ((a.N + kBN - 1) / kBN);
+    const int grid = tiles < num_sms ? tiles : num_sms;
+    const int vec_ok = (a.N % 8 == 0) && ((reinterpret_cast<uintptr_t>(a.D) & 15u) == 0);
+    note_launch();
+    mxfp4_kernel<<<grid, kThreads, kSmem, s>>>(a.tmA, a.tmB, a.sA, a.sB, static_cast<__nv_bfloat16 *>(a.D),
+                                                a.M, a.N, a.K, vec_ok, err);
+    return cudaGetLastError();
 }
 
 }  // namespace tmg
