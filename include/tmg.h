@@ -123,6 +123,35 @@ tmg_status tmg_gemm_mxfp4(const void *A, const void *B, const void *scaleA,
                           const void *scaleB, void *D, int64_t M, int64_t N,
                           int64_t K, void *stream);
 
+/* Skinny bf16 GEMM that allocates nothing.  The FlyDSL pages have no
+ * counterpart: this is a library-level variant for callers that may not
+ * allocate device memory at call time — e.g. a latency-critical loop that
+ * must not call cudaMalloc/cudaFree after start-up (both can synchronise the
+ * device), or a plug-in whose host owns all device memory through its own
+ * pool and passes in only the operands.
+ *
+ * Computes the same D = A·Bᵀ as tmg_gemm on the skinny tensor-core path:
+ *   A  device, bf16 (M, K) row-major, row stride lda (elements, >= K)
+ *   B  device, bf16 (N, K) row-major, row stride ldb (>= K)
+ *   D  device, bf16 (M, N) row-major, row stride ldd (>= N)
+ * Limits: M <= 64 and N <= 524288 (else TMG_ERR_INVALID_ARG); A and B rows
+ * 16-byte aligned (else TMG_ERR_UNSUPPORTED).
+ *
+ * Its split-K partial sums and tile counters live in one 8 MiB array in the
+ * library's static device memory, which every GPU that loads the library
+ * holds until the process exits.  No call allocates or frees memory.  The
+ * first call on a device looks up that array's device address (once per
+ * device, with the device current); make that first call before any stream
+ * capture.  Every call shares the one array and it keeps the last call's
+ * contents: each call clears the counters it uses with an asynchronous
+ * memset on `stream` before its kernel.  Calls whose GPU work overlaps (on
+ * different streams, or from different threads) race on the array and give
+ * wrong results: serialise them. */
+tmg_status tmg_gemm_skinny_noalloc(const void *A, const void *B, void *D,
+                                   int64_t M, int64_t N, int64_t K,
+                                   int64_t lda, int64_t ldb, int64_t ldd,
+                                   void *stream);
+
 /* Synchronise `stream`, then report: TMG_ERR_CUDA for a sticky or pending
  * CUDA error, TMG_ERR_TIMEOUT if a kernel's bounded wait ran out since the
  * last check (the device error word is cleared and the skinny-path scratch

@@ -18,7 +18,7 @@ F32, BF16 = 0, 1
 PATHS = {"auto": 0, "ffma": 1, "tc": 2, "skinny": 3, "skinny_ffma": 4}
 
 # Every function include/tmg.h declares.
-EXPORTS = ("tmg_gemm", "tmg_gemm_ex", "tmg_gemm_mxfp4", "tmg_check", "tmg_last_error",
+EXPORTS = ("tmg_gemm", "tmg_gemm_ex", "tmg_gemm_mxfp4", "tmg_gemm_skinny_noalloc", "tmg_check", "tmg_last_error",
            "tmg_set_wait_budget_ns", "tmg_debug_wait_timeout", "tmg_launch_count",
            "tmg_version", "tmg_shutdown")
 
@@ -78,6 +78,8 @@ def lib():
     L.tmg_gemm_ex.restype = ctypes.c_int
     L.tmg_gemm_mxfp4.argtypes = [P, P, P, P, P, I64, I64, I64, P]
     L.tmg_gemm_mxfp4.restype = ctypes.c_int
+    L.tmg_gemm_skinny_noalloc.argtypes = [P, P, P, I64, I64, I64, I64, I64, I64, P]
+    L.tmg_gemm_skinny_noalloc.restype = ctypes.c_int
     L.tmg_check.argtypes = [P]
     L.tmg_check.restype = ctypes.c_int
     L.tmg_last_error.argtypes = []

@@ -515,6 +515,72 @@ tmg_status tmg_gemm_mxfp4(const void *A, const void *B, const void *scaleA, cons
     return e == cudaSuccess ? TMG_OK : cuda_fail(e, "mxfp4 launch");
 }
 
+tmg_status tmg_gemm_skinny_noalloc(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K,
+                                   int64_t lda, int64_t ldb, int64_t ldd, void *stream)
+{
+    t_last_error.clear();
+    if (M < 0 || N < 0 || K < 0)
+        return fail(TMG_ERR_INVALID_ARG, "negative extent M=%lld N=%lld K=%lld", (long long)M, (long long)N,
+                    (long long)K);
+    if (M == 0 || N == 0)
+        return TMG_OK;
+    if (!D || (K > 0 && (!A || !B)))
+        return fail(TMG_ERR_INVALID_ARG, "null operand pointer");
+    if (M > 64)
+        return fail(TMG_ERR_INVALID_ARG, "M=%lld exceeds the fixed-scratch skinny limit of 64 rows", (long long)M);
+    if (ldd < N || (K > 0 && (lda < K || ldb < K)))
+        return fail(TMG_ERR_INVALID_ARG, "leading dimension smaller than the row length");
+    DeviceState *ds = nullptr;
+    tmg_status st;
+    if ((st = device_state(&ds)) != TMG_OK)
+        return st;
+    FixedScratch fs;
+    cudaError_t e = skinny_fixed_scratch(&fs);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetSymbolAddress(fixed skinny scratch)");
+    const int64_t tiles = (N + 127) / 128;
+    if (tiles > fs.max_tiles)
+        return fail(TMG_ERR_INVALID_ARG, "N=%lld exceeds the fixed-scratch skinny limit of %lld", (long long)N,
+                    (long long)fs.max_tiles * 128);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (K == 0) {
+        tmg_layout ld = row_major(M, N);
+        ld.stride[0][0] = ldd;
+        e = launch_zero_fill(D, to_dev(ld), M, N, 1, s);
+        return e == cudaSuccess ? TMG_OK : cuda_fail(e, "zero_fill launch");
+    }
+    if (!tma_ok(A, lda, 2, M, K) || !tma_ok(B, ldb, 2, N, K) || N > INT32_MAX || K > INT32_MAX)
+        return fail(TMG_ERR_UNSUPPORTED, "operands need 16-byte aligned rows (row strides a multiple of 8)");
+    SkinnyTcArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.mp = static_cast<int>((M + 15) / 16 * 16);
+    if ((st = encode_2d(&a.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, K, N, ldb, 64, 128)) != TMG_OK)
+        return st;
+    if ((st = encode_2d(&a.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, K, M, lda, 64, a.mp)) != TMG_OK)
+        return st;
+    const int64_t units = tiles * ((K + 63) / 64);
+    const int64_t cap = static_cast<int64_t>(fs.partial_bytes / skinny_partials_bytes(1, a.mp));
+    int64_t grid = ds->num_sms;
+    if (units < grid)
+        grid = units;
+    if (cap < grid)
+        grid = cap;
+    a.grid = static_cast<int>(grid);
+    a.partials = fs.partials;
+    a.counters = fs.counters;
+    a.D = D;
+    a.ldd = ldd;
+    a.M = static_cast<int>(M);
+    a.N = static_cast<int>(N);
+    a.K = static_cast<int>(K);
+    // The array keeps the previous call's contents: the tile counters must
+    // start at zero, the partial sums are always written before being read.
+    if ((e = cudaMemsetAsync(fs.counters, 0, static_cast<size_t>(tiles) * 4 * sizeof(uint32_t), s)) != cudaSuccess)
+        return cuda_fail(e, "cudaMemsetAsync(fixed skinny counters)");
+    e = launch_skinny_tc(a, err_ctx(*ds), s);
+    return e == cudaSuccess ? TMG_OK : cuda_fail(e, "skinny_tc launch (fixed scratch)");
+}
+
 tmg_status tmg_check(void *stream)
 {
     t_last_error.clear();

@@ -68,6 +68,17 @@ struct SkinnyTcArgs {
     int grid;          // number of CTAs (persistent)
 };
 cudaError_t launch_skinny_tc(const SkinnyTcArgs &a, const ErrCtx &err, cudaStream_t s);
+// The skinny kernel's fixed scratch in static device memory (for the entry
+// point that allocates nothing).  First call per device looks up its device
+// address with cudaGetSymbolAddress.
+struct FixedScratch {
+    float *partials;
+    size_t partial_bytes;
+    uint32_t *counters;
+    size_t counter_bytes;
+    int max_tiles;
+};
+cudaError_t skinny_fixed_scratch(FixedScratch *out);
 // Scratch bytes the skinny path needs for a given problem and grid.
 size_t skinny_partials_bytes(int grid, int mp);
 size_t skinny_counters_bytes(int64_t N);

@@ -22,6 +22,9 @@
 // owner), warps 2..5 epilogue; 8-stage ring of 16 KB (B) + mp·128 B (A).
 #include <cuda_bf16.h>
 
+#include <map>
+#include <mutex>
+
 #include "internal.h"
 
 namespace tmg {
@@ -312,6 +315,61 @@ cudaError_t launch_skinny_tc(const SkinnyTcArgs &a, const ErrCtx &err, cudaStrea
     skinny_tc_kernel<<<a.grid, kThreads, kSmem, s>>>(a.tmB, a.tmA, static_cast<__nv_bfloat16 *>(a.D), a.ldd,
                                                      a.M, a.N, a.K, a.mp, a.partials, a.counters, err);
     return cudaGetLastError();
+}
+
+}  // namespace tmg
+
+namespace tmg {
+
+// ---------------------------------------------------------------------------
+// Fixed-scratch variant.
+//
+// Some callers cannot allocate device memory when they call the GEMM: for
+// example a latency-critical loop that must not call cudaMalloc/cudaFree
+// after start-up (both can synchronise the whole device), or a plug-in whose
+// host application owns all device memory through its own pool and gives
+// the plug-in only the input and output buffers.  For them the skinny kernel
+// can take its split-K partial sums and per-tile counters from one array in
+// static device memory instead of from scratch that the ordinary call
+// allocates per stream.  The array is part of the library's device image:
+// every GPU that loads the library holds it until the process exits.
+namespace {
+
+constexpr size_t kFixedScratchBytes = size_t(8) << 20;                      // 8 MiB
+constexpr int kFixedMaxTiles = 4096;                                          // N <= 524288
+constexpr size_t kFixedCounterBytes = size_t(kFixedMaxTiles) * 4 * sizeof(uint32_t);  // 64 KiB
+
+static __device__ __align__(256) unsigned char g_fixed_scratch[kFixedScratchBytes];
+
+std::mutex g_fixed_mu;
+std::map<int, unsigned char *> g_fixed_addr;    // device ordinal -> device address
+
+}  // namespace
+
+cudaError_t skinny_fixed_scratch(FixedScratch *out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    std::lock_guard<std::mutex> lk(g_fixed_mu);
+    auto it = g_fixed_addr.find(dev);
+    if (it == g_fixed_addr.end()) {
+        // In host code `g_fixed_scratch` names a host-side stand-in, not device
+        // memory: the kernel must get the address the runtime reports for the
+        // current device.
+        unsigned char *p = nullptr;
+        e = cudaGetSymbolAddress(reinterpret_cast<void **>(&p), g_fixed_scratch);
+        if (e != cudaSuccess)
+            return e;
+        it = g_fixed_addr.emplace(dev, p).first;
+    }
+    out->counters = reinterpret_cast<uint32_t *>(it->second);
+    out->counter_bytes = kFixedCounterBytes;
+    out->partials = reinterpret_cast<float *>(it->second + kFixedCounterBytes);
+    out->partial_bytes = kFixedScratchBytes - kFixedCounterBytes;
+    out->max_tiles = kFixedMaxTiles;
+    return cudaSuccess;
 }
 
 }  // namespace tmg
