@@ -29,8 +29,9 @@
  * Ownership: the caller owns every buffer passed in (device memory, e.g.
  * torch tensors).  The library never frees or retains them beyond the
  * call.  The library owns only: a device error word (static device memory)
- * and per-(device, stream) split-K scratch for the skinny path, grown on
- * demand and released by tmg_shutdown().
+ * and per-(device, stream) scratch — split-K partials for the skinny path,
+ * relaid scales for the MXFP4 path — grown on demand and released by
+ * tmg_shutdown().
  *
  * Errors: nothing is allowed to fault.  Bad arguments return
  * TMG_ERR_INVALID_ARG, valid but unhandled requests TMG_ERR_UNSUPPORTED,

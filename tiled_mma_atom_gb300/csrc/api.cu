@@ -50,6 +50,8 @@ struct Scratch {
     size_t partials_bytes = 0;
     uint32_t *counters = nullptr;
     size_t counters_bytes = 0;
+    uint8_t *mx_scales = nullptr;      // MXFP4 scales in chunk order
+    size_t mx_scales_bytes = 0;
 };
 std::map<std::pair<int, uintptr_t>, Scratch> g_scratch;
 
@@ -294,6 +296,27 @@ Scratch *skinny_scratch(int dev, cudaStream_t s, size_t pbytes, size_t cbytes, t
     return &sc;
 }
 
+// Per-(device, stream) buffer for the MXFP4 scale relayout, grown on demand.
+uint8_t *mx_scale_scratch(int dev, cudaStream_t s, size_t bytes, tmg_status *st)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    Scratch &sc = g_scratch[{dev, reinterpret_cast<uintptr_t>(s)}];
+    if (sc.mx_scales_bytes < bytes) {
+        if (sc.mx_scales)
+            cudaFree(sc.mx_scales);
+        sc.mx_scales = nullptr;
+        sc.mx_scales_bytes = 0;
+        cudaError_t e = cudaMalloc(&sc.mx_scales, bytes);
+        if (e != cudaSuccess) {
+            *st = cuda_fail(e, "cudaMalloc(MXFP4 scale relayout)");
+            return nullptr;
+        }
+        sc.mx_scales_bytes = bytes;
+    }
+    *st = TMG_OK;
+    return sc.mx_scales;
+}
+
 tmg_status run_tc(const DeviceState &ds, const TcPlan &p, void *D, int64_t K, cudaStream_t s)
 {
     TcArgs a;
@@ -507,6 +530,16 @@ tmg_status tmg_gemm_mxfp4(const void *A, const void *B, const void *scaleA, cons
         return st;
     a.sA = static_cast<const uint8_t *>(scaleA);
     a.sB = static_cast<const uint8_t *>(scaleB);
+    {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        const size_t ra = mxfp4_relaid_scale_bytes(M, K), rb = mxfp4_relaid_scale_bytes(N, K);
+        uint8_t *buf = mx_scale_scratch(dev, s, ra + rb, &st);
+        if (!buf)
+            return st;
+        a.relA = buf;
+        a.relB = buf + ra;
+    }
     a.D = D;
     a.M = static_cast<int>(M);
     a.N = static_cast<int>(N);
@@ -645,6 +678,8 @@ void tmg_shutdown(void)
             cudaFree(kv.second.partials);
         if (kv.second.counters)
             cudaFree(kv.second.counters);
+        if (kv.second.mx_scales)
+            cudaFree(kv.second.mx_scales);
     }
     g_scratch.clear();
     cudaSetDevice(cur);

@@ -89,10 +89,14 @@ struct Mxfp4Args {
     CUtensorMap tmB;    // B codes (N, K/2) u8, box {128, BN}
     const uint8_t *sA;  // (M, K/32) e8m0
     const uint8_t *sB;  // (N, K/32) e8m0
+    uint8_t *relA;      // scratch: sA relaid in the tensor core's chunk order
+    uint8_t *relB;      // scratch: sB likewise
     void *D;            // bf16 (M,N) row-major, ldd = N
     int M, N, K;
 };
+// Two launches: the scale relayout pre-pass, then the GEMM.
 cudaError_t launch_mxfp4(const Mxfp4Args &a, int num_sms, const ErrCtx &err, cudaStream_t s);
+size_t mxfp4_relaid_scale_bytes(int64_t rows, int64_t K);
 
 // Probe kernel for the bounded wait (never signalled barrier).
 cudaError_t launch_wait_probe(const ErrCtx &err, cudaStream_t s);

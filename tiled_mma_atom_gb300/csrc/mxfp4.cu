@@ -11,14 +11,15 @@
 // (two scales per row per instruction), reading the packed e2m1 codes from
 // 128-byte-swizzled shared memory and the scales from tensor memory.
 //
-// Per K block of 256 elements (128 bytes of codes per row):
-//   producer warp   lane 0: TMA of the A and B code tiles (128 x 128 bytes
-//                   each).  All 32 lanes: load the tile's e8m0 scales (8
-//                   per row) and store them to shared memory in the
-//                   32-row x 16-byte "scale chunk" order the tensor core
-//                   reads (row r0 holds, for rows r0, r0+32, r0+64, r0+96,
-//                   four consecutive K-block scales each), then a proxy fence
-//                   and a second arrive on the stage's `full` barrier.
+// Per call, a small pre-pass (mx_scale_relayout_kernel) rewrites both
+// scale arrays into the order the tensor core reads: for each 128-row block
+// and each K block of 256 elements, 1 KB = two 512-byte chunks, chunk c
+// holding K-blocks 4c..4c+3; inside a chunk, 16-byte line r0 (0..31) holds
+// the four scales of rows r0, r0+32, r0+64, r0+96 for those K-blocks.
+// Per K block of the main loop (128 bytes of codes per row):
+//   producer lane   TMA of the A and B code tiles (128 x 128 bytes each)
+//                   and two 1 KB bulk copies of the relaid scales, all
+//                   completing on the stage's `full` barrier.
 //   MMA lane        tcgen05.cp (32x128b, replicated to the four TMEM lane
 //                   quarters) copies each scale chunk to this stage's TMEM
 //                   scale columns; then four MMAs, each selecting its two
@@ -90,11 +91,6 @@ __device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdes
                  : "memory");
 }
 
-__device__ __forceinline__ void fence_proxy_async_smem()
-{
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int &tm, int &tn)
 {
     const int group = kGroupM * tiles_n;
@@ -105,28 +101,37 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
     tn = r / gm;
 }
 
-// Lane l stores the scales of rows l, l+32, l+64, l+96 (8 K-blocks each,
-// one 8-byte load per row) into the two 512-byte chunks of this K block.
-__device__ __forceinline__ void stage_scales(uint8_t *dst, const uint8_t *__restrict__ S, int rows,
-                                             int row0, int kb, int sf_per_row, int lane)
+// Relayout pass: (rows, K/32) e8m0 row-major -> chunk order (see top).
+// One thread per 16-byte output line; blockIdx.y picks the operand.
+__global__ void mx_scale_relayout_kernel(const uint8_t *__restrict__ SA, int rowsA, uint8_t *__restrict__ outA,
+                                         const uint8_t *__restrict__ SB, int rowsB, uint8_t *__restrict__ outB,
+                                         int sf_per_row, int num_kb)
 {
-    uint32_t lo[4], hi[4];
+    const bool isB = blockIdx.y == 1;
+    const uint8_t *S = isB ? SB : SA;
+    const int rows = isB ? rowsB : rowsA;
+    uint8_t *out = isB ? outB : outA;
+    const int64_t lines = static_cast<int64_t>((rows + kBM - 1) / kBM) * num_kb * 64;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < lines;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int r0 = static_cast<int>(i & 31);
+        const int c = static_cast<int>((i >> 5) & 1);
+        const int64_t blk = i >> 6;                  // row block * num_kb + K block
+        const int kb = static_cast<int>(blk % num_kb);
+        const int64_t rb = blk / num_kb;
+        uint32_t w[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int r = row0 + lane + 32 * i;
-        uint2 v = make_uint2(0u, 0u);
-        if (r < rows)
-            v = __ldg(reinterpret_cast<const uint2 *>(S + static_cast<int64_t>(r) * sf_per_row + kb * 8));
-        lo[i] = v.x;
-        hi[i] = v.y;
+        for (int g = 0; g < 4; ++g) {
+            const int64_t row = rb * kBM + g * 32 + r0;
+            w[g] = row < rows ? __ldg(reinterpret_cast<const uint32_t *>(S + row * sf_per_row + kb * 8 + c * 4)) : 0u;
+        }
+        *reinterpret_cast<uint4 *>(out + i * 16) = make_uint4(w[0], w[1], w[2], w[3]);
     }
-    *reinterpret_cast<uint4 *>(dst + lane * 16) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-    *reinterpret_cast<uint4 *>(dst + kSfChunk + lane * 16) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
     mxfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                 const uint8_t *__restrict__ sA, const uint8_t *__restrict__ sB,
+                 const uint8_t *__restrict__ relA, const uint8_t *__restrict__ relB,
                  __nv_bfloat16 *__restrict__ D, int M, int N, int K, int vec_ok, ErrCtx err)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -147,11 +152,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tiles_m = (M + kBM - 1) / kBM, tiles_n = (N + kBN - 1) / kBN;
     const int num_tiles = tiles_m * tiles_n;
     const int num_kb = K / kBK;
-    const int sf_per_row = K / 32;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full[s], 2);     // TMA arrive (with bytes) + scales arrive
+            mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -175,41 +179,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem_base = *tmem_slot;
 
     if (warp == 0) {
-        // ------------------------------------------------ producer warp
-        int stage = 0;
-        uint32_t phase = 0;
-        int64_t issued = 0;
-        bool ok = true;
-        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-            int tm, tn;
-            tile_coords(t, tiles_m, tiles_n, tm, tn);
-            for (int kb = 0; kb < num_kb; ++kb) {
-                // every lane waits (each then owns the acquire), the warp
-                // leaves together if any lane gave up
-                const bool got = mbar_wait(&empty[stage], phase ^ 1u, err, abort_flag, kSiteProducerEmpty);
-                if (!__all_sync(0xFFFFFFFFu, got)) {
-                    ok = false;
-                    break;
-                }
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(&full[stage], 2 * kTileBytes);
+        if (lane == 0) {
+            // ---------------------------------------------- producer lane
+            int stage = 0;
+            uint32_t phase = 0;
+            int64_t issued = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                int tm, tn;
+                tile_coords(t, tiles_m, tiles_n, tm, tn);
+                const uint8_t *sfa_src = relA + static_cast<int64_t>(tm) * num_kb * kSfBytes;
+                const uint8_t *sfb_src = relB + static_cast<int64_t>(tn) * num_kb * kSfBytes;
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, err, abort_flag, kSiteProducerEmpty)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[stage], 2 * kTileBytes + 2 * kSfBytes);
                     tma_load_2d(tA + stage * kTileBytes, &tmA, &full[stage], kb * kBKBytes, tm * kBM);
                     tma_load_2d(tB + stage * kTileBytes, &tmB, &full[stage], kb * kBKBytes, tn * kBN);
-                }
-                stage_scales(sfA + stage * kSfBytes, sA, M, tm * kBM, kb, sf_per_row, lane);
-                stage_scales(sfB + stage * kSfBytes, sB, N, tn * kBN, kb, sf_per_row, lane);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&full[stage]);
-                ++issued;
-                if (++stage == kStages) {
-                    stage = 0;
-                    phase ^= 1u;
+                    bulk_load(sfA + stage * kSfBytes, sfa_src + kb * kSfBytes, kSfBytes, &full[stage]);
+                    bulk_load(sfB + stage * kSfBytes, sfb_src + kb * kSfBytes, kSfBytes, &full[stage]);
+                    ++issued;
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
                 }
             }
-        }
-        if (lane == 0) {
             for (int i = 0; i < kStages && i < issued; ++i) {
                 int s = stage - 1 - i;
                 uint32_t ph = phase;
@@ -325,6 +322,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
+size_t mxfp4_relaid_scale_bytes(int64_t rows, int64_t K)
+{
+    return static_cast<size_t>((rows + kBM - 1) / kBM) * static_cast<size_t>(K / kBK) * kSfBytes;
+}
+
 cudaError_t launch_mxfp4(const Mxfp4Args &a, int num_sms, const ErrCtx &err, cudaStream_t s)
 {
     static_assert(kSmem <= 232448, "shared memory budget");
@@ -332,11 +334,21 @@ cudaError_t launch_mxfp4(const Mxfp4Args &a, int num_sms, const ErrCtx &err, cud
     cudaError_t e = cudaFuncSetAttribute(mxfp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess)
         return e;
+    const int num_kb = a.K / kBK;
+    const int64_t lines = static_cast<int64_t>((a.M > a.N ? a.M : a.N) + kBM - 1) / kBM * num_kb * 64;
+    int64_t blocks = (lines + 255) / 256;
+    if (blocks > 4L * num_sms)
+        blocks = 4L * num_sms;
+    note_launch();
+    mx_scale_relayout_kernel<<<dim3(static_cast<unsigned>(blocks), 2), 256, 0, s>>>(
+        a.sA, a.M, a.relA, a.sB, a.N, a.relB, a.K / 32, num_kb);
+    if ((e = cudaGetLastError()) != cudaSuccess)
+        return e;
     const int tiles = ((a.M + kBM - 1) / kBM) * ((a.N + kBN - 1) / kBN);
     const int grid = tiles < num_sms ? tiles : num_sms;
     const int vec_ok = (a.N % 8 == 0) && ((reinterpret_cast<uintptr_t>(a.D) & 15u) == 0);
     note_launch();
-    mxfp4_kernel<<<grid, kThreads, kSmem, s>>>(a.tmA, a.tmB, a.sA, a.sB, static_cast<__nv_bfloat16 *>(a.D),
+    mxfp4_kernel<<<grid, kThreads, kSmem, s>>>(a.tmA, a.tmB, a.relA, a.relB, static_cast<__nv_bfloat16 *>(a.D),
                                                 a.M, a.N, a.K, vec_ok, err);
     return cudaGetLastError();
 }
