@@ -41,7 +41,7 @@ FP4_OVER_BF16 = 13.5 / 2.25
 FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 L2_FLUSH_BYTES = 512 << 20
 KERNEL_OF = {"fp32_128": "ffma_gemm_kernel", "bf16_1024": "tc_bf16_kernel",
-             "bf16_4096": "tc_bf16_kernel", "skinny_16x28672x8192": "skinny_tc_kernel",
+             "bf16_4096": "tc2_bf16_kernel", "skinny_16x28672x8192": "skinny_tc_kernel",
              "mxfp4_8192": "mxfp4_kernel"}
 
 

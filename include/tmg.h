@@ -65,14 +65,18 @@ typedef enum { TMG_F32 = 0, TMG_BF16 = 1 } tmg_dtype;
  *            layout path for bf16);
  *   TC     — persistent tcgen05 tensor-core GEMM, bf16, K-major operands;
  *   SKINNY — tensor-core swap-AB split-K GEMM for M <= 64, bf16, K-major;
- *   SKINNY_FFMA — CUDA-core split-K dot products for M <= 16, bf16, K-major.
+ *   SKINNY_FFMA — CUDA-core split-K dot products for M <= 16, bf16, K-major;
+ *   TC_SINGLE / TC_PAIR — TC restricted to one-CTA 128-row tiles or to
+ *            CTA-pair (cta_group::2) 256-row tiles; TC picks between them.
  * Forcing a family that cannot take the arguments returns UNSUPPORTED. */
 typedef enum {
     TMG_PATH_AUTO = 0,
     TMG_PATH_FFMA = 1,
     TMG_PATH_TC = 2,
     TMG_PATH_SKINNY = 3,
-    TMG_PATH_SKINNY_FFMA = 4
+    TMG_PATH_SKINNY_FFMA = 4,
+    TMG_PATH_TC_SINGLE = 5,
+    TMG_PATH_TC_PAIR = 6
 } tmg_path;
 
 /* A rank-2 layout over logical coordinates (row, col).  Mode t (0 = rows,

@@ -167,12 +167,14 @@ def test_tc_column_major_d_swaps_operands(tmg):
     parity.check_bf16(Dt.t(), parity.ref_full(A, B, oracle.BF16), K, parity.absmax(A), parity.absmax(B))
 
 
-def test_tc_wide_tiles_sampled(tmg):
-    """Enough tiles that the 128x256 tile configuration is chosen."""
+@pytest.mark.parametrize("path", ["tc_single", "tc_pair"])
+def test_tc_wide_tiles_sampled(tmg, path):
+    """Many tiles: the one-CTA kernel takes 128x256 tiles, the pair kernel
+    its widest tiles."""
     M, N, K = 4096, 2560, 512
     A = inputs.normal_bf16(M, K, 71)
     B = inputs.normal_bf16(N, K, 72)
-    D = tmg.gemm(*_gpu(A, B), path="tc")
+    D = tmg.gemm(*_gpu(A, B), path=path)
     tmg.check()
     ms, ns = parity.sample_coords(M, N, 20000, seed=1)
     ref = parity.ref_entries(A, B, oracle.BF16, ms, ns)
@@ -181,10 +183,50 @@ def test_tc_wide_tiles_sampled(tmg):
     # integer inputs at the same shape: sampled outputs exact
     Ai = inputs.integer_valued(M, K, 73)
     Bi = inputs.integer_valued(N, K, 74)
-    Di = tmg.gemm(*_gpu(Ai, Bi), path="tc")
+    Di = tmg.gemm(*_gpu(Ai, Bi), path=path)
     tmg.check()
     refi = parity.ref_entries(Ai, Bi, oracle.BF16, ms, ns)
     parity.check_exact_bf16(parity.bf16_bits(Di)[ms, ns], refi)
+
+
+# Shapes for which the pair kernel picks each tile width on 152 SMs
+# (76 pairs): (M, N) -> width.
+PAIR_SHAPES = [((512, 512), 128), ((2048, 1536), 192), ((2048, 1792), 224), ((2048, 2048), 256)]
+
+
+@pytest.mark.parametrize("shape,width", PAIR_SHAPES)
+def test_tc_pair_each_tile_width_vs_oracle(tmg, shape, width):
+    M, N = shape
+    K = 256
+    A = inputs.normal_bf16(M, K, 130 + width)
+    B = inputs.normal_bf16(N, K, 131 + width)
+    D = tmg.gemm(*_gpu(A, B), path="tc_pair")
+    tmg.check()
+    parity.check_bf16(D, parity.ref_full(A, B, oracle.BF16), K, parity.absmax(A), parity.absmax(B))
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 333, 200), (640, 1000, 520), (256, 16, 64)])
+def test_tc_pair_ragged_integer_exact(tmg, M, N, K):
+    """Ragged pair tiles (row half of the second CTA partly or wholly out of
+    range, ragged N and K) with integer inputs: bit-exact."""
+    A = inputs.integer_valued(M, K, 140 + M)
+    B = inputs.integer_valued(N, K, 141 + N)
+    D = tmg.gemm(*_gpu(A, B), path="tc_pair")
+    tmg.check()
+    parity.check_exact_bf16(parity.bf16_bits(D), parity.ref_full(A, B, oracle.BF16))
+
+
+def test_tc_single_and_pair_agree(tmg):
+    """One-CTA and CTA-pair kernels on the same inputs: integer inputs make
+    both exact, so they must agree bit for bit."""
+    M, N, K = 768, 896, 384
+    A = inputs.integer_valued(M, K, 150)
+    B = inputs.integer_valued(N, K, 151)
+    dA, dB = _gpu(A, B)
+    D1 = tmg.gemm(dA, dB, path="tc_single").clone()
+    D2 = tmg.gemm(dA, dB, path="tc_pair")
+    tmg.check()
+    assert torch.equal(D1, D2)
 
 
 def test_tc_deterministic(tmg):

@@ -15,7 +15,8 @@ LIB_PATH = os.path.join(HERE, "libtmg.so")
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = 0, 1, 2, 3, 4
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "CUDA", 4: "TIMEOUT"}
 F32, BF16 = 0, 1
-PATHS = {"auto": 0, "ffma": 1, "tc": 2, "skinny": 3, "skinny_ffma": 4}
+PATHS = {"auto": 0, "ffma": 1, "tc": 2, "skinny": 3, "skinny_ffma": 4, "tc_single": 5,
+         "tc_pair": 6}
 
 # Every function include/tmg.h declares.
 EXPORTS = ("tmg_gemm", "tmg_gemm_ex", "tmg_gemm_mxfp4", "tmg_gemm_skinny_noalloc", "tmg_check", "tmg_last_error",

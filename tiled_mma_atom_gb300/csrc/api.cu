@@ -317,24 +317,39 @@ uint8_t *mx_scale_scratch(int dev, cudaStream_t s, size_t bytes, tmg_status *st)
     return sc.mx_scales;
 }
 
-tmg_status run_tc(const DeviceState &ds, const TcPlan &p, void *D, int64_t K, cudaStream_t s)
+// mode: 0 = choose, 1 = one-CTA tiles, 2 = CTA-pair tiles.
+tmg_status run_tc(const DeviceState &ds, const TcPlan &p, void *D, int64_t K, int mode, cudaStream_t s)
 {
     TcArgs a;
     std::memset(&a, 0, sizeof a);
-    const int tiles256 = static_cast<int>(((p.M + 127) / 128) * ((p.N + 255) / 256));
-    a.bn = tiles256 >= ds.num_sms ? 256 : 128;
+    // Pairs pay off once their tiles fill every SM pair at least once;
+    // smaller problems keep more SMs busy with one-CTA 128-row tiles.
+    bool pair = mode == 2;
+    if (mode == 0 && p.M >= 256) {
+        const int bn2 = tc2_pick_bn(p.M, p.N, ds.num_sms);
+        pair = ((p.M + 255) / 256) * ((p.N + bn2 - 1) / bn2) >= ds.num_sms / 2;
+    }
+    int box_b;
+    if (pair) {
+        a.bn = tc2_pick_bn(p.M, p.N, ds.num_sms);
+        box_b = a.bn / 2;
+    } else {
+        const int tiles256 = static_cast<int>(((p.M + 127) / 128) * ((p.N + 255) / 256));
+        a.bn = tiles256 >= ds.num_sms ? 256 : 128;
+        box_b = a.bn;
+    }
     tmg_status st;
     if ((st = encode_2d(&a.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.A, K, p.M, p.lda, 64, 128)) != TMG_OK)
         return st;
-    if ((st = encode_2d(&a.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.B, K, p.N, p.ldb, 64, a.bn)) != TMG_OK)
+    if ((st = encode_2d(&a.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.B, K, p.N, p.ldb, 64, box_b)) != TMG_OK)
         return st;
     a.D = D;
     a.ldd = p.ldd;
     a.M = static_cast<int>(p.M);
     a.N = static_cast<int>(p.N);
     a.K = static_cast<int>(K);
-    cudaError_t e = launch_tc_bf16(a, ds.num_sms, err_ctx(ds), s);
-    return e == cudaSuccess ? TMG_OK : cuda_fail(e, "tc_bf16 launch");
+    cudaError_t e = pair ? launch_tc2_bf16(a, ds.num_sms, err_ctx(ds), s) : launch_tc_bf16(a, ds.num_sms, err_ctx(ds), s);
+    return e == cudaSuccess ? TMG_OK : cuda_fail(e, pair ? "tc2_bf16 launch" : "tc_bf16 launch");
 }
 
 tmg_status run_skinny(const DeviceState &ds, const TcPlan &p, void *D, int64_t K, cudaStream_t s)
@@ -405,7 +420,7 @@ tmg_status tmg_gemm_ex(const void *A, const void *B, void *D, int64_t M, int64_t
     t_last_error.clear();
     if (dtype != TMG_F32 && dtype != TMG_BF16)
         return fail(TMG_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
-    if (path < TMG_PATH_AUTO || path > TMG_PATH_SKINNY_FFMA)
+    if (path < TMG_PATH_AUTO || path > TMG_PATH_TC_PAIR)
         return fail(TMG_ERR_INVALID_ARG, "unknown path %d", (int)path);
     if (M < 0 || N < 0 || K < 0)
         return fail(TMG_ERR_INVALID_ARG, "negative extent M=%lld N=%lld K=%lld", (long long)M, (long long)N,
@@ -465,11 +480,13 @@ tmg_status tmg_gemm_ex(const void *A, const void *B, void *D, int64_t M, int64_t
         return e == cudaSuccess ? TMG_OK : cuda_fail(e, "ffma launch");
     }
     case TMG_PATH_TC:
+    case TMG_PATH_TC_SINGLE:
+    case TMG_PATH_TC_PAIR:
         if (dtype != TMG_BF16 || !plan.ok)
             return fail(TMG_ERR_UNSUPPORTED,
                         "tensor-core path needs bf16, K-major A and B (unit K stride, 16-byte aligned rows), "
                         "and row- or column-major D");
-        return run_tc(*ds, plan, D, K, s);
+        return run_tc(*ds, plan, D, K, use == TMG_PATH_TC ? 0 : (use == TMG_PATH_TC_SINGLE ? 1 : 2), s);
     case TMG_PATH_SKINNY:
         if (dtype != TMG_BF16 || !plan.ok || plan.M > 64)
             return fail(TMG_ERR_UNSUPPORTED,

@@ -51,9 +51,14 @@ struct TcArgs {
     void *D;           // bf16 (M,N), row stride ldd elements, unit column stride
     int64_t ldd;
     int M, N, K;
-    int bn;            // 128 or 256
+    int bn;            // tile width (N per tile)
 };
 cudaError_t launch_tc_bf16(const TcArgs &a, int num_sms, const ErrCtx &err, cudaStream_t s);
+// CTA-pair variant (cta_group::2, 256 x bn tiles; bn in {256, 224, 192, 128},
+// tmB box {64, bn/2}).
+cudaError_t launch_tc2_bf16(const TcArgs &a, int num_sms, const ErrCtx &err, cudaStream_t s);
+// Pair-tile width that best fills the last wave for an M x N output.
+int tc2_pick_bn(int64_t M, int64_t N, int num_sms);
 
 // ---------------------------------------------------- skinny swap-AB path
 struct SkinnyTcArgs {
