@@ -21,6 +21,21 @@ def tmg():
     return t
 
 
+# Kernel variants: one-CTA 128x128 tiles; CTA pairs with 256x128, 256x192
+# and 256x256 tiles (selected through the library's testing variables).
+VARIANTS = {"single": {"TMG_MXFP4_KERNEL": "single"},
+            "pair128": {"TMG_MXFP4_KERNEL": "pair", "TMG_MXFP4_BN": "128"},
+            "pair192": {"TMG_MXFP4_KERNEL": "pair", "TMG_MXFP4_BN": "192"},
+            "pair256": {"TMG_MXFP4_KERNEL": "pair", "TMG_MXFP4_BN": "256"}}
+
+
+@pytest.fixture(params=list(VARIANTS))
+def variant(request, monkeypatch):
+    for k, v in VARIANTS[request.param].items():
+        monkeypatch.setenv(k, v)
+    return request.param
+
+
 def _run(tmg, A, B, sA, sB):
     D = tmg.gemm_mxfp4(*(t.to(DEV) for t in (A, B, sA, sB)))
     tmg.check()
@@ -35,7 +50,7 @@ def _amax(X, S, K):
     return float(np.abs(oracle.read_mxfp4(X.numpy(), S.numpy(), X.shape[0], K)).max())
 
 
-def test_mxfp4_unit_scales_bit_exact(tmg):
+def test_mxfp4_unit_scales_bit_exact(tmg, variant):
     """Scales 2^0: every product is a multiple of 1/4 and |sum| < 2^15, so the
     fp32 accumulation is exact and D must be RNE_bf16(exact)."""
     M, N, K = 256, 384, 512
@@ -47,7 +62,7 @@ def test_mxfp4_unit_scales_bit_exact(tmg):
     parity.check_exact_bf16(parity.bf16_bits(D), _ref(A, B, sA, sB, M, N, K))
 
 
-def test_mxfp4_per_block_scales_bit_exact(tmg):
+def test_mxfp4_per_block_scales_bit_exact(tmg, variant):
     """Scales 2^-1..2^1 varying per row and per 32-element block: products
     are multiples of 2^-4 below 2^8 and sums stay below 2^17, so the result
     is still exact — any misplaced scale (wrong row, block or half-word)
@@ -61,25 +76,29 @@ def test_mxfp4_per_block_scales_bit_exact(tmg):
     parity.check_exact_bf16(parity.bf16_bits(D), _ref(A, B, sA, sB, M, N, K))
 
 
-def test_mxfp4_one_hot_scale_locates_each_block(tmg):
-    """All codes 1.0; one row of A gets scale 2^1 on a single K block.  Each
-    output of that row must be K + 32, all others K."""
-    M, N, K = 128, 128, 512
-    one = torch.full((M, K), 2, dtype=torch.int32)            # code 2 = 1.0
-    A = inputs.pack_fp4(one)
+def test_mxfp4_one_hot_scale_locates_each_block(tmg, variant):
+    """All codes 1.0; one row of A (or of B) gets scale 2^1 on a single K
+    block.  Each output of that row (column) must be K + 32, all others K."""
+    M, N, K = 256, 320, 512
+    one = torch.full((max(M, N), K), 2, dtype=torch.int32)    # code 2 = 1.0
+    A = inputs.pack_fp4(one[:M])
     B = inputs.pack_fp4(one[:N])
-    for row, blk in [(0, 0), (37, 5), (127, 15), (64, 9)]:
+    for side, idx, blk in [("a", 0, 0), ("a", 37, 5), ("a", 127, 15), ("a", 200, 9), ("a", 255, 3),
+                           ("b", 0, 1), ("b", 95, 7), ("b", 130, 12), ("b", 191, 14), ("b", 300, 2)]:
         sA = torch.full((M, K // 32), 127, dtype=torch.uint8)
         sB = torch.full((N, K // 32), 127, dtype=torch.uint8)
-        sA[row, blk] = 128
+        (sA if side == "a" else sB)[idx, blk] = 128
         D = _run(tmg, A, B, sA, sB).float().cpu()
         want = torch.full((M, N), float(K))
-        want[row, :] = K + 32
-        assert torch.equal(D, want), (row, blk)
+        if side == "a":
+            want[idx, :] = K + 32
+        else:
+            want[:, idx] = K + 32
+        assert torch.equal(D, want), (side, idx, blk)
 
 
-@pytest.mark.parametrize("M,N,K", [(300, 200, 1024), (128, 640, 256)])
-def test_mxfp4_random_vs_oracle(tmg, M, N, K):
+@pytest.mark.parametrize("M,N,K", [(300, 200, 1024), (256, 640, 256), (520, 392, 768)])
+def test_mxfp4_random_vs_oracle(tmg, variant, M, N, K):
     A = inputs.random_fp4_codes(M, K, 7)
     B = inputs.random_fp4_codes(N, K, 8)
     sA = inputs.random_e8m0(M, K, 9)
@@ -90,7 +109,7 @@ def test_mxfp4_random_vs_oracle(tmg, M, N, K):
 
 def test_mxfp4_workload_8192_sampled(tmg):
     """8192³ MXFP4 (codes U{0..15}, scale exponents U[-4,4]), the benchmark's
-    launch: sampled outputs vs the oracle."""
+    launch (automatic kernel choice): sampled outputs vs the oracle."""
     w = inputs.WORKLOADS["mxfp4_8192"]
     A, B, sA, sB = inputs.make_inputs(w)
     D = _run(tmg, A, B, sA, sB)
@@ -105,3 +124,15 @@ def test_mxfp4_rejects_unaligned_k(tmg):
     with pytest.raises(tmg.TmgError) as ei:
         tmg.gemm_mxfp4(A, A, s, s)
     assert ei.value.status == 1
+
+
+def test_mxfp4_small_m_uses_one_cta_kernel(tmg):
+    """M < 256 cannot fill a CTA pair; the automatic choice must still be
+    exact (integer-valued case: unit scales)."""
+    M, N, K = 100, 200, 256
+    A = inputs.random_fp4_codes(M, K, 11)
+    B = inputs.random_fp4_codes(N, K, 12)
+    sA = torch.full((M, K // 32), 127, dtype=torch.uint8)
+    sB = torch.full((N, K // 32), 127, dtype=torch.uint8)
+    D = _run(tmg, A, B, sA, sB)
+    parity.check_exact_bf16(parity.bf16_bits(D), _ref(A, B, sA, sB, M, N, K))

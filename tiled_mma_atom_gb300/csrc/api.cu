@@ -17,6 +17,7 @@
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -206,14 +207,15 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // with row stride `ld` elements: box {box_inner, box_rows}, 128-byte swizzle,
 // out-of-range elements read as zero.
 tmg_status encode_2d(CUtensorMap *map, CUtensorMapDataType dt, int elem, const void *base,
-                     int64_t inner, int64_t rows, int64_t ld, int box_inner, int box_rows)
+                     int64_t inner, int64_t rows, int64_t ld, int box_inner, int box_rows,
+                     CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B)
 {
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * elem};
     cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_rows)};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return fail(TMG_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled failed (%d) for %lldx%lld ld=%lld", (int)r,
@@ -541,28 +543,57 @@ tmg_status tmg_gemm_mxfp4(const void *A, const void *B, const void *scaleA, cons
         return fail(TMG_ERR_UNSUPPORTED, "MXFP4 scale arrays must be 8-byte aligned");
     Mxfp4Args a;
     std::memset(&a, 0, sizeof a);
+    // CTA pairs once their tiles fill every SM pair; else one-CTA 128x128.
+    bool pair = false;
+    if (M >= 256) {
+        a.bn = mxfp4_pair_pick_bn(M, N, ds->num_sms);
+        pair = ((M + 255) / 256) * ((N + a.bn - 1) / a.bn) >= ds->num_sms / 2;
+    }
+    if (const char *f = getenv("TMG_MXFP4_KERNEL")) {        // testing aid: "single" | "pair"
+        if (!strcmp(f, "single"))
+            pair = false;
+        else if (!strcmp(f, "pair") && M >= 256)
+            pair = true;
+        if (pair && a.bn == 0)
+            a.bn = 128;
+    }
+    if (pair && getenv("TMG_MXFP4_BN"))
+    {
+        const int v = atoi(getenv("TMG_MXFP4_BN"));
+        a.bn = (v == 128 || v == 256) ? v : 192;
+    }
+    const int box_b = pair ? a.bn / 2 : 128;
     if ((st = encode_2d(&a.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, K / 2, M, K / 2, 128, 128)) != TMG_OK)
         return st;
-    if ((st = encode_2d(&a.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, K / 2, N, K / 2, 128, 128)) != TMG_OK)
+    if ((st = encode_2d(&a.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, K / 2, N, K / 2, 128, box_b)) != TMG_OK)
         return st;
     a.sA = static_cast<const uint8_t *>(scaleA);
     a.sB = static_cast<const uint8_t *>(scaleB);
     {
         int dev = 0;
         cudaGetDevice(&dev);
-        const size_t ra = mxfp4_relaid_scale_bytes(M, K), rb = mxfp4_relaid_scale_bytes(N, K);
+        const size_t ra = mxfp4_relaid_scale_bytes(M, K, 128), rb = mxfp4_relaid_scale_bytes(N, K, pair ? a.bn : 128);
         uint8_t *buf = mx_scale_scratch(dev, s, ra + rb, &st);
         if (!buf)
             return st;
         a.relA = buf;
         a.relB = buf + ra;
+        if (pair) {
+            const int nsub = (a.bn + 127) / 128;
+            if ((st = encode_2d(&a.tmSA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.relA, 256, ra / 256, 256, 256, 4,
+                                CU_TENSOR_MAP_SWIZZLE_NONE)) != TMG_OK)
+                return st;
+            if ((st = encode_2d(&a.tmSB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.relB, 256, rb / 256, 256, 256,
+                                4 * nsub, CU_TENSOR_MAP_SWIZZLE_NONE)) != TMG_OK)
+                return st;
+        }
     }
     a.D = D;
     a.M = static_cast<int>(M);
     a.N = static_cast<int>(N);
     a.K = static_cast<int>(K);
-    cudaError_t e = launch_mxfp4(a, ds->num_sms, err_ctx(*ds), s);
-    return e == cudaSuccess ? TMG_OK : cuda_fail(e, "mxfp4 launch");
+    cudaError_t e = pair ? launch_mxfp4_pair(a, ds->num_sms, err_ctx(*ds), s) : launch_mxfp4(a, ds->num_sms, err_ctx(*ds), s);
+    return e == cudaSuccess ? TMG_OK : cuda_fail(e, pair ? "mxfp4 pair launch" : "mxfp4 launch");
 }
 
 tmg_status tmg_gemm_skinny_noalloc(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K,

@@ -29,19 +29,18 @@
 // 16 scale columns per stage.
 #include <cuda_bf16.h>
 
-#include "internal.h"
+#include "mx_common.cuh"
 
 namespace tmg {
 namespace {
 
+using namespace mx;
+
 constexpr int kBM = 128;
 constexpr int kBN = 128;
-constexpr int kBKBytes = 128;            // 256 e2m1 codes
-constexpr int kBK = 256;                 // elements
 constexpr int kStages = 6;
 constexpr int kTileBytes = kBM * kBKBytes;   // 16 KB (A and B alike)
-constexpr int kSfChunk = 512;            // 32 rows x 16 bytes
-constexpr int kSfBytes = 2 * kSfChunk;   // 8 scales per row, 128 rows
+constexpr int kSfBytes = kSfBlock;      // 8 scales per row, 128 rows
 constexpr int kThreads = 192;
 constexpr int kTmemCols = 512;
 constexpr int kAccCols = kBN;            // per buffer
@@ -49,47 +48,6 @@ constexpr int kSfCol0 = 2 * kAccCols;    // first scale column
 constexpr int kSfColsPerStage = 16;      // A: 2 chunks x 4, B: 2 chunks x 4
 constexpr int kGroupM = 8;
 constexpr int kSmem = kStages * (2 * kTileBytes + 2 * kSfBytes) + (2 * kStages + 4) * 8 + 16 + 1024;
-
-// Shared-memory descriptor without swizzle (8-row x 16-byte core matrices,
-// stride byte offset 128 between consecutive 8-row groups), for tcgen05.cp.
-__device__ __forceinline__ uint64_t sdesc_noswizzle_rows16(uint32_t saddr)
-{
-    uint64_t d = 0;
-    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-    d |= static_cast<uint64_t>(128 >> 4) << 16;
-    d |= static_cast<uint64_t>(128 >> 4) << 32;
-    d |= static_cast<uint64_t>(1) << 46;
-    return d;
-}
-
-// Instruction descriptor, kind::mxf4 block-scaled: B scale id (bits 4-5),
-// A format (7-9) = 1 (E2M1), B format (10-12) = 1 (E2M1), K-major A and B,
-// N >> 3 (17-22), scale type (23) = 1 (E8M0), M >> 4 (24-28), A scale id
-// (29-30), K size (31) = 0 (64 dense).
-__device__ __forceinline__ uint32_t idesc_mxf4(int M, int N, uint32_t sf_id)
-{
-    return (sf_id << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
-           (1u << 23) | (static_cast<uint32_t>(M >> 4) << 24) | (sf_id << 29);
-}
-
-__device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                         uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
-                                         uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %6, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X "
-        "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
-        : "memory");
-}
-
-__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc)
-{
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
-                 : "memory");
-}
 
 __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int &tm, int &tn)
 {
@@ -101,31 +59,39 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
     tn = r / gm;
 }
 
-// Relayout pass: (rows, K/32) e8m0 row-major -> chunk order (see top).
-// One thread per 16-byte output line; blockIdx.y picks the operand.
-__global__ void mx_scale_relayout_kernel(const uint8_t *__restrict__ SA, int rowsA, uint8_t *__restrict__ outA,
-                                         const uint8_t *__restrict__ SB, int rowsB, uint8_t *__restrict__ outB,
-                                         int sf_per_row, int num_kb)
+// Relayout pass: (rows, K/32) e8m0 row-major -> chunk order, rows grouped
+// by `group_rows` (see mx_common.cuh).  One thread per 16-byte output line;
+// blockIdx.y picks the operand.
+struct RelayoutOperand {
+    const uint8_t *S;
+    uint8_t *out;
+    int rows, group_rows, nsub;
+};
+
+__global__ void mx_scale_relayout_kernel(RelayoutOperand a, RelayoutOperand b, int sf_per_row, int num_kb)
 {
-    const bool isB = blockIdx.y == 1;
-    const uint8_t *S = isB ? SB : SA;
-    const int rows = isB ? rowsB : rowsA;
-    uint8_t *out = isB ? outB : outA;
-    const int64_t lines = static_cast<int64_t>((rows + kBM - 1) / kBM) * num_kb * 64;
+    const RelayoutOperand &o = blockIdx.y == 1 ? b : a;
+    const int64_t groups = (o.rows + o.group_rows - 1) / o.group_rows;
+    const int64_t lines = groups * num_kb * o.nsub * 64;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < lines;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int r0 = static_cast<int>(i & 31);
         const int c = static_cast<int>((i >> 5) & 1);
-        const int64_t blk = i >> 6;                  // row block * num_kb + K block
+        int64_t blk = i >> 6;                       // ((g * num_kb + kb) * nsub + sub)
+        const int sub = static_cast<int>(blk % o.nsub);
+        blk /= o.nsub;
         const int kb = static_cast<int>(blk % num_kb);
-        const int64_t rb = blk / num_kb;
+        const int64_t g = blk / num_kb;
         uint32_t w[4];
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-            const int64_t row = rb * kBM + g * 32 + r0;
-            w[g] = row < rows ? __ldg(reinterpret_cast<const uint32_t *>(S + row * sf_per_row + kb * 8 + c * 4)) : 0u;
+        for (int q = 0; q < 4; ++q) {
+            const int in_group = sub * 128 + q * 32 + r0;
+            const int64_t row = g * o.group_rows + in_group;
+            w[q] = (in_group < o.group_rows && row < o.rows)
+                       ? __ldg(reinterpret_cast<const uint32_t *>(o.S + row * sf_per_row + kb * 8 + c * 4))
+                       : 0u;
         }
-        *reinterpret_cast<uint4 *>(out + i * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4 *>(o.out + i * 16) = make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
 
@@ -239,10 +205,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t sf_col = tmem_base + kSfCol0 + stage * kSfColsPerStage;
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {
-                        tmem_cp_32x128b_x4(sf_col + c * 4,
-                                           sdesc_noswizzle_rows16(smem_u32(sfA + stage * kSfBytes + c * kSfChunk)));
-                        tmem_cp_32x128b_x4(sf_col + 8 + c * 4,
-                                           sdesc_noswizzle_rows16(smem_u32(sfB + stage * kSfBytes + c * kSfChunk)));
+                        tmem_cp_chunk(sf_col + c * 4,
+                                      sdesc_noswizzle_rows16(smem_u32(sfA + stage * kSfBytes + c * kSfChunk)));
+                        tmem_cp_chunk(sf_col + 8 + c * 4,
+                                      sdesc_noswizzle_rows16(smem_u32(sfB + stage * kSfBytes + c * kSfChunk)));
                     }
                     const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(tA + stage * kTileBytes));
                     const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(tB + stage * kTileBytes));
@@ -322,9 +288,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-size_t mxfp4_relaid_scale_bytes(int64_t rows, int64_t K)
+size_t mxfp4_relaid_scale_bytes(int64_t rows, int64_t K, int group_rows)
 {
-    return static_cast<size_t>((rows + kBM - 1) / kBM) * static_cast<size_t>(K / kBK) * kSfBytes;
+    const int64_t groups = (rows + group_rows - 1) / group_rows;
+    const int64_t nsub = (group_rows + 127) / 128;
+    return static_cast<size_t>(groups * nsub * (K / kBK) * kSfBlock);
+}
+
+cudaError_t launch_mx_scale_relayout(const uint8_t *sA, int M, uint8_t *relA, int groupA, const uint8_t *sB,
+                                     int N, uint8_t *relB, int groupB, int K, int num_sms, cudaStream_t s)
+{
+    const int num_kb = K / kBK;
+    RelayoutOperand a{sA, relA, M, groupA, (groupA + 127) / 128};
+    RelayoutOperand b{sB, relB, N, groupB, (groupB + 127) / 128};
+    const int64_t la = static_cast<int64_t>(mxfp4_relaid_scale_bytes(M, K, groupA) / 16);
+    const int64_t lb = static_cast<int64_t>(mxfp4_relaid_scale_bytes(N, K, groupB) / 16);
+    int64_t blocks = ((la > lb ? la : lb) + 255) / 256;
+    if (blocks > 4L * num_sms)
+        blocks = 4L * num_sms;
+    note_launch();
+    mx_scale_relayout_kernel<<<dim3(static_cast<unsigned>(blocks), 2), 256, 0, s>>>(a, b, K / 32, num_kb);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_mxfp4(const Mxfp4Args &a, int num_sms, const ErrCtx &err, cudaStream_t s)
@@ -334,15 +318,8 @@ cudaError_t launch_mxfp4(const Mxfp4Args &a, int num_sms, const ErrCtx &err, cud
     cudaError_t e = cudaFuncSetAttribute(mxfp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess)
         return e;
-    const int num_kb = a.K / kBK;
-    const int64_t lines = static_cast<int64_t>((a.M > a.N ? a.M : a.N) + kBM - 1) / kBM * num_kb * 64;
-    int64_t blocks = (lines + 255) / 256;
-    if (blocks > 4L * num_sms)
-        blocks = 4L * num_sms;
-    note_launch();
-    mx_scale_relayout_kernel<<<dim3(static_cast<unsigned>(blocks), 2), 256, 0, s>>>(
-        a.sA, a.M, a.relA, a.sB, a.N, a.relB, a.K / 32, num_kb);
-    if ((e = cudaGetLastError()) != cudaSuccess)
+    e = launch_mx_scale_relayout(a.sA, a.M, a.relA, kBM, a.sB, a.N, a.relB, kBN, a.K, num_sms, s);
+    if (e != cudaSuccess)
         return e;
     const int tiles = ((a.M + kBM - 1) / kBM) * ((a.N + kBN - 1) / kBN);
     const int grid = tiles < num_sms ? tiles : num_sms;

@@ -1,0 +1,393 @@
+// mxfp4_pair.cu — the MXFP4 GEMM of mxfp4.cu on CTA pairs
+// (tcgen05.mma.cta_group::2.kind::mxf4.block_scale, M = 256).
+//
+// Each cluster of two CTAs computes a 256 x BN tile (BN = 192 or 128).  CTA r
+// keeps in its own shared memory rows 128r..128r+127 of the A codes, rows
+// r·BN/2.. of the B codes, the scales of its own 128 A rows and the scales
+// of all BN B rows (its tensor core multiplies its 128 rows by every column
+// of the tile, so it needs every B scale).  All four loads of both CTAs are
+// TMA copies completing on CTA 0's `full` barrier.  CTA 0's MMA lane copies
+// the scale chunks of both CTAs into their TMEM with one
+// tcgen05.cp.cta_group::2 per chunk, then issues the pair MMAs.  TMEM per
+// CTA: two BN-column accumulators plus, per stage, 8 columns of A scales and
+// 8·ceil(BN/128) columns of B scales (B rows 0-127 in the first 4 columns of
+// each K-block group, rows 128.. in the next 4).
+//
+// The FlyDSL pages express the product with scaled MFMA/WMMA atoms (E8M0
+// scale per 32 K elements: "FlyDSL Kernel Authoring Skill", §6, MX-scaled
+// WMMA; "Kernel authoring guide", §4.3 GFX950 scaled MFMA).
+#include <cuda_bf16.h>
+
+#include <cstring>
+
+#include "mx_common.cuh"
+
+namespace tmg {
+namespace {
+
+using namespace mx;
+
+constexpr int kBM = 256;
+constexpr int kHalfM = 128;
+// warps 0-1 (producer, MMA) + epilogue warps: 4 with two accumulators, 8
+// with one (two warps per TMEM lane quarter, each draining half the columns)
+__host__ __device__ constexpr int pair_threads(int acc_bufs) { return acc_bufs == 1 ? 320 : 192; }
+constexpr int kGroupM = 8;
+constexpr int kTmemCols = 512;
+
+template <int BN, int ACC_BUFS>
+struct MxPairCfg {
+    static constexpr int NSUB = (BN + 127) / 128;
+    static constexpr int A_BYTES = kHalfM * kBKBytes;          // 16 KB
+    static constexpr int B_BYTES = (BN / 2) * kBKBytes;
+    static constexpr int SFA_BYTES = kSfBlock;
+    static constexpr int SFB_BYTES = NSUB * kSfBlock;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+    static constexpr int SF_COLS = 8 + 8 * NSUB;                 // per stage
+    static constexpr int TMEM_STAGES = (kTmemCols - ACC_BUFS * BN) / SF_COLS;
+    static constexpr int SMEM_STAGES = (220 * 1024 - 2048) / STAGE_BYTES;
+    static constexpr int STAGES0 = TMEM_STAGES < SMEM_STAGES ? TMEM_STAGES : SMEM_STAGES;
+    static constexpr int STAGES = STAGES0 > 8 ? 8 : STAGES0;
+    static constexpr int BAR_BYTES = (2 * STAGES + 4) * 8 + 16;
+    static constexpr int SMEM = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+};
+
+__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int &tm, int &tn)
+{
+    const int group = kGroupM * tiles_n;
+    const int first_m = (t / group) * kGroupM;
+    const int gm = min(tiles_m - first_m, kGroupM);
+    const int r = t % group;
+    tm = first_m + r % gm;
+    tn = r / gm;
+}
+
+// ACC_BUFS = 2: two accumulators, the epilogue of tile i overlaps the
+// mainloop of tile i+1.  ACC_BUFS = 1 (BN = 256, where two accumulators
+// would leave no TMEM for scales): the epilogue first drains the whole
+// accumulator into packed bf16 registers, releases TMEM, then stores.
+template <int BN, int ACC_BUFS>
+__global__ void __launch_bounds__(pair_threads(ACC_BUFS), 1)
+    mxfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                      const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
+                      __nv_bfloat16 *__restrict__ D, int M, int N, int K, int vec_ok, ErrCtx err)
+{
+    using C = MxPairCfg<BN, ACC_BUFS>;
+    constexpr int STAGES = C::STAGES;
+    constexpr int NSUB = C::NSUB;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    uint8_t *tA = smem;
+    uint8_t *tB = tA + STAGES * C::A_BYTES;
+    uint8_t *sfA = tB + STAGES * C::B_BYTES;
+    uint8_t *sfB = sfA + STAGES * C::SFA_BYTES;
+    uint64_t *full = reinterpret_cast<uint64_t *>(sfB + STAGES * C::SFB_BYTES);
+    uint64_t *empty = full + STAGES;
+    uint64_t *tfull = empty + STAGES;
+    uint64_t *tempty = tfull + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const uint32_t rank = cluster_ctarank();
+    const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
+    const int tiles_m = (M + kBM - 1) / kBM, tiles_n = (N + BN - 1) / BN;
+    const int num_tiles = tiles_m * tiles_n;
+    const int num_kb = K / kBK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 2 * (pair_threads(ACC_BUFS) / 32 - 2));   // epilogue warps of both CTAs
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmSA);
+        tma_prefetch_desc(&tmSB);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_slot, kTmemCols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------------------------------------- TMA producer
+            int stage = 0;
+            uint32_t phase = 0;
+            int64_t issued = 0;
+            bool ok = true;
+            for (int t = cluster; t < num_tiles && ok; t += nclusters) {
+                int tm, tn;
+                tile_coords(t, tiles_m, tiles_n, tm, tn);
+                // rows (of 256 bytes) of this CTA's / this tile's relaid scales
+                const int sfa_row0 = (tm * 2 + static_cast<int>(rank)) * num_kb * (kSfBlock / 256);
+                const int sfb_row0 = tn * num_kb * NSUB * (kSfBlock / 256);
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait_cluster(&empty[stage], phase ^ 1u, err, abort_flag, kSiteProducerEmpty)) {
+                        ok = false;
+                        break;
+                    }
+                    if (rank == 0)
+                        mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
+                    const uint32_t bar0 = mapa_shared(smem_u32(&full[stage]), 0);
+                    tma_load_2d_pair(tA + stage * C::A_BYTES, &tmA, bar0, kb * kBKBytes,
+                                     tm * kBM + static_cast<int>(rank) * kHalfM);
+                    tma_load_2d_pair(tB + stage * C::B_BYTES, &tmB, bar0, kb * kBKBytes,
+                                     tn * BN + static_cast<int>(rank) * (BN / 2));
+                    tma_load_2d_pair(sfA + stage * C::SFA_BYTES, &tmSA, bar0, 0, sfa_row0 + kb * (kSfBlock / 256));
+                    tma_load_2d_pair(sfB + stage * C::SFB_BYTES, &tmSB, bar0, 0,
+                                     sfb_row0 + kb * NSUB * (kSfBlock / 256));
+                    ++issued;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            for (int i = 0; i < STAGES && i < issued; ++i) {
+                int s = stage - 1 - i;
+                uint32_t ph = phase;
+                if (s < 0) {
+                    s += STAGES;
+                    ph ^= 1u;
+                }
+                if (rank == 0)
+                    mbar_wait_cluster(&full[s], ph, err, abort_flag, kSiteDrain);
+                mbar_wait_cluster(&empty[s], ph, err, abort_flag, kSiteDrain);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && rank == 0) {
+            // ------------------------------------------------ MMA issuer
+            int stage = 0;
+            uint32_t phase = 0;
+            int local = 0;
+            bool ok = true;
+            for (int t = cluster; t < num_tiles && ok; t += nclusters, ++local) {
+                const int acc = local % ACC_BUFS;
+                const uint32_t use_phase = (local / ACC_BUFS) & 1;
+                if (!mbar_wait_cluster(&tempty[acc], use_phase ^ 1u, err, abort_flag, kSiteMmaTmemEmpty))
+                    break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * BN;
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait_cluster(&full[stage], phase, err, abort_flag, kSiteMmaFull)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sfa_col = tmem_base + ACC_BUFS * BN + stage * C::SF_COLS;
+                    const uint32_t sfb_col = sfa_col + 8;
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        tmem_cp_chunk_pair(sfa_col + c * 4,
+                                           sdesc_noswizzle_rows16(smem_u32(sfA + stage * C::SFA_BYTES + c * kSfChunk)));
+#pragma unroll
+                        for (int sub = 0; sub < NSUB; ++sub)
+                            tmem_cp_chunk_pair(sfb_col + c * 4 * NSUB + sub * 4,
+                                               sdesc_noswizzle_rows16(smem_u32(sfB + stage * C::SFB_BYTES +
+                                                                               sub * kSfBlock + c * kSfChunk)));
+                    }
+                    const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(tA + stage * C::A_BYTES));
+                    const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(tB + stage * C::B_BYTES));
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint64_t koff = static_cast<uint64_t>((k * 32) >> 4);
+                        const int c = k >> 1;
+                        const uint32_t id = (k & 1) ? 2u : 0u;
+                        mma_mxf4_pair(d_tmem, adesc + koff, bdesc + koff, idesc_mxf4(kBM, BN, id), sfa_col + c * 4,
+                                      sfb_col + c * 4 * NSUB, (kb | k) != 0);
+                    }
+                    mma_commit_pair(&empty[stage], 0x3);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok)
+                    break;
+                mma_commit_pair(&tfull[acc], 0x3);
+            }
+        }
+    } else {
+        // ---------------------------------------------------- epilogue
+        const int q = warp & 3;
+        int local = 0;
+        for (int t = cluster; t < num_tiles; t += nclusters, ++local) {
+            int tm, tn;
+            tile_coords(t, tiles_m, tiles_n, tm, tn);
+            const int acc = local % ACC_BUFS;
+            if (!mbar_wait_cluster(&tfull[acc], (local / ACC_BUFS) & 1, err, abort_flag, kSiteEpiTmemFull))
+                break;
+            tc_fence_after();
+            const int row = tm * kBM + static_cast<int>(rank) * kHalfM + q * 32 + lane;
+            __nv_bfloat16 *drow = D + static_cast<int64_t>(row) * N;
+            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+            if constexpr (ACC_BUFS == 1) {
+                // drain this warp's half of the columns first so the next
+                // tile's MMAs can start, then store
+                constexpr int HALF = BN / 2;
+                const int h = (warp - 2) / 4;
+                uint32_t packed[HALF / 2];
+#pragma unroll
+                for (int c = 0; c < HALF / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(tbase + h * HALF + c * 32, v);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        packed[c * 16 + j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
+                if (row < M) {
+#pragma unroll
+                    for (int c = 0; c < HALF / 32; ++c) {
+                        const int col0 = tn * BN + h * HALF + c * 32;
+                        if (vec_ok && col0 + 32 <= N) {
+                            uint4 *dst = reinterpret_cast<uint4 *>(drow + col0);
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                dst[j] = make_uint4(packed[c * 16 + 4 * j], packed[c * 16 + 4 * j + 1],
+                                                    packed[c * 16 + 4 * j + 2], packed[c * 16 + 4 * j + 3]);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                if (col0 + j < N) {
+                                    const uint32_t w = packed[c * 16 + j / 2];
+                                    const uint16_t hv = (j & 1) ? static_cast<uint16_t>(w >> 16)
+                                                                : static_cast<uint16_t>(w & 0xFFFFu);
+                                    drow[col0 + j] = __ushort_as_bfloat16(hv);
+                                }
+                        }
+                    }
+                }
+                continue;
+            }
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(tbase + c * 32, v);
+                const int col0 = tn * BN + c * 32;
+                if (row < M) {
+                    if (vec_ok && col0 + 32 <= N) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(drow + col0);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            uint4 w;
+                            w.x = pack_bf16x2(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1]));
+                            w.y = pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3]));
+                            w.z = pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5]));
+                            w.w = pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7]));
+                            dst[j] = w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (col0 + j < N)
+                                drow[col0 + j] = __float2bfloat16_rn(__uint_as_float(v[j]));
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    cluster_sync();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, kTmemCols);
+    }
+}
+
+template <int BN, int ACC_BUFS>
+cudaError_t launch_pair(const Mxfp4Args &a, int num_sms, const ErrCtx &err, cudaStream_t s)
+{
+    using C = MxPairCfg<BN, ACC_BUFS>;
+    static_assert(C::STAGES >= 3, "pipeline depth");
+    static_assert(C::SMEM <= 232448, "shared memory budget");
+    static_assert(ACC_BUFS * BN + C::STAGES * C::SF_COLS <= kTmemCols, "TMEM budget");
+    static_assert(C::B_BYTES % 1024 == 0, "B half must be whole 8-row swizzle atoms");
+    auto kern = mxfp4_pair_kernel<BN, ACC_BUFS>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess)
+        return e;
+    e = launch_mx_scale_relayout(a.sA, a.M, a.relA, kHalfM, a.sB, a.N, a.relB, BN, a.K, num_sms, s);
+    if (e != cudaSuccess)
+        return e;
+    const int tiles = ((a.M + kBM - 1) / kBM) * ((a.N + BN - 1) / BN);
+    int clusters = num_sms / 2;
+    if (tiles < clusters)
+        clusters = tiles;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3(2 * clusters);
+    cfg.blockDim = dim3(pair_threads(ACC_BUFS));
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const int vec_ok = (a.N % 8 == 0) && ((reinterpret_cast<uintptr_t>(a.D) & 15u) == 0);
+    note_launch();
+    e = cudaLaunchKernelEx(&cfg, kern, a.tmA, a.tmB, a.tmSA, a.tmSB, static_cast<__nv_bfloat16 *>(a.D), a.M, a.N,
+                           a.K, vec_ok, err);
+    if (e != cudaSuccess)
+        return e;
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int mxfp4_pair_pick_bn(int64_t M, int64_t N, int num_sms)
+{
+    static const int cands[] = {256, 192, 128};
+    const int64_t clusters = num_sms / 2;
+    const int64_t tm = (M + kBM - 1) / kBM;
+    int best = 256;
+    int64_t best_cost = -1;
+    for (int bn : cands) {
+        const int64_t tiles = tm * ((N + bn - 1) / bn);
+        const int64_t cost = ((tiles + clusters - 1) / clusters) * (bn + 48);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = bn;
+        }
+    }
+    return best;
+}
+
+cudaError_t launch_mxfp4_pair(const Mxfp4Args &a, int num_sms, const ErrCtx &err, cudaStream_t s)
+{
+    if (a.bn == 256)
+        return launch_pair<256, 1>(a, num_sms, err, s);
+    if (a.bn == 192)
+        return launch_pair<192, 2>(a, num_sms, err, s);
+    return launch_pair<128, 2>(a, num_sms, err, s);
+}
+
+}  // namespace tmg
