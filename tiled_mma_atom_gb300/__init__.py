@@ -39,8 +39,10 @@ def _layout_of(t: torch.Tensor, rows: int, cols: int) -> Layout:
     return make_layout((rows, cols), (t.stride(0), t.stride(1)))
 
 
-def _as_layout(spec, t: torch.Tensor, rows: int, cols: int) -> Layout:
+def _as_layout(spec, t: torch.Tensor, rows: int, cols: int):
     if spec is None:
+        if t.dim() == 2 and t.shape[0] == rows and t.shape[1] == cols and t.is_contiguous():
+            return None          # the library's default: row-major (rows, cols):(cols, 1)
         return _layout_of(t, rows, cols)
     if isinstance(spec, Layout):
         return spec

@@ -20,6 +20,9 @@
 #include <cstdlib>
 #include <cstring>
 #include <map>
+#include <set>
+#include <tuple>
+#include <unordered_map>
 #include <mutex>
 #include <string>
 #include <utility>
@@ -206,10 +209,48 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // 2-D TMA descriptor over a row-major (rows, inner) matrix of `elem` bytes
 // with row stride `ld` elements: box {box_inner, box_rows}, 128-byte swizzle,
 // out-of-range elements read as zero.
+// Encoded descriptors are cached: a descriptor only records an address,
+// extents, strides and the box, so an identical request gets an identical
+// descriptor whatever the memory holds now.
+struct MapKey {
+    uintptr_t base;
+    int64_t inner, rows, ld;
+    int box_inner, box_rows, dt, swizzle;
+    bool operator==(const MapKey &o) const
+    {
+        return base == o.base && inner == o.inner && rows == o.rows && ld == o.ld && box_inner == o.box_inner &&
+               box_rows == o.box_rows && dt == o.dt && swizzle == o.swizzle;
+    }
+};
+struct MapKeyHash {
+    size_t operator()(const MapKey &k) const
+    {
+        uint64_t h = k.base * 0x9E3779B97F4A7C15ull;
+        for (uint64_t v : {static_cast<uint64_t>(k.inner), static_cast<uint64_t>(k.rows), static_cast<uint64_t>(k.ld),
+                           static_cast<uint64_t>(k.box_inner) << 32 | static_cast<uint32_t>(k.box_rows),
+                           static_cast<uint64_t>(k.dt) << 32 | static_cast<uint32_t>(k.swizzle)})
+            h = (h ^ v) * 0x100000001B3ull;
+        return static_cast<size_t>(h);
+    }
+};
+std::mutex g_map_mu;
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
+constexpr size_t kMaxCachedMaps = 1024;
+
 tmg_status encode_2d(CUtensorMap *map, CUtensorMapDataType dt, int elem, const void *base,
                      int64_t inner, int64_t rows, int64_t ld, int box_inner, int box_rows,
                      CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B)
 {
+    const MapKey key{reinterpret_cast<uintptr_t>(base), inner, rows, ld, box_inner, box_rows, static_cast<int>(dt),
+                     static_cast<int>(swizzle)};
+    {
+        std::lock_guard<std::mutex> lk(g_map_mu);
+        auto it = g_maps.find(key);
+        if (it != g_maps.end()) {
+            *map = it->second;
+            return TMG_OK;
+        }
+    }
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * elem};
     cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_rows)};
@@ -220,6 +261,10 @@ tmg_status encode_2d(CUtensorMap *map, CUtensorMapDataType dt, int elem, const v
     if (r != CUDA_SUCCESS)
         return fail(TMG_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled failed (%d) for %lldx%lld ld=%lld", (int)r,
                     (long long)rows, (long long)inner, (long long)ld);
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    if (g_maps.size() >= kMaxCachedMaps)
+        g_maps.clear();
+    g_maps.emplace(key, *map);
     return TMG_OK;
 }
 
@@ -336,8 +381,14 @@ tmg_status run_tc(const DeviceState &ds, const TcPlan &p, void *D, int64_t K, in
         a.bn = tc2_pick_bn(p.M, p.N, ds.num_sms);
         box_b = a.bn / 2;
     } else {
-        const int tiles256 = static_cast<int>(((p.M + 127) / 128) * ((p.N + 255) / 256));
-        a.bn = tiles256 >= ds.num_sms ? 256 : 128;
+        // widest tile that still gives every SM work; 64 for small problems
+        const int64_t rows = (p.M + 127) / 128;
+        if (rows * ((p.N + 255) / 256) >= ds.num_sms)
+            a.bn = 256;
+        else if (rows * ((p.N + 127) / 128) >= ds.num_sms / 2)
+            a.bn = 128;
+        else
+            a.bn = 64;
         box_b = a.bn;
     }
     tmg_status st;
@@ -385,6 +436,28 @@ tmg_status run_skinny(const DeviceState &ds, const TcPlan &p, void *D, int64_t K
 }  // namespace
 
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+cudaError_t ensure_smem_attr(const void *func, int bytes)
+{
+    static std::mutex mu;
+    static std::set<std::tuple<int, const void *, int>> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    const auto key = std::make_tuple(dev, func, bytes);
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        if (done.count(key))
+            return cudaSuccess;
+    }
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) {
+        std::lock_guard<std::mutex> lk(mu);
+        done.insert(key);
+    }
+    return e;
+}
 
 namespace {
 
@@ -731,6 +804,8 @@ void tmg_shutdown(void)
     }
     g_scratch.clear();
     cudaSetDevice(cur);
+    std::lock_guard<std::mutex> lk2(g_map_mu);
+    g_maps.clear();
 }
 
 }  // extern "C"

@@ -6,9 +6,11 @@
 //    Skill", §2 "Coordinate Mapping": index = sum of coordinate x stride; a
 //    nested mode's scalar coordinate is split first-sub-mode-fastest).  The
 //    page's "Naive GEMM Template" (§8) computes one output per thread with a
-//    K loop of scalar loads; here a CTA stages 16-deep K slices of a 64x64 (or
-//    32x32) output tile in shared memory and each thread accumulates a
-//    register tile, summing k in increasing order.
+//    K loop of scalar loads; here a CTA stages 32-deep K slices of a 64x64 (or
+//    32x32) output tile in shared memory, prefetching the next slice into
+//    registers (the prologue / loop-carried prefetch of §3 "Runtime Loops with
+//    Loop-Carried Values"), and each thread accumulates a register tile,
+//    summing k in increasing order.
 //
 // 2. skinny_ffma: M <= 16 decode-shaped GEMM with K-major bf16 operands.  A
 //    warp streams four rows of B with 128-bit loads, lanes splitting K, and
@@ -61,23 +63,57 @@ __device__ __forceinline__ void st_elt<__nv_bfloat16>(__nv_bfloat16 *p, int64_t 
 }
 
 constexpr int kFfmaThreads = 256;
-constexpr int kFfmaBK = 16;
 
 // Thread (tx, ty) of a 16x16 grid owns rows ty + 16 i and columns tx + 16 j
-// of the CTA tile, i < BM/16, j < BN/16.
-template <typename T, int BM, int BN>
+// of the CTA tile, i < BM/16, j < BN/16.  Software-pipelined: while the
+// threads multiply the K slice in shared memory, the next slice's elements
+// are already in flight into registers; two shared buffers alternate, so one
+// barrier per slice suffices.  Each output still sums k in increasing order.
+template <typename T, int BM, int BN, int kFfmaBK>
 __global__ void __launch_bounds__(kFfmaThreads)
     ffma_gemm_kernel(const T *__restrict__ A, const T *__restrict__ B, T *__restrict__ D,
                      DevLayout la, DevLayout lb, DevLayout ld, int64_t M, int64_t N, int64_t K)
 {
     constexpr int TM = BM / 16, TN = BN / 16;
-    __shared__ float As[kFfmaBK][BM + 1];
-    __shared__ float Bs[kFfmaBK][BN + 1];
+    constexpr int LA = BM * kFfmaBK / kFfmaThreads;     // elements of A each thread loads per slice
+    constexpr int LB = BN * kFfmaBK / kFfmaThreads;
+    __shared__ float As[2][kFfmaBK][BM + 1];
+    __shared__ float Bs[2][kFfmaBK][BN + 1];
 
     const int tid = threadIdx.x;
     const int tx = tid % 16, ty = tid / 16;
     const int64_t m0 = static_cast<int64_t>(blockIdx.y) * BM;
     const int64_t n0 = static_cast<int64_t>(blockIdx.x) * BN;
+
+    float ra[LA], rb[LB];
+    // element e = tid + 256 r of the slice: k fastest (row-major operands read
+    // contiguous runs), then row
+    auto load = [&](int64_t k0) {
+#pragma unroll
+        for (int r = 0; r < LA; ++r) {
+            const int e = tid + kFfmaThreads * r;
+            const int64_t m = m0 + e / kFfmaBK, k = k0 + e % kFfmaBK;
+            ra[r] = (m < M && k < K) ? ld_elt(A, crd2idx(la, m, k)) : 0.f;
+        }
+#pragma unroll
+        for (int r = 0; r < LB; ++r) {
+            const int e = tid + kFfmaThreads * r;
+            const int64_t n = n0 + e / kFfmaBK, k = k0 + e % kFfmaBK;
+            rb[r] = (n < N && k < K) ? ld_elt(B, crd2idx(lb, n, k)) : 0.f;
+        }
+    };
+    auto stash = [&](int buf) {
+#pragma unroll
+        for (int r = 0; r < LA; ++r) {
+            const int e = tid + kFfmaThreads * r;
+            As[buf][e % kFfmaBK][e / kFfmaBK] = ra[r];
+        }
+#pragma unroll
+        for (int r = 0; r < LB; ++r) {
+            const int e = tid + kFfmaThreads * r;
+            Bs[buf][e % kFfmaBK][e / kFfmaBK] = rb[r];
+        }
+    };
 
     float acc[TM][TN];
 #pragma unroll
@@ -86,35 +122,33 @@ __global__ void __launch_bounds__(kFfmaThreads)
         for (int j = 0; j < TN; ++j)
             acc[i][j] = 0.f;
 
+    load(0);
+    stash(0);
+    __syncthreads();
+    int buf = 0;
     for (int64_t k0 = 0; k0 < K; k0 += kFfmaBK) {
-        // k fastest across threads: row-major operands read 64-byte runs
-        for (int e = tid; e < BM * kFfmaBK; e += kFfmaThreads) {
-            const int kk = e % kFfmaBK, mm = e / kFfmaBK;
-            const int64_t m = m0 + mm, k = k0 + kk;
-            As[kk][mm] = (m < M && k < K) ? ld_elt(A, crd2idx(la, m, k)) : 0.f;
-        }
-        for (int e = tid; e < BN * kFfmaBK; e += kFfmaThreads) {
-            const int kk = e % kFfmaBK, nn = e / kFfmaBK;
-            const int64_t n = n0 + nn, k = k0 + kk;
-            Bs[kk][nn] = (n < N && k < K) ? ld_elt(B, crd2idx(lb, n, k)) : 0.f;
-        }
-        __syncthreads();
+        const bool more = k0 + kFfmaBK < K;
+        if (more)
+            load(k0 + kFfmaBK);
 #pragma unroll
         for (int kk = 0; kk < kFfmaBK; ++kk) {
             float a[TM], b[TN];
 #pragma unroll
             for (int i = 0; i < TM; ++i)
-                a[i] = As[kk][ty + 16 * i];
+                a[i] = As[buf][kk][ty + 16 * i];
 #pragma unroll
             for (int j = 0; j < TN; ++j)
-                b[j] = Bs[kk][tx + 16 * j];
+                b[j] = Bs[buf][kk][tx + 16 * j];
 #pragma unroll
             for (int i = 0; i < TM; ++i)
 #pragma unroll
                 for (int j = 0; j < TN; ++j)
                     acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
         }
+        if (more)
+            stash(buf ^ 1);
         __syncthreads();
+        buf ^= 1;
     }
 
 #pragma unroll
@@ -221,36 +255,37 @@ __global__ void __launch_bounds__(256)
     }
 }
 
-}  // namespace
-
-cudaError_t launch_ffma(const FfmaArgs &a, int dtype, int num_sms, const ErrCtx &err,
-                        cudaStream_t s)
+template <typename T, int BM, int BN, int BK>
+cudaError_t launch_ffma_cfg(const FfmaArgs &a, cudaStream_t s)
 {
-    (void)err;
-    // small problems: 32x32 tiles for more CTAs; else 64x64
-    const bool small = (a.M * a.N) <= static_cast<int64_t>(num_sms) * 64 * 64;
-    const int bm = small ? 32 : 64;
-    dim3 grid(static_cast<unsigned>((a.N + bm - 1) / bm), static_cast<unsigned>((a.M + bm - 1) / bm));
+    dim3 grid(static_cast<unsigned>((a.N + BN - 1) / BN), static_cast<unsigned>((a.M + BM - 1) / BM));
     if (grid.y > 65535u)
         return cudaErrorInvalidConfiguration;
     note_launch();
-    if (dtype == 0) {
-        const float *A = static_cast<const float *>(a.A), *B = static_cast<const float *>(a.B);
-        float *D = static_cast<float *>(a.D);
-        if (small)
-            ffma_gemm_kernel<float, 32, 32><<<grid, kFfmaThreads, 0, s>>>(A, B, D, a.la, a.lb, a.ld, a.M, a.N, a.K);
-        else
-            ffma_gemm_kernel<float, 64, 64><<<grid, kFfmaThreads, 0, s>>>(A, B, D, a.la, a.lb, a.ld, a.M, a.N, a.K);
-    } else {
-        const __nv_bfloat16 *A = static_cast<const __nv_bfloat16 *>(a.A);
-        const __nv_bfloat16 *B = static_cast<const __nv_bfloat16 *>(a.B);
-        __nv_bfloat16 *D = static_cast<__nv_bfloat16 *>(a.D);
-        if (small)
-            ffma_gemm_kernel<__nv_bfloat16, 32, 32><<<grid, kFfmaThreads, 0, s>>>(A, B, D, a.la, a.lb, a.ld, a.M, a.N, a.K);
-        else
-            ffma_gemm_kernel<__nv_bfloat16, 64, 64><<<grid, kFfmaThreads, 0, s>>>(A, B, D, a.la, a.lb, a.ld, a.M, a.N, a.K);
-    }
+    ffma_gemm_kernel<T, BM, BN, BK><<<grid, kFfmaThreads, 0, s>>>(static_cast<const T *>(a.A), static_cast<const T *>(a.B),
+                                                                  static_cast<T *>(a.D), a.la, a.lb, a.ld, a.M, a.N, a.K);
     return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_ffma_t(const FfmaArgs &a, int num_sms, cudaStream_t s)
+{
+    // Latency-bound small problems: many 16x16 tiles, 128-deep K slices (one
+    // global round trip per 128 k); mid-size: 32x32; large: 64x64.
+    const int64_t mn = a.M * a.N;
+    if (mn <= static_cast<int64_t>(num_sms) * 16 * 16 * 2)
+        return launch_ffma_cfg<T, 16, 16, 128>(a, s);
+    if (mn <= static_cast<int64_t>(num_sms) * 64 * 64)
+        return launch_ffma_cfg<T, 32, 32, 32>(a, s);
+    return launch_ffma_cfg<T, 64, 64, 32>(a, s);
+}
+
+}  // namespace
+
+cudaError_t launch_ffma(const FfmaArgs &a, int dtype, int num_sms, const ErrCtx &err, cudaStream_t s)
+{
+    (void)err;
+    return dtype == 0 ? launch_ffma_t<float>(a, num_sms, s) : launch_ffma_t<__nv_bfloat16>(a, num_sms, s);
 }
 
 cudaError_t launch_zero_fill(void *D, const DevLayout &ld, int64_t M, int64_t N, int dtype,

@@ -119,4 +119,7 @@ cudaError_t launch_wait_probe(const ErrCtx &err, cudaStream_t s);
 // Counts every kernel launch made through the launchers above.
 void note_launch();
 
+// Raise a kernel's dynamic shared-memory limit once per device (cached).
+cudaError_t ensure_smem_attr(const void *func, int bytes);
+
 }  // namespace tmg

@@ -68,30 +68,44 @@ struct RelayoutOperand {
     int rows, group_rows, nsub;
 };
 
-__global__ void mx_scale_relayout_kernel(RelayoutOperand a, RelayoutOperand b, int sf_per_row, int num_kb)
+// A CTA takes one 128-row sub-block and up to 8 consecutive K blocks: it
+// reads the 128 x 64 bytes of scales row by row (8-byte loads, consecutive
+// threads on consecutive bytes), then writes the 8 output blocks of 1 KB as
+// consecutive 16-byte lines.  blockIdx.y picks the operand.
+__global__ void __launch_bounds__(256)
+    mx_scale_relayout_kernel(RelayoutOperand a, RelayoutOperand b, int sf_per_row, int num_kb)
 {
     const RelayoutOperand &o = blockIdx.y == 1 ? b : a;
+    __shared__ uint32_t tile[128][17];                 // 16 words of scales per row, +1 pad
+    const int kgroups = (num_kb + 7) / 8;
     const int64_t groups = (o.rows + o.group_rows - 1) / o.group_rows;
-    const int64_t lines = groups * num_kb * o.nsub * 64;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < lines;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int r0 = static_cast<int>(i & 31);
-        const int c = static_cast<int>((i >> 5) & 1);
-        int64_t blk = i >> 6;                       // ((g * num_kb + kb) * nsub + sub)
-        const int sub = static_cast<int>(blk % o.nsub);
-        blk /= o.nsub;
-        const int kb = static_cast<int>(blk % num_kb);
-        const int64_t g = blk / num_kb;
-        uint32_t w[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int in_group = sub * 128 + q * 32 + r0;
+    const int64_t nblocks = groups * o.nsub * kgroups;
+    for (int64_t blk = blockIdx.x; blk < nblocks; blk += gridDim.x) {
+        const int kgrp = static_cast<int>(blk % kgroups);
+        const int64_t rest = blk / kgroups;
+        const int sub = static_cast<int>(rest % o.nsub);
+        const int64_t g = rest / o.nsub;
+        const int kb0 = kgrp * 8;
+        const int nk = num_kb - kb0 < 8 ? num_kb - kb0 : 8;
+        for (int e = threadIdx.x; e < 128 * 8; e += 256) {
+            const int r = e >> 3, kk = e & 7;
+            const int in_group = sub * 128 + r;
             const int64_t row = g * o.group_rows + in_group;
-            w[q] = (in_group < o.group_rows && row < o.rows)
-                       ? __ldg(reinterpret_cast<const uint32_t *>(o.S + row * sf_per_row + kb * 8 + c * 4))
-                       : 0u;
+            uint2 v = make_uint2(0u, 0u);
+            if (kk < nk && in_group < o.group_rows && row < o.rows)
+                v = __ldg(reinterpret_cast<const uint2 *>(o.S + row * sf_per_row + (kb0 + kk) * 8));
+            tile[r][2 * kk] = v.x;
+            tile[r][2 * kk + 1] = v.y;
         }
-        *reinterpret_cast<uint4 *>(o.out + i * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+        __syncthreads();
+        for (int l = threadIdx.x; l < nk * 64; l += 256) {
+            const int kk = l >> 6, c = (l >> 5) & 1, r0 = l & 31;
+            const int w = 2 * kk + c;
+            const uint4 out = make_uint4(tile[r0][w], tile[32 + r0][w], tile[64 + r0][w], tile[96 + r0][w]);
+            uint8_t *dst = o.out + ((g * num_kb + kb0 + kk) * o.nsub + sub) * kSfBlock + c * kSfChunk + r0 * 16;
+            *reinterpret_cast<uint4 *>(dst) = out;
+        }
+        __syncthreads();
     }
 }
 
@@ -301,11 +315,12 @@ cudaError_t launch_mx_scale_relayout(const uint8_t *sA, int M, uint8_t *relA, in
     const int num_kb = K / kBK;
     RelayoutOperand a{sA, relA, M, groupA, (groupA + 127) / 128};
     RelayoutOperand b{sB, relB, N, groupB, (groupB + 127) / 128};
-    const int64_t la = static_cast<int64_t>(mxfp4_relaid_scale_bytes(M, K, groupA) / 16);
-    const int64_t lb = static_cast<int64_t>(mxfp4_relaid_scale_bytes(N, K, groupB) / 16);
-    int64_t blocks = ((la > lb ? la : lb) + 255) / 256;
-    if (blocks > 4L * num_sms)
-        blocks = 4L * num_sms;
+    const int64_t kgroups = (num_kb + 7) / 8;
+    const int64_t ba = (M + groupA - 1) / groupA * a.nsub * kgroups;
+    const int64_t bb = (N + groupB - 1) / groupB * b.nsub * kgroups;
+    int64_t blocks = ba > bb ? ba : bb;
+    if (blocks > 8L * num_sms)
+        blocks = 8L * num_sms;
     note_launch();
     mx_scale_relayout_kernel<<<dim3(static_cast<unsigned>(blocks), 2), 256, 0, s>>>(a, b, K / 32, num_kb);
     return cudaGetLastError();
@@ -315,7 +330,7 @@ cudaError_t launch_mxfp4(const Mxfp4Args &a, int num_sms, const ErrCtx &err, cud
 {
     static_assert(kSmem <= 232448, "shared memory budget");
     static_assert(kSfCol0 + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
-    cudaError_t e = cudaFuncSetAttribute(mxfp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(mxfp4_kernel), kSmem);
     if (e != cudaSuccess)
         return e;
     e = launch_mx_scale_relayout(a.sA, a.M, a.relA, kBM, a.sB, a.N, a.relB, kBN, a.K, num_sms, s);

@@ -329,7 +329,7 @@ cudaError_t launch_pair(const Mxfp4Args &a, int num_sms, const ErrCtx &err, cuda
     static_assert(ACC_BUFS * BN + C::STAGES * C::SF_COLS <= kTmemCols, "TMEM budget");
     static_assert(C::B_BYTES % 1024 == 0, "B half must be whole 8-row swizzle atoms");
     auto kern = mxfp4_pair_kernel<BN, ACC_BUFS>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), C::SMEM);
     if (e != cudaSuccess)
         return e;
     e = launch_mx_scale_relayout(a.sA, a.M, a.relA, kHalfM, a.sB, a.N, a.relB, BN, a.K, num_sms, s);

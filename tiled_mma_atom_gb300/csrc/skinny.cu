@@ -308,7 +308,7 @@ size_t skinny_counters_bytes(int64_t N)
 cudaError_t launch_skinny_tc(const SkinnyTcArgs &a, const ErrCtx &err, cudaStream_t s)
 {
     static_assert(kSmem <= 232448, "shared memory budget");
-    cudaError_t e = cudaFuncSetAttribute(skinny_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(skinny_tc_kernel), kSmem);
     if (e != cudaSuccess)
         return e;
     note_launch();

@@ -249,7 +249,7 @@ cudaError_t launch_pair(const TcArgs &a, int num_sms, const ErrCtx &err, cudaStr
     static_assert(2 * BN <= C::TMEM_COLS, "TMEM budget");
     static_assert(C::B_BYTES % 1024 == 0, "B half must be whole 8-row swizzle atoms");
     auto kern = tc2_bf16_kernel<BN>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), C::SMEM);
     if (e != cudaSuccess)
         return e;
     const int tiles = ((a.M + kBM - 1) / kBM) * ((a.N + BN - 1) / BN);

@@ -251,7 +251,7 @@ cudaError_t launch_cfg(const TcArgs &a, int num_sms, const ErrCtx &err, cudaStre
     using C = Cfg<BN, STAGES>;
     static_assert(C::SMEM <= 232448, "shared memory budget");
     auto kern = tc_bf16_kernel<BN, STAGES>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), C::SMEM);
     if (e != cudaSuccess)
         return e;
     const int tiles = ((a.M + kBM - 1) / kBM) * ((a.N + BN - 1) / BN);
@@ -269,6 +269,8 @@ cudaError_t launch_tc_bf16(const TcArgs &a, int num_sms, const ErrCtx &err, cuda
 {
     if (a.bn == 256)
         return launch_cfg<256, 4>(a, num_sms, err, s);
+    if (a.bn == 64)
+        return launch_cfg<64, 8>(a, num_sms, err, s);
     return launch_cfg<128, 6>(a, num_sms, err, s);
 }
 
