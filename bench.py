@@ -344,6 +344,12 @@ def max_over_ranks(pg, x):
     return float(t.item())
 
 
+def aggregate_tflops(world, flops_per_step, steps, slowest_rank_ms):
+    """Whole-job throughput: every rank ran `steps` replicas of the workload;
+    the job took as long as its slowest rank."""
+    return world * flops_per_step * steps / (slowest_rank_ms * 1e-3) / 1e12
+
+
 def run_reference(args, world, rank, pg):
     from tiled_mma_atom_gb300 import inputs
     w = inputs.WORKLOADS[args.workload]
@@ -423,7 +429,7 @@ def main():
     kernel_ms = sum(ms)
     kernel_ms_max = max_over_ranks(pg, kernel_ms)
     ms_per_step = kernel_ms_max / args.steps
-    value = world * w.flops * args.steps / (kernel_ms_max * 1e-3) / 1e12
+    value = aggregate_tflops(world, w.flops, args.steps, kernel_ms_max)
     rl = roofline(w, kernel_ms / args.steps, peaks, peak_kind, traffic)
 
     e2e_s, h2d, d2h = time_e2e(w, max(3, min(20, args.steps)), dev, stream)

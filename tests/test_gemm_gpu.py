@@ -342,3 +342,62 @@ def test_launch_count_increments(tmg):
     tmg.gemm(*_gpu(A, A))
     tmg.check()
     assert tmg.launch_count() == before + 1
+
+
+# ------------------------------------------------------------ edge cases
+
+def test_tc_padded_leading_dimensions(tmg):
+    """A, B with padded rows (ld = K + 8) and D with an odd row stride (no
+    16-byte stores possible: the scalar store path)."""
+    M, N, K, ldd = 200, 100, 136, 101
+    A = inputs.normal_bf16(M, K + 8, 161)
+    B = inputs.normal_bf16(N, K + 8, 162)
+    Dbuf = torch.full((M, ldd), float("nan"), dtype=torch.bfloat16, device=DEV)
+    tmg.gemm(*_gpu(A, B), Dbuf, M=M, N=N, K=K, layoutA=((M, K), (K + 8, 1)), layoutB=((N, K), (K + 8, 1)),
+             layoutD=((M, N), (ldd, 1)), path="tc")
+    tmg.check()
+    ref = parity.ref_full(A[:, :K].contiguous(), B[:, :K].contiguous(), oracle.BF16)
+    parity.check_bf16(Dbuf[:, :N], ref, K, parity.absmax(A), parity.absmax(B))
+    assert torch.isnan(Dbuf[:, N:].float()).all(), "padding of D was written"
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 1, 64), (1, 300, 64), (1, 1, 8), (257, 3, 8), (5, 7, 0)])
+def test_degenerate_shapes_auto_path(tmg, M, N, K):
+    """One-row / one-column outputs, the smallest K, and K = 0, on the
+    automatic path (bf16)."""
+    A = inputs.integer_valued(M, K, 170 + M)
+    B = inputs.integer_valued(N, K, 171 + N)
+    D = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=DEV)
+    tmg.gemm(*_gpu(A, B), D, M=M, N=N, K=K)
+    tmg.check()
+    if K == 0:
+        assert (D == 0).all()
+        return
+    parity.check_exact_bf16(parity.bf16_bits(D), parity.ref_full(A, B, oracle.BF16))
+
+
+def test_skinny_long_k_integer_exact(tmg):
+    """K = 65536 on the skinny path: each tile's K run spans many CTAs."""
+    M, N, K = 4, 256, 65536
+    A = inputs.integer_valued(M, K, 181, lo=-1, hi=1)
+    B = inputs.integer_valued(N, K, 182, lo=-1, hi=1)
+    D = tmg.gemm(*_gpu(A, B), path="skinny")
+    tmg.check()
+    parity.check_exact_bf16(parity.bf16_bits(D), parity.ref_full(A, B, oracle.BF16))
+
+
+def test_ffma_nested_output_layout(tmg):
+    """D written through a nested column mode: n = n0 + 4 n1 at n0 * 16 + n1
+    inside each row."""
+    M, N, K = 9, 16, 33
+    A = inputs.uniform_f32(M, K, 191)
+    B = inputs.uniform_f32(N, K, 192)
+    Dbuf = torch.full((M, N), float("nan"), device=DEV)
+    tmg.gemm(A.to(DEV), B.to(DEV), Dbuf, M=M, N=N, K=K, layoutD=((M, (4, 4)), (N, (4, 1))))
+    tmg.check()
+    ref = parity.ref_full(A, B, oracle.F32)
+    d = Dbuf.cpu()
+    got = torch.empty(M, N)
+    for n in range(N):
+        got[:, n] = d[:, (n % 4) * 4 + n // 4]
+    parity.check_fp32(got, ref)
