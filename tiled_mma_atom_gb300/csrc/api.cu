@@ -645,7 +645,8 @@ tmg_status tmg_gemm_mxfp4(const void *A, const void *B, const void *scaleA, cons
     {
         int dev = 0;
         cudaGetDevice(&dev);
-        const size_t ra = mxfp4_relaid_scale_bytes(M, K, 128), rb = mxfp4_relaid_scale_bytes(N, K, pair ? a.bn : 128);
+        const size_t ra = mxfp4_relaid_scale_bytes(M, K, 128, pair);
+        const size_t rb = mxfp4_relaid_scale_bytes(N, K, pair ? a.bn : 128, pair);
         uint8_t *buf = mx_scale_scratch(dev, s, ra + rb, &st);
         if (!buf)
             return st;
@@ -653,11 +654,11 @@ tmg_status tmg_gemm_mxfp4(const void *A, const void *B, const void *scaleA, cons
         a.relB = buf + ra;
         if (pair) {
             const int nsub = (a.bn + 127) / 128;
-            if ((st = encode_2d(&a.tmSA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.relA, 256, ra / 256, 256, 256, 4,
+            if ((st = encode_2d(&a.tmSA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.relA, 256, ra / 256, 256, 256, 16,
                                 CU_TENSOR_MAP_SWIZZLE_NONE)) != TMG_OK)
                 return st;
             if ((st = encode_2d(&a.tmSB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.relB, 256, rb / 256, 256, 256,
-                                4 * nsub, CU_TENSOR_MAP_SWIZZLE_NONE)) != TMG_OK)
+                                16 * nsub, CU_TENSOR_MAP_SWIZZLE_NONE)) != TMG_OK)
                 return st;
         }
     }

@@ -92,8 +92,8 @@ size_t skinny_counters_bytes(int64_t N);
 struct Mxfp4Args {
     CUtensorMap tmA;    // A codes (M, K/2) u8, box {128, 128 (one CTA) | 128 (pair half)}, 128B swizzle
     CUtensorMap tmB;    // B codes (N, K/2) u8, box {128, 128 | bn/2}
-    CUtensorMap tmSA;   // pair kernel: relaid A scales as rows of 256 bytes, box {256, 4}
-    CUtensorMap tmSB;   // pair kernel: relaid B scales, box {256, 4 * ceil(bn/128)}
+    CUtensorMap tmSA;   // pair kernel: relaid A scales (wide form) as rows of 256 bytes, box {256, 16}
+    CUtensorMap tmSB;   // pair kernel: relaid B scales (wide form), box {256, 16 * ceil(bn/128)}
     const uint8_t *sA;  // (M, K/32) e8m0
     const uint8_t *sB;  // (N, K/32) e8m0
     uint8_t *relA;      // scratch: sA relaid in the tensor core's chunk order
@@ -108,10 +108,12 @@ cudaError_t launch_mxfp4(const Mxfp4Args &a, int num_sms, const ErrCtx &err, cud
 // CTA-pair kernel (256 x bn tiles), also two launches.
 cudaError_t launch_mxfp4_pair(const Mxfp4Args &a, int num_sms, const ErrCtx &err, cudaStream_t s);
 int mxfp4_pair_pick_bn(int64_t M, int64_t N, int num_sms);
-// Relaid scale bytes for `rows` rows grouped by `group_rows` (see mx_common.cuh).
-size_t mxfp4_relaid_scale_bytes(int64_t rows, int64_t K, int group_rows);
+// Relaid scale bytes for `rows` rows grouped by `group_rows`, compact or
+// wide form (see mx_common.cuh).
+size_t mxfp4_relaid_scale_bytes(int64_t rows, int64_t K, int group_rows, bool wide);
 cudaError_t launch_mx_scale_relayout(const uint8_t *sA, int M, uint8_t *relA, int groupA, const uint8_t *sB,
-                                     int N, uint8_t *relB, int groupB, int K, int num_sms, cudaStream_t s);
+                                     int N, uint8_t *relB, int groupB, int K, bool wide, int num_sms,
+                                     cudaStream_t s);
 
 // Probe kernel for the bounded wait (never signalled barrier).
 cudaError_t launch_wait_probe(const ErrCtx &err, cudaStream_t s);

@@ -5,11 +5,17 @@
 // Scales of one operand are relaid (pre-pass, mx_scale_relayout in mxfp4.cu)
 // into groups of `group_rows` rows (the rows one CTA or one pair tile
 // consumes); for each group and each 256-element K block there are
-// nsub = ceil(group_rows / 128) blocks of 1 KB, each two 512-byte chunks;
-// chunk c holds K-blocks 4c..4c+3, and its 16-byte line r0 (0..31) holds the
-// scales of sub-block rows r0, r0+32, r0+64, r0+96 — the order that
-// tcgen05.cp 32x128b.warpx4 writes to TMEM (lane = row mod 32, column = row
-// / 32, byte = K-block), which is how the block-scaled MMA reads them.
+// nsub = ceil(group_rows / 128) sub-blocks of 128 rows, each two 512-byte
+// chunks; chunk c holds K-blocks 4c..4c+3, and its 16-byte line r0 (0..31)
+// holds the scales of sub-block rows r0, r0+32, r0+64, r0+96 — the order in
+// which TMEM must hold them (lane = row mod 32 in every lane quarter,
+// column = row / 32, byte = K-block) for the block-scaled MMA.
+//   compact form (one-CTA kernel): per (group, K block) the nsub sub-blocks
+//     of 1 KB, [chunk 0][chunk 1] each; copied with 32x128b.warpx4.
+//   wide form (pair kernel): per (group, K block) nsub x 4 KB; wide copy p
+//     (p < nsub) takes the 4 KB at p x 4 KB = [X x4][Y x4], the chunks for
+//     its columns 0-3 and 4-7: (chunk 0, chunk 1) of the one sub-block when
+//     nsub = 1, (sub-block 0, sub-block 1) of chunk p when nsub = 2.
 #pragma once
 
 #include "internal.h"
@@ -85,6 +91,30 @@ __device__ __forceinline__ void tmem_cp_chunk_pair(uint32_t taddr, uint64_t sdes
 {
     asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
                  : "memory");
+}
+
+// Wide copies: 128 lanes x 32 bytes (8 TMEM columns) per instruction.  Each
+// tcgen05.cp costs the tensor pipe about the same whatever its width, so the
+// pair kernel moves its scales with these: the source holds, for lane l, the
+// 16-byte line (l mod 32) of two chunks — i.e. each 512-byte chunk repeated
+// four times — as two 2 KB halves (columns 0-3 from the first, 4-7 from the
+// second).  Descriptor: no swizzle, 8-row x 16-byte core matrices 128 bytes
+// apart, the two 16-byte column halves 2 KB apart.
+constexpr int kWideSrcBytes = 4096;
+
+__device__ __forceinline__ uint64_t sdesc_wide_scales(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(2048 >> 4) << 16;     // leading byte offset: next 16-byte column half
+    d |= static_cast<uint64_t>(128 >> 4) << 32;      // stride byte offset: next 8-row group
+    d |= static_cast<uint64_t>(1) << 46;
+    return d;
+}
+
+__device__ __forceinline__ void tmem_cp_wide_pair(uint32_t taddr, uint64_t sdesc)
+{
+    asm volatile("tcgen05.cp.cta_group::2.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
 }  // namespace mx

@@ -66,6 +66,7 @@ struct RelayoutOperand {
     const uint8_t *S;
     uint8_t *out;
     int rows, group_rows, nsub;
+    int wide;          // write the wide form (see mx_common.cuh)
 };
 
 // A CTA takes one 128-row sub-block and up to 8 consecutive K blocks: it
@@ -98,11 +99,22 @@ __global__ void __launch_bounds__(256)
             tile[r][2 * kk + 1] = v.y;
         }
         __syncthreads();
-        for (int l = threadIdx.x; l < nk * 64; l += 256) {
-            const int kk = l >> 6, c = (l >> 5) & 1, r0 = l & 31;
+        const int reps = o.wide ? 4 : 1;
+        for (int l = threadIdx.x; l < nk * 64 * reps; l += 256) {
+            const int rep = l % reps, l1 = l / reps;
+            const int kk = l1 >> 6, c = (l1 >> 5) & 1, r0 = l1 & 31;
             const int w = 2 * kk + c;
             const uint4 out = make_uint4(tile[r0][w], tile[32 + r0][w], tile[64 + r0][w], tile[96 + r0][w]);
-            uint8_t *dst = o.out + ((g * num_kb + kb0 + kk) * o.nsub + sub) * kSfBlock + c * kSfChunk + r0 * 16;
+            const int64_t blk = g * num_kb + kb0 + kk;
+            uint8_t *dst;
+            if (!o.wide) {
+                dst = o.out + (blk * o.nsub + sub) * kSfBlock + c * kSfChunk + r0 * 16;
+            } else {
+                // copy p, half j: nsub == 1 -> (p, j) = (0, c); nsub == 2 -> (c, sub)
+                const int p = o.nsub == 1 ? 0 : c;
+                const int j = o.nsub == 1 ? c : sub;
+                dst = o.out + blk * o.nsub * kWideSrcBytes + p * kWideSrcBytes + j * 2048 + rep * kSfChunk + r0 * 16;
+            }
             *reinterpret_cast<uint4 *>(dst) = out;
         }
         __syncthreads();
@@ -302,19 +314,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-size_t mxfp4_relaid_scale_bytes(int64_t rows, int64_t K, int group_rows)
+size_t mxfp4_relaid_scale_bytes(int64_t rows, int64_t K, int group_rows, bool wide)
 {
     const int64_t groups = (rows + group_rows - 1) / group_rows;
     const int64_t nsub = (group_rows + 127) / 128;
-    return static_cast<size_t>(groups * nsub * (K / kBK) * kSfBlock);
+    return static_cast<size_t>(groups * nsub * (K / kBK) * (wide ? kWideSrcBytes : kSfBlock));
 }
 
 cudaError_t launch_mx_scale_relayout(const uint8_t *sA, int M, uint8_t *relA, int groupA, const uint8_t *sB,
-                                     int N, uint8_t *relB, int groupB, int K, int num_sms, cudaStream_t s)
+                                     int N, uint8_t *relB, int groupB, int K, bool wide, int num_sms,
+                                     cudaStream_t s)
 {
     const int num_kb = K / kBK;
-    RelayoutOperand a{sA, relA, M, groupA, (groupA + 127) / 128};
-    RelayoutOperand b{sB, relB, N, groupB, (groupB + 127) / 128};
+    RelayoutOperand a{sA, relA, M, groupA, (groupA + 127) / 128, wide ? 1 : 0};
+    RelayoutOperand b{sB, relB, N, groupB, (groupB + 127) / 128, wide ? 1 : 0};
     const int64_t kgroups = (num_kb + 7) / 8;
     const int64_t ba = (M + groupA - 1) / groupA * a.nsub * kgroups;
     const int64_t bb = (N + groupB - 1) / groupB * b.nsub * kgroups;
@@ -333,7 +346,7 @@ cudaError_t launch_mxfp4(const Mxfp4Args &a, int num_sms, const ErrCtx &err, cud
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(mxfp4_kernel), kSmem);
     if (e != cudaSuccess)
         return e;
-    e = launch_mx_scale_relayout(a.sA, a.M, a.relA, kBM, a.sB, a.N, a.relB, kBN, a.K, num_sms, s);
+    e = launch_mx_scale_relayout(a.sA, a.M, a.relA, kBM, a.sB, a.N, a.relB, kBN, a.K, false, num_sms, s);
     if (e != cudaSuccess)
         return e;
     const int tiles = ((a.M + kBM - 1) / kBM) * ((a.N + kBN - 1) / kBN);

@@ -40,12 +40,12 @@ struct MxPairCfg {
     static constexpr int NSUB = (BN + 127) / 128;
     static constexpr int A_BYTES = kHalfM * kBKBytes;          // 16 KB
     static constexpr int B_BYTES = (BN / 2) * kBKBytes;
-    static constexpr int SFA_BYTES = kSfBlock;
-    static constexpr int SFB_BYTES = NSUB * kSfBlock;
+    static constexpr int SFA_BYTES = kWideSrcBytes;
+    static constexpr int SFB_BYTES = NSUB * kWideSrcBytes;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
     static constexpr int SF_COLS = 8 + 8 * NSUB;                 // per stage
     static constexpr int TMEM_STAGES = (kTmemCols - ACC_BUFS * BN) / SF_COLS;
-    static constexpr int SMEM_STAGES = (220 * 1024 - 2048) / STAGE_BYTES;
+    static constexpr int SMEM_STAGES = (230 * 1024 - 2048) / STAGE_BYTES;
     static constexpr int STAGES0 = TMEM_STAGES < SMEM_STAGES ? TMEM_STAGES : SMEM_STAGES;
     static constexpr int STAGES = STAGES0 > 8 ? 8 : STAGES0;
     static constexpr int BAR_BYTES = (2 * STAGES + 4) * 8 + 16;
@@ -134,8 +134,8 @@ __global__ void __launch_bounds__(pair_threads(ACC_BUFS), 1)
                 int tm, tn;
                 tile_coords(t, tiles_m, tiles_n, tm, tn);
                 // rows (of 256 bytes) of this CTA's / this tile's relaid scales
-                const int sfa_row0 = (tm * 2 + static_cast<int>(rank)) * num_kb * (kSfBlock / 256);
-                const int sfb_row0 = tn * num_kb * NSUB * (kSfBlock / 256);
+                const int sfa_row0 = (tm * 2 + static_cast<int>(rank)) * num_kb * (C::SFA_BYTES / 256);
+                const int sfb_row0 = tn * num_kb * (C::SFB_BYTES / 256);
                 for (int kb = 0; kb < num_kb; ++kb) {
                     if (!mbar_wait_cluster(&empty[stage], phase ^ 1u, err, abort_flag, kSiteProducerEmpty)) {
                         ok = false;
@@ -148,9 +148,8 @@ __global__ void __launch_bounds__(pair_threads(ACC_BUFS), 1)
                                      tm * kBM + static_cast<int>(rank) * kHalfM);
                     tma_load_2d_pair(tB + stage * C::B_BYTES, &tmB, bar0, kb * kBKBytes,
                                      tn * BN + static_cast<int>(rank) * (BN / 2));
-                    tma_load_2d_pair(sfA + stage * C::SFA_BYTES, &tmSA, bar0, 0, sfa_row0 + kb * (kSfBlock / 256));
-                    tma_load_2d_pair(sfB + stage * C::SFB_BYTES, &tmSB, bar0, 0,
-                                     sfb_row0 + kb * NSUB * (kSfBlock / 256));
+                    tma_load_2d_pair(sfA + stage * C::SFA_BYTES, &tmSA, bar0, 0, sfa_row0 + kb * (C::SFA_BYTES / 256));
+                    tma_load_2d_pair(sfB + stage * C::SFB_BYTES, &tmSB, bar0, 0, sfb_row0 + kb * (C::SFB_BYTES / 256));
                     ++issued;
                     if (++stage == STAGES) {
                         stage = 0;
@@ -192,16 +191,14 @@ __global__ void __launch_bounds__(pair_threads(ACC_BUFS), 1)
                     tc_fence_after();
                     const uint32_t sfa_col = tmem_base + ACC_BUFS * BN + stage * C::SF_COLS;
                     const uint32_t sfb_col = sfa_col + 8;
+                    // 1 + NSUB wide copies: A scales (both K-block groups),
+                    // then B scales per K-block group (NSUB = 2) or both
+                    // groups at once (NSUB = 1)
+                    tmem_cp_wide_pair(sfa_col, sdesc_wide_scales(smem_u32(sfA + stage * C::SFA_BYTES)));
 #pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        tmem_cp_chunk_pair(sfa_col + c * 4,
-                                           sdesc_noswizzle_rows16(smem_u32(sfA + stage * C::SFA_BYTES + c * kSfChunk)));
-#pragma unroll
-                        for (int sub = 0; sub < NSUB; ++sub)
-                            tmem_cp_chunk_pair(sfb_col + c * 4 * NSUB + sub * 4,
-                                               sdesc_noswizzle_rows16(smem_u32(sfB + stage * C::SFB_BYTES +
-                                                                               sub * kSfBlock + c * kSfChunk)));
-                    }
+                    for (int p = 0; p < NSUB; ++p)
+                        tmem_cp_wide_pair(sfb_col + 8 * p,
+                                          sdesc_wide_scales(smem_u32(sfB + stage * C::SFB_BYTES + p * kWideSrcBytes)));
                     const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(tA + stage * C::A_BYTES));
                     const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(tB + stage * C::B_BYTES));
 #pragma unroll
@@ -332,7 +329,7 @@ cudaError_t launch_pair(const Mxfp4Args &a, int num_sms, const ErrCtx &err, cuda
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), C::SMEM);
     if (e != cudaSuccess)
         return e;
-    e = launch_mx_scale_relayout(a.sA, a.M, a.relA, kHalfM, a.sB, a.N, a.relB, BN, a.K, num_sms, s);
+    e = launch_mx_scale_relayout(a.sA, a.M, a.relA, kHalfM, a.sB, a.N, a.relB, BN, a.K, true, num_sms, s);
     if (e != cudaSuccess)
         return e;
     const int tiles = ((a.M + kBM - 1) / kBM) * ((a.N + BN - 1) / BN);
