@@ -205,6 +205,36 @@ def test_tc_pair_each_tile_width_vs_oracle(tmg, shape, width):
     parity.check_bf16(D, parity.ref_full(A, B, oracle.BF16), K, parity.absmax(A), parity.absmax(B))
 
 
+@pytest.mark.parametrize("width", [128, 192, 224, 256])
+def test_tc_pair_stream_k_tail_exact(tmg, width, monkeypatch):
+    """2048 x 2560 leaves a partial last wave for every pair tile width, so
+    the last tiles run stream-K and are summed from fp32 partials.  Integer
+    inputs: bit-exact; twice in a row (the tile counters reset themselves)."""
+    monkeypatch.setenv("TMG_TC_PAIR_BN", str(width))
+    M, N, K = 2048, 2560, 1024
+    A = inputs.integer_valued(M, K, 200 + width)
+    B = inputs.integer_valued(N, K, 201 + width)
+    dA, dB = _gpu(A, B)
+    D1 = tmg.gemm(dA, dB, path="tc_pair").clone()
+    D2 = tmg.gemm(dA, dB, path="tc_pair")
+    tmg.check()
+    assert torch.equal(D1, D2)
+    parity.check_exact_bf16(parity.bf16_bits(D2), parity.ref_full(A, B, oracle.BF16))
+
+
+def test_tc_pair_stream_k_random_vs_oracle(tmg):
+    """Random inputs through the stream-K tail (4096 x 4096 has 256 tiles of
+    256 columns over 76 pairs); sampled outputs in the split tiles' region."""
+    M, N, K = 4096, 4096, 512
+    A = inputs.normal_bf16(M, K, 211)
+    B = inputs.normal_bf16(N, K, 212)
+    D = tmg.gemm(*_gpu(A, B), path="tc_pair")
+    tmg.check()
+    ms, ns = parity.sample_coords(M, N, 30000, seed=9)
+    ref = parity.ref_entries(A, B, oracle.BF16, ms, ns)
+    parity.check_bf16_values(parity.to_f64(D)[ms, ns], ref, K, parity.absmax(A), parity.absmax(B))
+
+
 @pytest.mark.parametrize("M,N,K", [(300, 333, 200), (640, 1000, 520), (256, 16, 64)])
 def test_tc_pair_ragged_integer_exact(tmg, M, N, K):
     """Ragged pair tiles (row half of the second CTA partly or wholly out of

@@ -56,6 +56,10 @@ struct Scratch {
     size_t counters_bytes = 0;
     uint8_t *mx_scales = nullptr;      // MXFP4 scales in chunk order
     size_t mx_scales_bytes = 0;
+    float *tc2_partials = nullptr;     // pair kernel stream-K partial tiles
+    size_t tc2_partials_bytes = 0;
+    uint32_t *tc2_counters = nullptr;  // pair kernel stream-K tile counters
+    size_t tc2_counters_bytes = 0;
 };
 std::map<std::pair<int, uintptr_t>, Scratch> g_scratch;
 
@@ -365,6 +369,43 @@ uint8_t *mx_scale_scratch(int dev, cudaStream_t s, size_t bytes, tmg_status *st)
 }
 
 // mode: 0 = choose, 1 = one-CTA tiles, 2 = CTA-pair tiles.
+// Per-(device, stream) stream-K scratch of the pair kernel, grown on demand;
+// counters are zeroed when allocated and reset by the kernel after use.
+tmg_status tc2_scratch(int dev, cudaStream_t s, TcArgs &a)
+{
+    const size_t pb = tc2_partials_bytes(a), cb = tc2_counters_bytes(a);
+    a.partials = nullptr;
+    a.counters = nullptr;
+    if (pb == 0)
+        return TMG_OK;
+    std::lock_guard<std::mutex> lk(g_mu);
+    Scratch &sc = g_scratch[{dev, reinterpret_cast<uintptr_t>(s)}];
+    cudaError_t e;
+    if (sc.tc2_partials_bytes < pb) {
+        if (sc.tc2_partials)
+            cudaFree(sc.tc2_partials);
+        sc.tc2_partials = nullptr;
+        sc.tc2_partials_bytes = 0;
+        if ((e = cudaMalloc(&sc.tc2_partials, pb)) != cudaSuccess)
+            return cuda_fail(e, "cudaMalloc(pair stream-K partials)");
+        sc.tc2_partials_bytes = pb;
+    }
+    if (sc.tc2_counters_bytes < cb) {
+        if (sc.tc2_counters)
+            cudaFree(sc.tc2_counters);
+        sc.tc2_counters = nullptr;
+        sc.tc2_counters_bytes = 0;
+        if ((e = cudaMalloc(&sc.tc2_counters, cb)) != cudaSuccess)
+            return cuda_fail(e, "cudaMalloc(pair stream-K counters)");
+        if ((e = cudaMemsetAsync(sc.tc2_counters, 0, cb, s)) != cudaSuccess)
+            return cuda_fail(e, "cudaMemsetAsync(pair stream-K counters)");
+        sc.tc2_counters_bytes = cb;
+    }
+    a.partials = sc.tc2_partials;
+    a.counters = sc.tc2_counters;
+    return TMG_OK;
+}
+
 tmg_status run_tc(const DeviceState &ds, const TcPlan &p, void *D, int64_t K, int mode, cudaStream_t s)
 {
     TcArgs a;
@@ -379,6 +420,11 @@ tmg_status run_tc(const DeviceState &ds, const TcPlan &p, void *D, int64_t K, in
     int box_b;
     if (pair) {
         a.bn = tc2_pick_bn(p.M, p.N, ds.num_sms);
+        if (const char *f = getenv("TMG_TC_PAIR_BN")) {      // testing aid: 128 | 192 | 224 | 256
+            const int v = atoi(f);
+            if (v == 128 || v == 192 || v == 224 || v == 256)
+                a.bn = v;
+        }
         box_b = a.bn / 2;
     } else {
         // widest tile that still gives every SM work; 64 for small problems
@@ -401,6 +447,13 @@ tmg_status run_tc(const DeviceState &ds, const TcPlan &p, void *D, int64_t K, in
     a.M = static_cast<int>(p.M);
     a.N = static_cast<int>(p.N);
     a.K = static_cast<int>(K);
+    if (pair) {
+        tc2_plan(a, ds.num_sms);
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if ((st = tc2_scratch(dev, s, a)) != TMG_OK)
+            return st;
+    }
     cudaError_t e = pair ? launch_tc2_bf16(a, ds.num_sms, err_ctx(ds), s) : launch_tc_bf16(a, ds.num_sms, err_ctx(ds), s);
     return e == cudaSuccess ? TMG_OK : cuda_fail(e, pair ? "tc2_bf16 launch" : "tc_bf16 launch");
 }
@@ -758,9 +811,14 @@ tmg_status tmg_check(void *stream)
         cudaGetDevice(&dev);
         {
             std::lock_guard<std::mutex> lk(g_mu);
-            for (auto &kv : g_scratch)
-                if (kv.first.first == dev && kv.second.counters)
+            for (auto &kv : g_scratch) {
+                if (kv.first.first != dev)
+                    continue;
+                if (kv.second.counters)
                     cudaMemset(kv.second.counters, 0, kv.second.counters_bytes);
+                if (kv.second.tc2_counters)
+                    cudaMemset(kv.second.tc2_counters, 0, kv.second.tc2_counters_bytes);
+            }
         }
         cudaDeviceSynchronize();
         return fail(TMG_ERR_TIMEOUT, "a kernel wait ran out of its budget (error word 0x%08x, site %u)", w,
@@ -802,6 +860,10 @@ void tmg_shutdown(void)
             cudaFree(kv.second.counters);
         if (kv.second.mx_scales)
             cudaFree(kv.second.mx_scales);
+        if (kv.second.tc2_partials)
+            cudaFree(kv.second.tc2_partials);
+        if (kv.second.tc2_counters)
+            cudaFree(kv.second.tc2_counters);
     }
     g_scratch.clear();
     cudaSetDevice(cur);

@@ -47,18 +47,28 @@ cudaError_t launch_zero_fill(void *D, const DevLayout &ld, int64_t M, int64_t N,
 // ------------------------------------------------------ tcgen05 bf16 path
 struct TcArgs {
     CUtensorMap tmA;   // A (M,K) bf16 K-major, box {64, 128}, 128B swizzle
-    CUtensorMap tmB;   // B (N,K) bf16 K-major, box {64, BN}, 128B swizzle
+    CUtensorMap tmB;   // B (N,K) bf16 K-major, box {64, BN} (pair kernel: {64, BN/2}), 128B swizzle
     void *D;           // bf16 (M,N), row stride ldd elements, unit column stride
     int64_t ldd;
     int M, N, K;
     int bn;            // tile width (N per tile)
+    // pair kernel schedule (tc2_plan) and its stream-K scratch
+    int pairs;         // clusters launched
+    int dp_tiles;      // tiles run data-parallel
+    int sk_tiles;      // tiles after them, run stream-K
+    float *partials;   // tc2_partials_bytes()
+    uint32_t *counters;  // tc2_counters_bytes(), zero on entry
 };
 cudaError_t launch_tc_bf16(const TcArgs &a, int num_sms, const ErrCtx &err, cudaStream_t s);
 // CTA-pair variant (cta_group::2, 256 x bn tiles; bn in {256, 224, 192, 128},
-// tmB box {64, bn/2}).
+// tmB box {64, bn/2}).  Call tc2_plan first, then provide the scratch.
 cudaError_t launch_tc2_bf16(const TcArgs &a, int num_sms, const ErrCtx &err, cudaStream_t s);
-// Pair-tile width that best fills the last wave for an M x N output.
+// Pair-tile width for an M x N output.
 int tc2_pick_bn(int64_t M, int64_t N, int num_sms);
+// Fill pairs / dp_tiles / sk_tiles for a.M, a.N, a.K, a.bn.
+void tc2_plan(TcArgs &a, int num_sms);
+size_t tc2_partials_bytes(const TcArgs &a);
+size_t tc2_counters_bytes(const TcArgs &a);
 
 // ---------------------------------------------------- skinny swap-AB path
 struct SkinnyTcArgs {
