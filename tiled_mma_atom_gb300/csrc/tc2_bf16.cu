@@ -17,12 +17,10 @@
 //
 // Schedule.  A pair MMA costs nearly the same whatever its width, so tiles
 // are as wide as possible (BN = 256 unless the last column tile would be
-// mostly empty).  When the tile count is not a multiple of the P pairs, the
-// tiles of all but the last full wave run data-parallel (pair c takes tiles
-// c, c + P, ... in grouped order), and the remaining 1-2 waves' worth run
-// stream-K: their (tile, K block) units are cut into P equal contiguous runs,
-// one per pair, which each pair works through before its data-parallel
-// tiles.  A tile split across pairs leaves fp32 partial sums in
+// mostly empty).  When the tile count is not a multiple of the P pairs, 1-2
+// waves' worth of tiles run stream-K — their (tile, K block) units cut into
+// P equal contiguous runs, one per pair — and the rest data-parallel (pair c
+// takes c, c + P, ...); each pair does its stream-K run first.  A tile split across pairs leaves fp32 partial sums in
 // scratch; the last pair to finish a piece of it (a counter per tile, CTA
 // and epilogue warp) adds the partials in pair order — a fixed order, so the
 // result does not depend on timing — rounds to bf16 and resets the counter.
@@ -65,17 +63,19 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
 
 // Per-pair walk over its segments: its stream-K run first, then its
 // data-parallel tiles, so the fix-ups of split tiles overlap the
-// data-parallel work instead of trailing it.  Every role of both CTAs walks
-// the same sequence.
+// data-parallel work instead of trailing it.  The stream-K tiles are the
+// first sk_tiles of the grouped order and the data-parallel ones follow, so
+// the pairs sweep the grouped order front to back (operand panels stay in
+// L2 while they are used).  Every role of both CTAs walks the same sequence.
 struct SegWalk {
-    int nclusters, dp_tiles, num_kb;
+    int nclusters, dp_tiles, sk_tiles, num_kb;
     int64_t u, u_end;          // stream-K units of this pair (relative to the stream-K region)
     int next_dp;               // next data-parallel tile
     int sk_seg;                // stream-K segments handed out so far
 
-    __device__ SegWalk(int c, int nc, int dp, int sk_tiles, int nkb) : nclusters(nc), dp_tiles(dp), num_kb(nkb)
+    __device__ SegWalk(int c, int nc, int dp, int sk, int nkb) : nclusters(nc), dp_tiles(dp), sk_tiles(sk), num_kb(nkb)
     {
-        const int64_t U = static_cast<int64_t>(sk_tiles) * nkb;
+        const int64_t U = static_cast<int64_t>(sk) * nkb;
         u = U * c / nc;
         u_end = U * (c + 1) / nc;
         next_dp = c;
@@ -89,7 +89,7 @@ struct SegWalk {
         if (u >= u_end) {
             if (next_dp >= dp_tiles)
                 return false;
-            tile = next_dp;
+            tile = sk_tiles + next_dp;
             next_dp += nclusters;
             kb0 = 0;
             kb1 = num_kb;
@@ -101,7 +101,7 @@ struct SegWalk {
         kb0 = static_cast<int>(u % num_kb);
         const int64_t left = u_end - u;
         kb1 = left < static_cast<int64_t>(num_kb - kb0) ? kb0 + static_cast<int>(left) : num_kb;
-        tile = dp_tiles + rel;
+        tile = rel;
         partial = !(kb0 == 0 && kb1 == num_kb);
         slot = sk_seg == 0 ? 0 : 1;
         ++sk_seg;
@@ -339,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
             __threadfence();
             __syncwarp();
-            const int rel = tile - dp_tiles;
+            const int rel = tile;
             const int c_first = unit_owner(static_cast<int64_t>(rel) * num_kb, U, nclusters);
             const int c_last = unit_owner(static_cast<int64_t>(rel + 1) * num_kb - 1, U, nclusters);
             uint32_t *counter = counters + (static_cast<int64_t>(rel) * 2 + rank) * 4 + q;
@@ -358,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = 0; j < 32; ++j)
                     v[j] = 0.f;
                 for (int cc = c_first; cc <= c_last; ++cc) {
-                    const int first_tile = dp_tiles + static_cast<int>((U * cc / nclusters) / num_kb);
+                    const int first_tile = static_cast<int>((U * cc / nclusters) / num_kb);
                     const int s2 = first_tile == tile ? 0 : 1;
                     const float4 *src = reinterpret_cast<const float4 *>(
                         partials + ((static_cast<int64_t>(2 * cc + s2) * 2 + rank) * 4 + q) * warp_elems);
