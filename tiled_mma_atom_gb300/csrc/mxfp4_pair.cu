@@ -1,17 +1,24 @@
 // mxfp4_pair.cu — the MXFP4 GEMM of mxfp4.cu on CTA pairs
 // (tcgen05.mma.cta_group::2.kind::mxf4.block_scale, M = 256).
 //
-// Each cluster of two CTAs computes a 256 x BN tile (BN = 192 or 128).  CTA r
+// Each cluster of two CTAs computes a 256 x BN tile (BN = 256, 192 or 128).  CTA r
 // keeps in its own shared memory rows 128r..128r+127 of the A codes, rows
 // r·BN/2.. of the B codes, the scales of its own 128 A rows and the scales
 // of all BN B rows (its tensor core multiplies its 128 rows by every column
 // of the tile, so it needs every B scale).  All four loads of both CTAs are
-// TMA copies completing on CTA 0's `full` barrier.  CTA 0's MMA lane copies
-// the scale chunks of both CTAs into their TMEM with one
-// tcgen05.cp.cta_group::2 per chunk, then issues the pair MMAs.  TMEM per
-// CTA: two BN-column accumulators plus, per stage, 8 columns of A scales and
-// 8·ceil(BN/128) columns of B scales (B rows 0-127 in the first 4 columns of
-// each K-block group, rows 128.. in the next 4).
+// TMA copies completing on CTA 0's `full` barrier.  Warp roles: 0 TMA
+// producer; 1 MMA issuer (CTA 0); 2 scale copier (CTA 0), which moves each
+// stage's scales of both CTAs into their TMEM with wide
+// tcgen05.cp.cta_group::2 copies and commits to the stage's `sready`
+// barrier; the rest epilogue.  Keeping the copies out of the MMA lane's
+// instruction stream lets it queue MMAs back to back (measured on MXFP4
+// 8192³: 218 -> 209 µs).  TMEM per CTA: the accumulator(s) plus, per stage,
+// 8 columns of A scales and 8·ceil(BN/128) columns of B scales (B rows 0-127
+// in the first 4 columns of each K-block group, rows 128.. in the next 4).
+// A stage's scale columns are rewritten only after its `full` barrier
+// completes again, which needs the stage's `empty` commit — issued after
+// the MMAs that read those columns — so the copier never overwrites scales
+// still in use.
 //
 // The FlyDSL pages express the product with scaled MFMA/WMMA atoms (E8M0
 // scale per 32 K elements: "FlyDSL Kernel Authoring Skill", §6, MX-scaled
@@ -29,9 +36,11 @@ using namespace mx;
 
 constexpr int kBM = 256;
 constexpr int kHalfM = 128;
-// warps 0-1 (producer, MMA) + epilogue warps: 4 with two accumulators, 8
-// with one (two warps per TMEM lane quarter, each draining half the columns)
-__host__ __device__ constexpr int pair_threads(int acc_bufs) { return acc_bufs == 1 ? 320 : 192; }
+// warps 0-2 (producer, MMA, scale copier) + epilogue warps: 4 with two
+// accumulators, 8 with one (two warps per TMEM lane quarter, each draining
+// half the columns)
+constexpr int kFirstEpiWarp = 3;
+__host__ __device__ constexpr int pair_threads(int acc_bufs) { return acc_bufs == 1 ? 352 : 224; }
 constexpr int kGroupM = 8;
 constexpr int kTmemCols = 512;
 
@@ -48,7 +57,7 @@ struct MxPairCfg {
     static constexpr int SMEM_STAGES = (230 * 1024 - 2048) / STAGE_BYTES;
     static constexpr int STAGES0 = TMEM_STAGES < SMEM_STAGES ? TMEM_STAGES : SMEM_STAGES;
     static constexpr int STAGES = STAGES0 > 8 ? 8 : STAGES0;
-    static constexpr int BAR_BYTES = (2 * STAGES + 4) * 8 + 16;
+    static constexpr int BAR_BYTES = (3 * STAGES + 4) * 8 + 16;
     static constexpr int SMEM = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
 };
 
@@ -86,7 +95,8 @@ __global__ void __launch_bounds__(pair_threads(ACC_BUFS), 1)
     uint64_t *empty = full + STAGES;
     uint64_t *tfull = empty + STAGES;
     uint64_t *tempty = tfull + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
+    uint64_t *sready = tempty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sready + STAGES);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -100,10 +110,11 @@ __global__ void __launch_bounds__(pair_threads(ACC_BUFS), 1)
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
+            mbar_init(&sready[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
-            mbar_init(&tempty[b], 2 * (pair_threads(ACC_BUFS) / 32 - 2));   // epilogue warps of both CTAs
+            mbar_init(&tempty[b], 2 * (pair_threads(ACC_BUFS) / 32 - kFirstEpiWarp));   // epilogue warps of both CTAs
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -188,17 +199,14 @@ __global__ void __launch_bounds__(pair_threads(ACC_BUFS), 1)
                         ok = false;
                         break;
                     }
+                    // the stage's scales are in TMEM once `sready` completes
+                    if (!mbar_wait_cluster(&sready[stage], phase, err, abort_flag, kSiteMmaFull)) {
+                        ok = false;
+                        break;
+                    }
                     tc_fence_after();
                     const uint32_t sfa_col = tmem_base + ACC_BUFS * BN + stage * C::SF_COLS;
                     const uint32_t sfb_col = sfa_col + 8;
-                    // 1 + NSUB wide copies: A scales (both K-block groups),
-                    // then B scales per K-block group (NSUB = 2) or both
-                    // groups at once (NSUB = 1)
-                    tmem_cp_wide_pair(sfa_col, sdesc_wide_scales(smem_u32(sfA + stage * C::SFA_BYTES)));
-#pragma unroll
-                    for (int p = 0; p < NSUB; ++p)
-                        tmem_cp_wide_pair(sfb_col + 8 * p,
-                                          sdesc_wide_scales(smem_u32(sfB + stage * C::SFB_BYTES + p * kWideSrcBytes)));
                     const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(tA + stage * C::A_BYTES));
                     const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(tB + stage * C::B_BYTES));
 #pragma unroll
@@ -220,6 +228,37 @@ __global__ void __launch_bounds__(pair_threads(ACC_BUFS), 1)
                 mma_commit_pair(&tfull[acc], 0x3);
             }
         }
+    } else if (warp == 2) {
+        if (lane == 0 && rank == 0) {
+            // --------------------------------------------- scale copier
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int t = cluster; t < num_tiles && ok; t += nclusters) {
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait_cluster(&full[stage], phase, err, abort_flag, kSiteMmaFull)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sfa_col = tmem_base + ACC_BUFS * BN + stage * C::SF_COLS;
+                    const uint32_t sfb_col = sfa_col + 8;
+                    // 1 + NSUB wide copies: A scales (both K-block groups),
+                    // then B scales per K-block group (NSUB = 2) or both
+                    // groups at once (NSUB = 1)
+                    tmem_cp_wide_pair(sfa_col, sdesc_wide_scales(smem_u32(sfA + stage * C::SFA_BYTES)));
+#pragma unroll
+                    for (int p = 0; p < NSUB; ++p)
+                        tmem_cp_wide_pair(sfb_col + 8 * p,
+                                          sdesc_wide_scales(smem_u32(sfB + stage * C::SFB_BYTES + p * kWideSrcBytes)));
+                    mma_commit_pair(&sready[stage], 0x1);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
     } else {
         // ---------------------------------------------------- epilogue
         const int q = warp & 3;
@@ -238,7 +277,7 @@ __global__ void __launch_bounds__(pair_threads(ACC_BUFS), 1)
                 // drain this warp's half of the columns first so the next
                 // tile's MMAs can start, then store
                 constexpr int HALF = BN / 2;
-                const int h = (warp - 2) / 4;
+                const int h = (warp - kFirstEpiWarp) / 4;
                 uint32_t packed[HALF / 2];
 #pragma unroll
                 for (int c = 0; c < HALF / 32; ++c) {
