@@ -23,6 +23,10 @@ _LIB = os.path.join(_HERE, "liboracle.so")
 
 F32 = 0
 BF16 = 1
+E4M3 = 2
+
+# Epilogues of the fused GEMM (see orc_gemm_fused in oracle.c).
+EPILOGUES = {"none": 0, "bias": 1, "bias_relu": 2, "bias_silu": 3, "bias_gelu": 4}
 
 
 class Layout(ctypes.Structure):
@@ -99,6 +103,14 @@ def lib():
         L.orc_decode_f32.restype = ctypes.c_double
         L.orc_decode_e2m1.argtypes = [ctypes.c_uint8]
         L.orc_decode_e2m1.restype = ctypes.c_double
+        L.orc_decode_e4m3.argtypes = [ctypes.c_uint8]
+        L.orc_decode_e4m3.restype = ctypes.c_double
+        L.orc_activation.argtypes = [ctypes.c_double, I32]
+        L.orc_activation.restype = ctypes.c_double
+        L.orc_gemm_fused.argtypes = [P, P, I32, I64, I64, I64, P, P, P, I32, P, I32]
+        L.orc_gemm_fused.restype = I32
+        L.orc_gemm_fused_entries.argtypes = [P, P, I32, I64, P, P, P, I32, P, P, I64, P, I32]
+        L.orc_gemm_fused_entries.restype = I32
         L.orc_decode_e8m0.argtypes = [ctypes.c_uint8]
         L.orc_decode_e8m0.restype = ctypes.c_double
         L.orc_round_bf16.argtypes = [ctypes.c_double]
@@ -160,6 +172,63 @@ def decode_bf16(bits: int) -> float:
 
 def decode_e2m1(code: int) -> float:
     return lib().orc_decode_e2m1(code)
+
+
+def decode_e4m3(code: int) -> float:
+    return lib().orc_decode_e4m3(code)
+
+
+def activation(y: float, epilogue: str) -> float:
+    return lib().orc_activation(float(y), EPILOGUES[epilogue])
+
+
+def _elem_bits(x: np.ndarray, dtype: int) -> np.ndarray:
+    want = np.uint16 if dtype == BF16 else np.uint8
+    x = np.ascontiguousarray(x)
+    if x.dtype != want:
+        raise TypeError(f"expected {want} elements, got {x.dtype}")
+    return x
+
+
+def _vec(v, n: int):
+    if v is None:
+        return None, None
+    a = np.ascontiguousarray(v, dtype=np.float32)
+    if a.shape != (n,):
+        raise ValueError(f"vector of shape {a.shape}, expected ({n},)")
+    return a, a.ctypes.data
+
+
+def gemm_fused(A: np.ndarray, B: np.ndarray, dtype: int, M: int, N: int, K: int,
+               scale_a=None, scale_b=None, bias=None, epilogue: str = "none",
+               threads: int = 0) -> np.ndarray:
+    """act(A·Bᵀ * scale_a[m] * scale_b[n] + bias[n]) in fp64, (M, N).
+    A (M,K) and B (N,K) dense row-major bits: uint16 (bf16) or uint8 (E4M3)."""
+    Ab, Bb = _elem_bits(A, dtype), _elem_bits(B, dtype)
+    (sa, psa), (sb, psb), (bi, pbi) = _vec(scale_a, M), _vec(scale_b, N), _vec(bias, N)
+    D = np.empty((M, N), dtype=np.float64)
+    rc = lib().orc_gemm_fused(_ptr(Ab), _ptr(Bb), dtype, M, N, K, psa, psb, pbi,
+                              EPILOGUES[epilogue], _ptr(D), threads)
+    if rc:
+        raise RuntimeError(f"orc_gemm_fused failed ({rc})")
+    return D
+
+
+def gemm_fused_entries(A: np.ndarray, B: np.ndarray, dtype: int, M: int, N: int, K: int, ms, ns,
+                       scale_a=None, scale_b=None, bias=None, epilogue: str = "none",
+                       threads: int = 0) -> np.ndarray:
+    """Outputs (ms[i], ns[i]) of gemm_fused, each summed directly."""
+    Ab, Bb = _elem_bits(A, dtype), _elem_bits(B, dtype)
+    (sa, psa), (sb, psb), (bi, pbi) = _vec(scale_a, M), _vec(scale_b, N), _vec(bias, N)
+    ms = np.ascontiguousarray(ms, dtype=np.int64)
+    ns = np.ascontiguousarray(ns, dtype=np.int64)
+    out = np.empty(ms.shape[0], dtype=np.float64)
+    rc = lib().orc_gemm_fused_entries(_ptr(Ab), _ptr(Bb), dtype, K, psa, psb, pbi,
+                                      EPILOGUES[epilogue], _ptr(ms), _ptr(ns), ms.shape[0],
+                                      _ptr(out), threads)
+    if rc:
+        raise RuntimeError(f"orc_gemm_fused_entries failed ({rc})")
+    return out
 
 
 def decode_e8m0(byte: int) -> float:

@@ -35,6 +35,22 @@
  * - bf16 output rounding: the pages cast f32 -> bf16 (`.to(fx.BFloat16)`,
  *   §3 "Internal Types") without naming a rounding mode; round-to-nearest-
  *   even from the IEEE 754 definition is the reading taken.
+ * - Fused epilogue (orc_gemm_fused): the preshuffle GEMM of "Kernel
+ *   authoring guide", §11 "Complete example: Preshuffle GEMM", takes
+ *   scale_a, scale_b and bias tensors, fp8 or bf16 inputs, bf16 output and
+ *   an epilogue among none / bias / bias_relu / bias_silu / bias_gelu, but
+ *   does not spell out their arithmetic.  Reading taken, the plainest one:
+ *     y[m,n] = act( acc[m,n] * scale_a[m] * scale_b[n] + bias[n] )
+ *   with scale_a one fp32 factor per row of A, scale_b one per row of B
+ *   (per column of D), bias one fp32 value per column of D (added only by
+ *   the bias_* epilogues), and the activation applied last:
+ *   relu(y) = max(y, 0); silu(y) = y / (1 + e^-y); gelu(y) = y * Phi(y)
+ *   = y/2 * (1 + erf(y / sqrt 2)), the exact (erf) form of GELU, not the
+ *   tanh approximation.
+ * - fp8 inputs: the pages' fp8 atoms use Float8E4M3FNUZ on CDNA3 ("FlyDSL
+ *   Kernel Authoring Skill", §6).  The E4M3 read here is the OCP 8-bit
+ *   floating point format E4M3 (bias 7, no infinities, S.1111.111 = NaN,
+ *   largest finite 448), the FP8 format of the GB300 tensor cores.
  *
  * Every function here is pinned by tests/test_oracle_pins.py against values
  * the pages print, closed forms, brute force and independent libraries.
@@ -55,7 +71,7 @@ typedef struct {
     int64_t stride[2][2];
 } orc_layout;
 
-enum { ORC_F32 = 0, ORC_BF16 = 1 };
+enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_E4M3 = 2 };
 
 /* ---------------------------------------------------------------- layouts */
 
@@ -120,6 +136,20 @@ double orc_decode_e2m1(uint8_t code)
     return s ? -mag : mag;
 }
 
+/* OCP FP8 E4M3: s | e3 e2 e1 e0 | m2 m1 m0, bias 7.  e == 0 is subnormal:
+ * (m/8) * 2^-6.  e == 15 with m == 7 is NaN (no infinities).  Otherwise
+ * (1 + m/8) * 2^(e-7). */
+double orc_decode_e4m3(uint8_t code)
+{
+    int s = (code >> 7) & 1;
+    int e = (code >> 3) & 15;
+    int m = code & 7;
+    if (e == 15 && m == 7)
+        return NAN;
+    double mag = (e == 0) ? ldexp(m / 8.0, -6) : ldexp(1.0 + m / 8.0, e - 7);
+    return s ? -mag : mag;
+}
+
 /* OCP MX E8M0: 2^(byte - 127); 0xFF encodes NaN. */
 double orc_decode_e8m0(uint8_t byte)
 {
@@ -175,6 +205,8 @@ static double fetch(const void *X, const orc_layout *L, int dtype,
     int64_t i = orc_crd2idx(r, c, L);
     if (dtype == ORC_BF16)
         return orc_decode_bf16(((const uint16_t *)X)[i]);
+    if (dtype == ORC_E4M3)
+        return orc_decode_e4m3(((const uint8_t *)X)[i]);
     return orc_decode_f32(((const uint32_t *)X)[i]);
 }
 
@@ -336,5 +368,96 @@ int orc_read_mxfp4(const uint8_t *X, const uint8_t *S, int64_t R, int64_t K,
     for (int64_t r = 0; r < R; ++r)
         for (int64_t k = 0; k < K; ++k)
             out[r * K + k] = fetch_mxfp4(X, S, K, r, k);
+    return 0;
+}
+
+/* ------------------------------------------------------- fused epilogue */
+
+enum { ORC_EPI_NONE = 0, ORC_EPI_BIAS = 1, ORC_EPI_BIAS_RELU = 2,
+       ORC_EPI_BIAS_SILU = 3, ORC_EPI_BIAS_GELU = 4 };
+
+/* The activation of an epilogue, in fp64 (identity for none / bias). */
+double orc_activation(double y, int epi)
+{
+    switch (epi) {
+    case ORC_EPI_BIAS_RELU:
+        return y > 0.0 ? y : 0.0;
+    case ORC_EPI_BIAS_SILU:
+        return y / (1.0 + exp(-y));
+    case ORC_EPI_BIAS_GELU:
+        return 0.5 * y * (1.0 + erf(y / sqrt(2.0)));
+    default:
+        return y;
+    }
+}
+
+/* act(acc * sa[m] * sb[n] + bias[n]) for one output; sa / sb may be NULL
+ * (factor 1); bias is read only by the bias_* epilogues. */
+static double epilogue(double acc, int64_t m, int64_t n, const float *sa,
+                       const float *sb, const float *bias, int epi)
+{
+    double y = acc;
+    if (sa)
+        y *= (double)sa[m];
+    if (sb)
+        y *= (double)sb[n];
+    if (epi >= ORC_EPI_BIAS)
+        y += (double)bias[n];
+    return orc_activation(y, epi);
+}
+
+/* Fused GEMM: A (M,K) and B (N,K) dense row-major in `dtype` (bf16 or
+ * E4M3); D (M x N dense row-major fp64) before the bf16 output rounding. */
+int orc_gemm_fused(const void *A, const void *B, int dtype, int64_t M,
+                   int64_t N, int64_t K, const float *sa, const float *sb,
+                   const float *bias, int epi, double *D, int nthreads)
+{
+    if (!A || !B || !D || M < 0 || N < 0 || K < 0 || epi < 0 || epi > 4 ||
+        (epi >= ORC_EPI_BIAS && !bias) || (dtype != ORC_BF16 && dtype != ORC_E4M3))
+        return 1;
+    orc_layout la, lb;
+    memset(&la, 0, sizeof la);
+    memset(&lb, 0, sizeof lb);
+    la.depth[0] = la.depth[1] = lb.depth[0] = lb.depth[1] = 1;
+    la.shape[0][0] = M;
+    la.shape[1][0] = K;
+    la.stride[0][0] = K;
+    la.stride[1][0] = 1;
+    lb.shape[0][0] = N;
+    lb.shape[1][0] = K;
+    lb.stride[0][0] = K;
+    lb.stride[1][0] = 1;
+    int rc = orc_gemm(A, &la, B, &lb, dtype, M, N, K, D, nthreads);
+    if (rc)
+        return rc;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n)
+            D[m * N + n] = epilogue(D[m * N + n], m, n, sa, sb, bias, epi);
+    return 0;
+}
+
+/* Selected outputs of orc_gemm_fused, each summed directly. */
+int orc_gemm_fused_entries(const void *A, const void *B, int dtype, int64_t K,
+                           const float *sa, const float *sb, const float *bias,
+                           int epi, const int64_t *ms, const int64_t *ns,
+                           int64_t count, double *out, int nthreads)
+{
+    if (!A || !B || !ms || !ns || !out || count < 0 || epi < 0 || epi > 4 ||
+        (epi >= ORC_EPI_BIAS && !bias) || (dtype != ORC_BF16 && dtype != ORC_E4M3))
+        return 1;
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t i = 0; i < count; ++i) {
+        const int64_t m = ms[i], n = ns[i];
+        double s = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            double a = dtype == ORC_BF16 ? orc_decode_bf16(((const uint16_t *)A)[m * K + k])
+                                         : orc_decode_e4m3(((const uint8_t *)A)[m * K + k]);
+            double b = dtype == ORC_BF16 ? orc_decode_bf16(((const uint16_t *)B)[n * K + k])
+                                         : orc_decode_e4m3(((const uint8_t *)B)[n * K + k]);
+            s += a * b;
+        }
+        out[i] = epilogue(s, m, n, sa, sb, bias, epi);
+    }
     return 0;
 }

@@ -340,3 +340,106 @@ def test_mxfp4_unit_scales_all_codes():
     ones = inputs.pack_fp4(torch.full((3, 64), 2)).numpy()
     s1 = np.full((3, 2), 127, np.uint8)
     assert np.all(oracle.gemm_mxfp4(ones, ones, s1, s1, 3, 3, 64) == 64)
+
+
+# ------------------------------------------------------- fp8 and epilogues
+
+def test_e4m3_spec_values():
+    """OFP8 E4M3 table values (min/max subnormal and normal, 1.0, 448, NaN).
+    A wrong bias (8 as in FNUZ) or a missing subnormal branch fails here."""
+    with open(os.path.join(GOLDEN, "e4m3_codes.txt")) as f:
+        rows = [l.split() for l in f if l.strip() and not l.startswith("#")]
+    for code, val in rows:
+        got = oracle.decode_e4m3(int(code, 16))
+        if val == "nan":
+            assert math.isnan(got), code
+        else:
+            assert got == float(val), (code, got, val)
+            assert math.copysign(1.0, got) == math.copysign(1.0, float(val)), code
+
+
+def test_e4m3_all_codes_match_torch():
+    """Every one of the 256 codes against torch's float8_e4m3fn decode (an
+    independent implementation of the same OCP format)."""
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([oracle.decode_e4m3(c) for c in range(256)])
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+    assert np.array_equal(np.signbit(got[ok]), np.signbit(ref[ok]))
+
+
+def test_activation_closed_forms():
+    """Textbook values: sigma(1) = 0.7310585786300049 (silu(1) = sigma(1)),
+    Phi(1) = 0.8413447460685429 (gelu(1) = Phi(1), gelu(-1) = -(1 - Phi(1)));
+    relu, and none/bias are the identity."""
+    act = oracle.activation
+    assert act(1.0, "bias_silu") == pytest.approx(0.7310585786300049, abs=1e-15)
+    assert act(1.0, "bias_gelu") == pytest.approx(0.8413447460685429, abs=1e-15)
+    assert act(-1.0, "bias_gelu") == pytest.approx(-0.15865525393145707, abs=1e-15)
+    assert act(-3.5, "bias_relu") == 0.0 and act(2.25, "bias_relu") == 2.25
+    for e in ("none", "bias"):
+        assert act(-7.5, e) == -7.5
+    assert act(0.0, "bias_silu") == 0.0 and act(0.0, "bias_gelu") == 0.0
+
+
+@pytest.mark.parametrize("epi", ["bias_silu", "bias_gelu"])
+def test_activation_odd_identity(epi):
+    """x*s(x) - (-x)*s(-x) = x for s = sigma and s = Phi (s(x) + s(-x) = 1):
+    a sign error or a wrong argument scale inside the activation fails."""
+    for x in np.linspace(-9, 9, 73):
+        assert oracle.activation(x, epi) - oracle.activation(-x, epi) == pytest.approx(x, abs=1e-12)
+
+
+@pytest.mark.parametrize("epi,fn", [("bias_silu", torch.nn.functional.silu),
+                                    ("bias_gelu", torch.nn.functional.gelu)])
+def test_activation_matches_torch_fp64(epi, fn):
+    """Against torch's fp64 silu and exact (erf) gelu, an independent library."""
+    x = torch.linspace(-12, 12, 241, dtype=torch.float64)
+    ref = fn(x).numpy()
+    got = np.array([oracle.activation(v, epi) for v in x.numpy()])
+    np.testing.assert_allclose(got, ref, rtol=1e-14, atol=1e-15)
+
+
+def test_fused_epilogue_hand_example():
+    """A = [[1,2],[3,4]], B = [[1,0],[1,1]] -> acc = [[1,3],[3,7]];
+    scale_a = [2, .5] (by row of D), scale_b = [1, 3] (by column), bias =
+    [10, -20] (by column): y = [[12, -2], [11.5, -9.5]].  Swapping which
+    vector indexes rows or columns, or adding bias before scaling, fails."""
+    A = inputs.bits_of(torch.tensor([[1.0, 2.0], [3.0, 4.0]]).to(torch.bfloat16))
+    B = inputs.bits_of(torch.tensor([[1.0, 0.0], [1.0, 1.0]]).to(torch.bfloat16))
+    kw = dict(scale_a=[2.0, 0.5], scale_b=[1.0, 3.0], bias=[10.0, -20.0])
+    y = oracle.gemm_fused(A, B, oracle.BF16, 2, 2, 2, epilogue="bias", **kw)
+    assert np.array_equal(y, [[12.0, -2.0], [11.5, -9.5]])
+    r = oracle.gemm_fused(A, B, oracle.BF16, 2, 2, 2, epilogue="bias_relu", **kw)
+    assert np.array_equal(r, [[12.0, 0.0], [11.5, 0.0]])
+    n = oracle.gemm_fused(A, B, oracle.BF16, 2, 2, 2, epilogue="none", scale_a=[2.0, 0.5])
+    assert np.array_equal(n, [[2.0, 6.0], [1.5, 3.5]])
+    # the same product with E4M3 codes 1 = 0x38, 2 = 0x40, 3 = 0x44, 4 = 0x48
+    A8 = np.array([[0x38, 0x40], [0x44, 0x48]], dtype=np.uint8)
+    B8 = np.array([[0x38, 0x00], [0x38, 0x38]], dtype=np.uint8)
+    assert np.array_equal(oracle.gemm_fused(A8, B8, oracle.E4M3, 2, 2, 2, epilogue="bias", **kw), y)
+
+
+def test_fused_matches_numpy_and_entries():
+    """The fused oracle against numpy's fp64 matmul of the decoded operands
+    followed by the epilogue written with numpy/scipy (an independent
+    evaluation), and its sampled-entry form against the full one."""
+    from scipy.special import erf
+    M, N, K = 37, 29, 70
+    g = torch.Generator().manual_seed(5)
+    A = torch.randn(M, K, generator=g).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    B = torch.randn(N, K, generator=g).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    sa = torch.rand(M, generator=g).numpy() + 0.5
+    sb = torch.rand(N, generator=g).numpy() + 0.5
+    bias = torch.randn(N, generator=g).numpy()
+    a = torch.from_numpy(A).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    b = torch.from_numpy(B).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    y = (a @ b.T) * sa.astype(np.float64)[:, None] * sb.astype(np.float64)[None, :] + bias.astype(np.float64)
+    ref = 0.5 * y * (1 + erf(y / np.sqrt(2)))
+    got = oracle.gemm_fused(A, B, oracle.E4M3, M, N, K, sa, sb, bias, "bias_gelu")
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+    ms, ns = np.array([0, 36, 5, 17]), np.array([0, 28, 11, 3])
+    ent = oracle.gemm_fused_entries(A, B, oracle.E4M3, M, N, K, ms, ns, sa, sb, bias, "bias_gelu")
+    np.testing.assert_allclose(ent, got[ms, ns], rtol=1e-13, atol=1e-13)
