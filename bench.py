@@ -36,16 +36,20 @@ sys.path.insert(0, ROOT)
 METRIC = "GEMM TFLOP/s and % of GB300 dense tensor (or HBM) roofline, 1 GPU"
 HEADLINE = "bf16_4096"
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# nominal dense ratio fp4 : bf16 on GB300 (13.5 : 2.25 PFLOP/s)
+# nominal dense ratios fp4 : bf16 and fp8 : bf16 on GB300 (13.5, 4.5 : 2.25 PFLOP/s)
 FP4_OVER_BF16 = 13.5 / 2.25
+FP8_OVER_BF16 = 4.5 / 2.25
 # fp32 FFMA peak: 152 SMs x 128 FMA/clk x 2 flop x 2.07 GHz
 FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+# GB300 nominal dense peaks (context beside the measured denominators)
+NOMINAL = {"bf16": 2250.0, "e4m3": 4500.0, "mxfp4": 13500.0, "hbm": 7900.0, "alu": FP32_ALU_TFLOPS}
 L2_FLUSH_BYTES = 512 << 20
 L2_CLEAN_BYTES = 320 << 20
 L2_BYTES = 129 * 10**6
 KERNEL_OF = {"fp32_128": "ffma_gemm_kernel", "bf16_1024": "tc_bf16_kernel",
-             "bf16_4096": "tc2_bf16_kernel", "skinny_16x28672x8192": "skinny_tc_kernel",
-             "mxfp4_8192": "mxfp4_kernel"}
+             "bf16_4096": "tc2_gemm_kernel", "skinny_16x28672x8192": "skinny_tc_kernel",
+             "mxfp4_8192": "mxfp4_pair_kernel", "e4m3_8192_bias_gelu": "tc2_gemm_kernel",
+             "bf16_4096_bias_silu": "tc2_gemm_kernel"}
 
 
 def load_peaks():
@@ -134,7 +138,7 @@ class ClockSampler:
 def input_bytes(w):
     if w.dtype == "mxfp4":
         return (w.M + w.N) * (w.K // 2 + w.K // 32)
-    elem = 4 if w.dtype == "f32" else 2
+    elem = {"f32": 4, "bf16": 2, "e4m3": 1}[w.dtype]
     return (w.M + w.N) * w.K * elem
 
 
@@ -176,6 +180,10 @@ def make_call(w, dev_in, out, stream):
     if w.dtype == "mxfp4":
         A, B, sA, sB = dev_in
         return lambda: tmg.gemm_mxfp4(A, B, sA, sB, out, stream=stream)
+    if w.epilogue is not None:
+        A, B, sa, sb, bias = dev_in
+        return lambda: tmg.gemm_fused(A, B, out, scale_a=sa, scale_b=sb, bias=bias,
+                                      epilogue=w.epilogue, stream=stream)
     A, B = dev_in
     return lambda: tmg.gemm(A, B, out, stream=stream)
 
@@ -200,9 +208,15 @@ def roofline(w, ms_per_launch, peaks, peak_kind, traffic):
         if w.dtype == "mxfp4":
             peak = peak * FP4_OVER_BF16
             src = f"{peak_kind} bf16 burst x nominal fp4/bf16 ratio 6"
+        elif w.dtype == "e4m3":
+            peak = peak * FP8_OVER_BF16
+            src = f"{peak_kind} bf16 burst x nominal fp8/bf16 ratio 2"
         r = {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
              "peak_source": src}
     r["frac"] = r["achieved"] / r["peak"]
+    nominal = NOMINAL[w.dtype if r["bound"] == "tensor" else r["bound"]]
+    r["nominal_peak"] = nominal
+    r["frac_nominal"] = r["achieved"] / nominal
     r["traffic"] = traffic.get(w.name)
     r["kernel"] = KERNEL_OF[w.name]
     return r
@@ -295,6 +309,15 @@ def oracle_sample(w, budget_s):
             A, B, sA, sB = [t.numpy() for t in host]
             t0 = time.perf_counter()
             oracle.gemm_mxfp4(A[:rows], B, sA[:rows], sB, rows, w.N, w.K)
+            return time.perf_counter() - t0
+        if w.epilogue is not None:
+            A, B, sa, sb, bias = host
+            dtype = oracle.E4M3 if w.dtype == "e4m3" else oracle.BF16
+            a = inputs.bits_of(A[:rows])
+            b = inputs.bits_of(B)
+            t0 = time.perf_counter()
+            oracle.gemm_fused(a, b, dtype, rows, w.N, w.K, sa[:rows].numpy(), sb.numpy(), bias.numpy(),
+                              w.epilogue)
             return time.perf_counter() - t0
         A, B = host
         dtype = oracle.F32 if w.dtype == "f32" else oracle.BF16
@@ -466,6 +489,7 @@ def main():
             "dtype": "bf16" if w.dtype == "bf16" else w.dtype, "data": "synthetic",
             "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
                        "a": w.a_dist, "b": w.b_dist, "accumulate": "fp32",
+                       **({"epilogue": w.epilogue} if w.epilogue else {}),
                        "l2": l2_policy(w)[1],
                        "timing": "CUDA events around each library call on its stream",
                        "ms_median": statistics.median(ms), "ms_min": min(ms),

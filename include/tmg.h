@@ -30,8 +30,8 @@
  * torch tensors).  The library never frees or retains them beyond the
  * call.  The library owns only: a device error word (static device memory)
  * and per-(device, stream) scratch — split-K partials for the skinny path,
- * relaid scales for the MXFP4 path — grown on demand and released by
- * tmg_shutdown().
+ * stream-K partial tiles for the CTA-pair kernels, relaid scales for the
+ * MXFP4 path — grown on demand and released by tmg_shutdown().
  *
  * Errors: nothing is allowed to fault.  Bad arguments return
  * TMG_ERR_INVALID_ARG, valid but unhandled requests TMG_ERR_UNSUPPORTED,
@@ -57,8 +57,25 @@ typedef enum {
     TMG_ERR_TIMEOUT = 4
 } tmg_status;
 
-/* Element type of A, B and D (identical); accumulation is always fp32. */
-typedef enum { TMG_F32 = 0, TMG_BF16 = 1 } tmg_dtype;
+/* Element type.  tmg_gemm: the type of A, B and D (identical), F32 or BF16.
+ * tmg_gemm_fused: the type of A and B, BF16 or E4M3 (D is bf16).
+ * Accumulation is always fp32.  E4M3 is the OCP 8-bit floating point format
+ * (sign, 4 exponent bits with bias 7, 3 mantissa bits; no infinities;
+ * S.1111.111 is NaN; largest finite value 448). */
+typedef enum { TMG_F32 = 0, TMG_BF16 = 1, TMG_E4M3 = 2 } tmg_dtype;
+
+/* Epilogue of tmg_gemm_fused, applied to each fp32 result before the bf16
+ * rounding: y = acc * scale_a[m] * scale_b[n], then for the BIAS variants
+ * y += bias[n], then the activation:
+ *   RELU: max(y, 0);  SILU: y / (1 + exp(-y));
+ *   GELU: y/2 * (1 + erf(y / sqrt(2)))  (the erf form, not the tanh one). */
+typedef enum {
+    TMG_EPI_NONE = 0,
+    TMG_EPI_BIAS = 1,
+    TMG_EPI_BIAS_RELU = 2,
+    TMG_EPI_BIAS_SILU = 3,
+    TMG_EPI_BIAS_GELU = 4
+} tmg_epilogue;
 
 /* Which kernel family runs a gemm.  AUTO picks by dtype, layout and shape:
  *   FFMA   — CUDA-core fp32 FMA, any layout (the fp32 path, and the general
@@ -112,6 +129,33 @@ tmg_status tmg_gemm_ex(const void *A, const void *B, void *D, int64_t M,
                        int64_t N, int64_t K, tmg_dtype dtype,
                        const tmg_layout *layoutA, const tmg_layout *layoutB,
                        const tmg_layout *layoutD, tmg_path path, void *stream);
+
+/* Fused GEMM: D[m,n] = bf16_rne( act( (sum_k a(m,k) * b(n,k)) * scale_a[m]
+ * * scale_b[n] + bias[n] ) ), fp32 accumulation.  The options mirror the
+ * preshuffle GEMM of "Kernel authoring guide" (rocm.github.io), §11
+ * "Complete example: Preshuffle GEMM": fp8 or bf16 inputs, bf16 output,
+ * optional scale_a / scale_b / bias tensors and the epilogues none, bias,
+ * bias_relu, bias_silu, bias_gelu.  The pages do not spell out how these
+ * combine; the reading taken is the formula above (scale_a by row of A,
+ * scale_b by row of B, bias by column of D, activation last).
+ *   A         device, (M, K) row-major, K contiguous, of type in_dtype.
+ *   B         device, (N, K) row-major, K contiguous, of type in_dtype.
+ *   D         device, bf16 (M, N) row-major.
+ *   in_dtype  TMG_BF16 or TMG_E4M3 (TMG_F32: UNSUPPORTED).
+ *   scale_a   device fp32 [M] or NULL (all ones).
+ *   scale_b   device fp32 [N] or NULL (all ones).
+ *   bias      device fp32 [N]; required (else INVALID_ARG) by the BIAS
+ *             epilogues, ignored by TMG_EPI_NONE.
+ * K == 0 gives D = act(bias) (zeros for TMG_EPI_NONE).  Tensor-core kernel
+ * (CTA pairs, kind::f16 or kind::f8f6f4): A, B 16-byte aligned and K times
+ * the element size a multiple of 16 bytes (else UNSUPPORTED).  The caller
+ * owns all buffers; the library reuses its per-(device, stream) stream-K
+ * scratch. */
+tmg_status tmg_gemm_fused(const void *A, const void *B, void *D, int64_t M,
+                          int64_t N, int64_t K, tmg_dtype in_dtype,
+                          const float *scale_a, const float *scale_b,
+                          const float *bias, tmg_epilogue epilogue,
+                          void *stream);
 
 /* MXFP4 GEMM: D[m,n] = sum_k a(m,k) * b(n,k) with
  *   a(m,k) = e2m1(code of A at (m,k)) * 2^(scaleA[m, k/32] - 127), same for b.

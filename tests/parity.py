@@ -6,6 +6,10 @@ Bounds (stated once, used everywhere):
   * bf16 / MXFP4 paths: per element |D - D_ref| <= 2e-2 * sqrt(K) *
     max|A| * max|B|, and relative Frobenius error ||D - D_ref|| / ||D_ref||
     <= 5e-3.  (max|A| of MXFP4 is the largest decoded magnitude.)
+  * fused GEMM (scales, bias, activation): per element |D - D_ref| <=
+    1.13 * 2e-2 * sqrt(K) * max|A| * max|B| * max|scale_a| * max|scale_b|
+    + 2^-8 |D_ref| (1.13 bounds the slope of relu, silu and gelu; the last
+    term is the bf16 rounding of the result), relative Frobenius <= 5e-3.
   * exact cases (integer-valued inputs, identity/permutation/all-ones B):
     D must equal the bf16 round-to-nearest-even of the exact result, bit for
     bit (fp32 for the fp32 path).
@@ -43,6 +47,21 @@ def check_bf16_values(d: np.ndarray, ref: np.ndarray, K: int, amax: float, bmax:
     assert err.max() <= bound, f"max |D-Dref| {err.max():.4g} > bound {bound:.4g}"
     assert fro <= BF16_FRO, f"relative Frobenius {fro:.3e} > {BF16_FRO}"
     return {"max_err": float(err.max()), "bound": float(bound), "fro": float(fro)}
+
+
+ACT_SLOPE = 1.13      # max |d act / dy| of relu (1), silu (1.0998) and gelu (1.1289)
+
+
+def check_fused_values(d: np.ndarray, ref: np.ndarray, K: int, amax: float, bmax: float,
+                       samax: float = 1.0, sbmax: float = 1.0) -> dict:
+    err = np.abs(d - ref)
+    bound = ACT_SLOPE * BF16_ELEM_FACTOR * np.sqrt(K) * amax * bmax * samax * sbmax + 2.0 ** -8 * np.abs(ref)
+    fro = np.linalg.norm(d - ref) / max(np.linalg.norm(ref), 1e-300)
+    assert np.all(np.isfinite(d)), "non-finite output"
+    worst = float((err - bound).max())
+    assert worst <= 0, f"max excess over the bound {worst:.4g} (max err {err.max():.4g})"
+    assert fro <= BF16_FRO, f"relative Frobenius {fro:.3e} > {BF16_FRO}"
+    return {"max_err": float(err.max()), "fro": float(fro)}
 
 
 def check_bf16(D: torch.Tensor, ref: np.ndarray, K: int, amax: float, bmax: float) -> dict:

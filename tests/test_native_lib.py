@@ -94,3 +94,22 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(_native, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(_native.TmgError):
         _native.lib()
+
+
+def test_fused_rejects_bad_arguments_before_device_work(native):
+    lib = native.lib()
+    # fp32 inputs have no tensor-core path
+    assert lib.tmg_gemm_fused(16, 16, 16, 4, 4, 64, native.F32, None, None, None, 0, None) == native.ERR_UNSUPPORTED
+    # an unknown input type or epilogue
+    assert lib.tmg_gemm_fused(16, 16, 16, 4, 4, 64, 9, None, None, None, 0, None) == native.ERR_INVALID_ARG
+    assert lib.tmg_gemm_fused(16, 16, 16, 4, 4, 64, native.BF16, None, None, None, 7, None) == native.ERR_INVALID_ARG
+    # a bias epilogue without a bias
+    for epi in (1, 2, 3, 4):
+        assert lib.tmg_gemm_fused(16, 16, 16, 4, 4, 64, native.E4M3, None, None, None, epi,
+                                  None) == native.ERR_INVALID_ARG
+    assert "bias" in lib.tmg_last_error().decode()
+    # negative extents, empty problems
+    assert lib.tmg_gemm_fused(16, 16, 16, -1, 4, 64, native.BF16, None, None, None, 0, None) == native.ERR_INVALID_ARG
+    assert lib.tmg_gemm_fused(16, 16, 16, 0, 4, 64, native.BF16, None, None, None, 0, None) == native.OK
+    # E4M3 is not an element type of tmg_gemm (its D would be E4M3)
+    assert _call(native, 4, 4, 4, dtype=native.E4M3) == native.ERR_INVALID_ARG

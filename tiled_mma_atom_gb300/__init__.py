@@ -19,9 +19,9 @@ from __future__ import annotations
 import torch
 
 from . import _native
-from ._native import (BF16, F32, PATHS, Layout, TmgError, make_layout)  # noqa: F401
+from ._native import (BF16, E4M3, EPILOGUES, F32, PATHS, Layout, TmgError, make_layout)  # noqa: F401
 
-__all__ = ["gemm", "gemm_mxfp4", "check", "make_layout", "Layout", "TmgError",
+__all__ = ["gemm", "gemm_fused", "gemm_mxfp4", "check", "make_layout", "Layout", "TmgError",
            "set_wait_budget_ns", "debug_wait_timeout", "launch_count", "version",
            "shutdown", "PATHS"]
 
@@ -87,6 +87,54 @@ def gemm(A: torch.Tensor, B: torch.Tensor, D: torch.Tensor | None = None, *,
     L = _native.lib()
     st = L.tmg_gemm_ex(A.data_ptr(), B.data_ptr(), D.data_ptr(), M, N, K, dt,
                        la, lb, ld, PATHS[path], _stream_handle(stream))
+    _native.raise_on(st)
+    return D
+
+
+def _fp32_vec(v, n: int, name: str, dev):
+    if v is None:
+        return None
+    if v.dtype != torch.float32 or tuple(v.shape) != (n,) or not v.is_contiguous() or v.device != dev:
+        raise ValueError(f"{name} must be a contiguous float32 tensor of shape ({n},) on {dev}")
+    return v.data_ptr()
+
+
+def gemm_fused(A: torch.Tensor, B: torch.Tensor, D: torch.Tensor | None = None, *,
+               scale_a: torch.Tensor | None = None, scale_b: torch.Tensor | None = None,
+               bias: torch.Tensor | None = None, epilogue: str = "none", stream=None) -> torch.Tensor:
+    """D = bf16(act(A·Bᵀ · scale_a[m] · scale_b[n] + bias[n])), fp32 accumulation.
+
+    A (M,K) and B (N,K): contiguous CUDA tensors of dtype bfloat16 or
+    float8_e4m3fn (both the same).  scale_a (M,), scale_b (N,), bias (N,):
+    float32 or None.  epilogue: "none", "bias", "bias_relu", "bias_silu",
+    "bias_gelu" (GELU in its erf form).  D: bfloat16 (M,N), allocated if not
+    given.  Asynchronous on `stream`."""
+    if A.dtype != B.dtype:
+        raise TypeError("A and B must share one dtype")
+    if A.dtype == torch.bfloat16:
+        dt = BF16
+    elif A.dtype == torch.float8_e4m3fn:
+        dt = E4M3
+    else:
+        raise TypeError(f"unsupported input dtype {A.dtype}: use bfloat16 or float8_e4m3fn")
+    if epilogue not in EPILOGUES:
+        raise ValueError(f"unknown epilogue {epilogue!r}; one of {sorted(EPILOGUES)}")
+    if A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[1]:
+        raise ValueError("A must be (M,K) and B (N,K)")
+    M, K = A.shape
+    N = B.shape[0]
+    for name, t in (("A", A), ("B", B)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if D is None:
+        D = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    if D.dtype != torch.bfloat16 or tuple(D.shape) != (M, N) or not D.is_contiguous():
+        raise ValueError("D must be a contiguous bfloat16 tensor of shape (M, N)")
+    st = _native.lib().tmg_gemm_fused(A.data_ptr(), B.data_ptr(), D.data_ptr(), M, N, K, dt,
+                                      _fp32_vec(scale_a, M, "scale_a", A.device),
+                                      _fp32_vec(scale_b, N, "scale_b", A.device),
+                                      _fp32_vec(bias, N, "bias", A.device),
+                                      EPILOGUES[epilogue], _stream_handle(stream))
     _native.raise_on(st)
     return D
 

@@ -14,12 +14,13 @@ LIB_PATH = os.path.join(HERE, "libtmg.so")
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = 0, 1, 2, 3, 4
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "CUDA", 4: "TIMEOUT"}
-F32, BF16 = 0, 1
+F32, BF16, E4M3 = 0, 1, 2
+EPILOGUES = {"none": 0, "bias": 1, "bias_relu": 2, "bias_silu": 3, "bias_gelu": 4}
 PATHS = {"auto": 0, "ffma": 1, "tc": 2, "skinny": 3, "skinny_ffma": 4, "tc_single": 5,
          "tc_pair": 6}
 
 # Every function include/tmg.h declares.
-EXPORTS = ("tmg_gemm", "tmg_gemm_ex", "tmg_gemm_mxfp4", "tmg_gemm_skinny_noalloc", "tmg_check", "tmg_last_error",
+EXPORTS = ("tmg_gemm", "tmg_gemm_ex", "tmg_gemm_fused", "tmg_gemm_mxfp4", "tmg_gemm_skinny_noalloc", "tmg_check", "tmg_last_error",
            "tmg_set_wait_budget_ns", "tmg_debug_wait_timeout", "tmg_launch_count",
            "tmg_version", "tmg_shutdown")
 
@@ -77,6 +78,8 @@ def lib():
     L.tmg_gemm.restype = ctypes.c_int
     L.tmg_gemm_ex.argtypes = [P, P, P, I64, I64, I64, ctypes.c_int, LP, LP, LP, ctypes.c_int, P]
     L.tmg_gemm_ex.restype = ctypes.c_int
+    L.tmg_gemm_fused.argtypes = [P, P, P, I64, I64, I64, ctypes.c_int, P, P, P, ctypes.c_int, P]
+    L.tmg_gemm_fused.restype = ctypes.c_int
     L.tmg_gemm_mxfp4.argtypes = [P, P, P, P, P, I64, I64, I64, P]
     L.tmg_gemm_mxfp4.restype = ctypes.c_int
     L.tmg_gemm_skinny_noalloc.argtypes = [P, P, P, I64, I64, I64, I64, I64, I64, P]

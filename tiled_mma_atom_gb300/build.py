@@ -17,7 +17,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libtmg.so")
-SOURCES = ["api.cu", "ffma.cu", "tc_bf16.cu", "tc2_bf16.cu", "skinny.cu", "mxfp4.cu", "mxfp4_pair.cu"]
+SOURCES = ["api.cu", "ffma.cu", "tc_bf16.cu", "tc2_bf16.cu", "tc2_fused.cu", "skinny.cu", "mxfp4.cu",
+           "mxfp4_pair.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                 "-I", CSRC, "-I", INCLUDE]
@@ -72,12 +73,13 @@ def build(force: bool = False, verbose: bool = False, extra: list[str] | None = 
     return LIB
 
 
-def source_hash(name: str) -> str:
-    """sha256 of csrc/<name> plus the shared device header (identifies the
-    kernel a profile was taken from)."""
+def source_hash(name) -> str:
+    """sha256 of csrc/<name> (a file name or a list of them) plus the shared
+    device header (identifies the kernel a profile was taken from)."""
     import hashlib
     h = hashlib.sha256()
-    for f in (name, "device.cuh"):
+    names = [name] if isinstance(name, str) else list(name)
+    for f in names + ["device.cuh"]:
         p = os.path.join(CSRC, f)
         if os.path.exists(p):
             with open(p, "rb") as fh:

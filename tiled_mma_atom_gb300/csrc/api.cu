@@ -546,6 +546,8 @@ tmg_status tmg_gemm_ex(const void *A, const void *B, void *D, int64_t M, int64_t
                        const tmg_layout *layoutD, tmg_path path, void *stream)
 {
     t_last_error.clear();
+    if (dtype == TMG_E4M3)
+        return fail(TMG_ERR_INVALID_ARG, "E4M3 is an input type of tmg_gemm_fused only (D is bf16 there)");
     if (dtype != TMG_F32 && dtype != TMG_BF16)
         return fail(TMG_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
     if (path < TMG_PATH_AUTO || path > TMG_PATH_TC_PAIR)
@@ -638,6 +640,65 @@ tmg_status tmg_gemm(const void *A, const void *B, void *D, int64_t M, int64_t N,
                     const tmg_layout *layoutA, const tmg_layout *layoutB, const tmg_layout *layoutD, void *stream)
 {
     return tmg_gemm_ex(A, B, D, M, N, K, dtype, layoutA, layoutB, layoutD, TMG_PATH_AUTO, stream);
+}
+
+tmg_status tmg_gemm_fused(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K,
+                          tmg_dtype in_dtype, const float *scale_a, const float *scale_b, const float *bias,
+                          tmg_epilogue epilogue, void *stream)
+{
+    t_last_error.clear();
+    if (in_dtype == TMG_F32)
+        return fail(TMG_ERR_UNSUPPORTED, "the fused GEMM takes bf16 or E4M3 inputs (fp32 has no tensor-core path)");
+    if (in_dtype != TMG_BF16 && in_dtype != TMG_E4M3)
+        return fail(TMG_ERR_INVALID_ARG, "unknown input dtype %d", (int)in_dtype);
+    if (epilogue < TMG_EPI_NONE || epilogue > TMG_EPI_BIAS_GELU)
+        return fail(TMG_ERR_INVALID_ARG, "unknown epilogue %d", (int)epilogue);
+    if (M < 0 || N < 0 || K < 0)
+        return fail(TMG_ERR_INVALID_ARG, "negative extent M=%lld N=%lld K=%lld", (long long)M, (long long)N,
+                    (long long)K);
+    if (epilogue >= TMG_EPI_BIAS && !bias)
+        return fail(TMG_ERR_INVALID_ARG, "epilogue %d adds a bias but bias is NULL", (int)epilogue);
+    if (M == 0 || N == 0)
+        return TMG_OK;
+    if (!D || (K > 0 && (!A || !B)))
+        return fail(TMG_ERR_INVALID_ARG, "null operand pointer");
+    DeviceState *ds = nullptr;
+    tmg_status st;
+    if ((st = device_state(&ds)) != TMG_OK)
+        return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const Tc2Epi epi{scale_a, scale_b, bias, static_cast<int>(epilogue)};
+    if (K == 0) {
+        cudaError_t e = launch_fused_k0(D, M, N, epi, s);
+        return e == cudaSuccess ? TMG_OK : cuda_fail(e, "fused K=0 launch");
+    }
+    const bool e4m3 = in_dtype == TMG_E4M3;
+    const int elem = e4m3 ? 1 : 2;
+    if (!tma_ok(A, K, elem, M, K) || !tma_ok(B, K, elem, N, K) || M > INT32_MAX || N > INT32_MAX ||
+        K > INT32_MAX)
+        return fail(TMG_ERR_UNSUPPORTED, "the fused GEMM needs 16-byte aligned operands and rows (K * %d bytes "
+                    "a multiple of 16)", elem);
+    TcArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.bn = tc2_fused_pick_bn(N);
+    a.kb_elems = e4m3 ? 128 : 64;
+    const CUtensorMapDataType dt = e4m3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    if ((st = encode_2d(&a.tmA, dt, elem, A, K, M, K, a.kb_elems, 128)) != TMG_OK)
+        return st;
+    if ((st = encode_2d(&a.tmB, dt, elem, B, K, N, K, a.kb_elems, a.bn / 2)) != TMG_OK)
+        return st;
+    a.D = D;
+    a.ldd = N;
+    a.M = static_cast<int>(M);
+    a.N = static_cast<int>(N);
+    a.K = static_cast<int>(K);
+    tc2_plan(a, ds->num_sms);
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if ((st = tc2_scratch(dev, s, a)) != TMG_OK)
+        return st;
+    cudaError_t e = launch_tc2_fused(a, epi, e4m3, err_ctx(*ds), s);
+    return e == cudaSuccess ? TMG_OK : cuda_fail(e, "fused pair launch");
 }
 
 tmg_status tmg_gemm_mxfp4(const void *A, const void *B, const void *scaleA, const void *scaleB, void *D, int64_t M,

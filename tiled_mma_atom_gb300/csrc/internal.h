@@ -52,6 +52,7 @@ struct TcArgs {
     int64_t ldd;
     int M, N, K;
     int bn;            // tile width (N per tile)
+    int kb_elems;      // pair kernel: elements per K block, 64 (bf16) or 128 (E4M3); 0 means 64
     // pair kernel schedule (tc2_plan) and its stream-K scratch
     int pairs;         // clusters launched
     int dp_tiles;      // tiles run data-parallel
@@ -65,6 +66,25 @@ cudaError_t launch_tc_bf16(const TcArgs &a, int num_sms, const ErrCtx &err, cuda
 cudaError_t launch_tc2_bf16(const TcArgs &a, int num_sms, const ErrCtx &err, cudaStream_t s);
 // Pair-tile width for an M x N output.
 int tc2_pick_bn(int64_t M, int64_t N, int num_sms);
+
+// Fused epilogue of the pair kernel: D = bf16(act(acc * scale_a[m] *
+// scale_b[n] + bias[n])); scale_a / scale_b may be null (factor 1), bias is
+// read only by the bias_* epilogues.
+enum { kEpiNone = 0, kEpiBias = 1, kEpiBiasRelu = 2, kEpiBiasSilu = 3, kEpiBiasGelu = 4 };
+struct Tc2Epi {
+    const float *scale_a;
+    const float *scale_b;
+    const float *bias;
+    int epi;
+};
+// Pair kernel with the fused epilogue (tc2_fused.cu); bf16 or E4M3 inputs
+// (tmA/tmB over bytes for E4M3, box {128, rows}; a.kb_elems = 128);
+// a.bn in {256, 128}.  Call tc2_plan first, then provide the scratch.
+cudaError_t launch_tc2_fused(const TcArgs &a, const Tc2Epi &e, bool in_e4m3, const ErrCtx &err,
+                             cudaStream_t s);
+int tc2_fused_pick_bn(int64_t N);
+// D[m,n] = bf16(act(bias[n])) (or 0 without a bias): the fused GEMM at K = 0.
+cudaError_t launch_fused_k0(void *D, int64_t M, int64_t N, const Tc2Epi &e, cudaStream_t s);
 // Fill pairs / dp_tiles / sk_tiles for a.M, a.N, a.K, a.bn.
 void tc2_plan(TcArgs &a, int num_sms);
 size_t tc2_partials_bytes(const TcArgs &a);

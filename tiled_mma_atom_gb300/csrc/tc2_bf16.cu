@@ -1,434 +1,16 @@
-// tc2_bf16.cu — the bf16 GEMM of tc_bf16.cu on CTA pairs: each cluster of
-// two CTAs computes 256 x BN output tiles with tcgen05.mma.cta_group::2
-// (M = 256).  CTA r (r = 0, 1) holds rows 128r..128r+127 of the A tile and
-// rows r·BN/2 .. (r+1)·BN/2 - 1 of the B tile in its own shared memory, so
-// each SM loads half the B tile it would need alone: per SM and K block,
-// 16 KB of A plus BN/2 x 128 bytes of B instead of 16 KB plus BN x 128 bytes.
-//
-// Roles, in both CTAs unless stated:
-//   warp 0        TMA producer for this CTA's halves; the loads of both CTAs
-//                 complete on CTA 0's `full` barrier (CTA 0 announces the
-//                 pair's byte count); waits on its own `empty` barrier.
-//   warp 1        CTA 0 only: issues the pair MMAs and commits with a
-//                 multicast arrive on the `empty` / `tmem_full` barriers of
-//                 both CTAs.  Both CTAs' warp 1 allocate TMEM together.
-//   warps 2..5    epilogue of this CTA's 128 accumulator rows; each warp
-//                 then arrives on CTA 0's `tmem_empty` barrier (count 8).
-//
-// Schedule.  A pair MMA costs nearly the same whatever its width, so tiles
-// are as wide as possible (BN = 256 unless the last column tile would be
-// mostly empty).  When the tile count is not a multiple of the P pairs, 1-2
-// waves' worth of tiles run stream-K — their (tile, K block) units cut into
-// P equal contiguous runs, one per pair — and the rest data-parallel (pair c
-// takes c, c + P, ...); each pair does its stream-K run first.  A tile split across pairs leaves fp32 partial sums in
-// scratch; the last pair to finish a piece of it (a counter per tile, CTA
-// and epilogue warp) adds the partials in pair order — a fixed order, so the
-// result does not depend on timing — rounds to bf16 and resets the counter.
-#include <cuda_bf16.h>
-
-#include <cstring>
-
-#include "internal.h"
+// tc2_bf16.cu — the bf16 GEMM on CTA pairs (kernel in tc2_kernel.cuh):
+// the launches of the plain bf16 kernels, the schedule plan (data-parallel
+// tiles and the stream-K tail) and the tile-width choice.
+#include "tc2_kernel.cuh"
 
 namespace tmg {
-namespace {
-
-constexpr int kBM = 256;           // rows per pair tile
-constexpr int kHalfM = 128;        // rows per CTA
-constexpr int kBK = 64;
-constexpr int kUmmaK = 16;
-constexpr int kThreads = 192;
-constexpr int kGroupM = 8;
-
-template <int BN>
-struct PairCfg {
-    static constexpr int A_BYTES = kHalfM * kBK * 2;            // 16 KB
-    static constexpr int B_BYTES = (BN / 2) * kBK * 2;          // this CTA's half
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = (220 * 1024 - 2048) / STAGE_BYTES > 8 ? 8 : (220 * 1024 - 2048) / STAGE_BYTES;
-    static constexpr int TMEM_COLS = 512;
-    static constexpr int BAR_BYTES = (2 * STAGES + 4) * 8 + 16;
-    static constexpr int SMEM = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
-};
-
-__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int &tm, int &tn)
-{
-    const int group = kGroupM * tiles_n;
-    const int first_m = (t / group) * kGroupM;
-    const int gm = min(tiles_m - first_m, kGroupM);
-    const int r = t % group;
-    tm = first_m + r % gm;
-    tn = r / gm;
-}
-
-// Per-pair walk over its segments: its stream-K run first, then its
-// data-parallel tiles, so the fix-ups of split tiles overlap the
-// data-parallel work instead of trailing it.  The stream-K tiles are the
-// first sk_tiles of the grouped order and the data-parallel ones follow, so
-// the pairs sweep the grouped order front to back (operand panels stay in
-// L2 while they are used).  Every role of both CTAs walks the same sequence.
-struct SegWalk {
-    int nclusters, dp_tiles, sk_tiles, num_kb;
-    int64_t u, u_end;          // stream-K units of this pair (relative to the stream-K region)
-    int next_dp;               // next data-parallel tile
-    int sk_seg;                // stream-K segments handed out so far
-
-    __device__ SegWalk(int c, int nc, int dp, int sk, int nkb) : nclusters(nc), dp_tiles(dp), sk_tiles(sk), num_kb(nkb)
-    {
-        const int64_t U = static_cast<int64_t>(sk) * nkb;
-        u = U * c / nc;
-        u_end = U * (c + 1) / nc;
-        next_dp = c;
-        sk_seg = 0;
-    }
-
-    // Next segment: tile, K-block range, whether it is a piece of a split
-    // tile, and the pair's scratch slot for it (0 = first piece, 1 = last).
-    __device__ bool next(int &tile, int &kb0, int &kb1, bool &partial, int &slot)
-    {
-        if (u >= u_end) {
-            if (next_dp >= dp_tiles)
-                return false;
-            tile = sk_tiles + next_dp;
-            next_dp += nclusters;
-            kb0 = 0;
-            kb1 = num_kb;
-            partial = false;
-            slot = 0;
-            return true;
-        }
-        const int rel = static_cast<int>(u / num_kb);
-        kb0 = static_cast<int>(u % num_kb);
-        const int64_t left = u_end - u;
-        kb1 = left < static_cast<int64_t>(num_kb - kb0) ? kb0 + static_cast<int>(left) : num_kb;
-        tile = rel;
-        partial = !(kb0 == 0 && kb1 == num_kb);
-        slot = sk_seg == 0 ? 0 : 1;
-        ++sk_seg;
-        u += kb1 - kb0;
-        return true;
-    }
-};
-
-// Pair whose stream-K run contains unit u (of U units over P pairs).
-__device__ __forceinline__ int unit_owner(int64_t u, int64_t U, int P)
-{
-    return static_cast<int>(((u + 1) * P - 1) / U);
-}
-
-// Round 32 fp32 values of one output row to bf16 and store them at
-// drow[col0 .. col0+31] (bounded by N).
-__device__ __forceinline__ void store_row_chunk(__nv_bfloat16 *drow, int col0, int N, int vec_ok,
-                                                const float (&v)[32])
-{
-    if (vec_ok && col0 + 32 <= N) {
-        uint4 *dst = reinterpret_cast<uint4 *>(drow + col0);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            uint4 w;
-            w.x = pack_bf16x2(v[8 * j + 0], v[8 * j + 1]);
-            w.y = pack_bf16x2(v[8 * j + 2], v[8 * j + 3]);
-            w.z = pack_bf16x2(v[8 * j + 4], v[8 * j + 5]);
-            w.w = pack_bf16x2(v[8 * j + 6], v[8 * j + 7]);
-            dst[j] = w;
-        }
-    } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-            if (col0 + j < N)
-                drow[col0 + j] = __float2bfloat16_rn(v[j]);
-    }
-}
-
-template <int BN>
-__global__ void __launch_bounds__(kThreads, 1)
-    tc2_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    __nv_bfloat16 *__restrict__ D, int64_t ldd, int M, int N, int K, int dp_tiles, int sk_tiles,
-                    float *__restrict__ partials, uint32_t *__restrict__ counters, int vec_ok, ErrCtx err)
-{
-    using C = PairCfg<BN>;
-    constexpr int STAGES = C::STAGES;
-    constexpr uint32_t STAGE_TX = 2u * C::STAGE_BYTES;
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw = smem_u32(smem_raw);
-    uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-    uint8_t *sA = smem;
-    uint8_t *sB = smem + STAGES * C::A_BYTES;
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * C::STAGE_BYTES);
-    uint64_t *empty = full + STAGES;
-    uint64_t *tfull = empty + STAGES;
-    uint64_t *tempty = tfull + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const uint32_t rank = cluster_ctarank();
-    const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
-    const int tiles_m = (M + kBM - 1) / kBM, tiles_n = (N + BN - 1) / BN;
-    const int num_kb = (K + kBK - 1) / kBK;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
-        }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&tfull[b], 1);
-            mbar_init(&tempty[b], 8);
-        }
-        *abort_flag = 0;
-        fence_mbar_init();
-    }
-    if (warp == 0 && lane == 0) {
-        tma_prefetch_desc(&tmA);
-        tma_prefetch_desc(&tmB);
-    }
-    if (warp == 1) {
-        tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
-        tmem_relinquish_pair();
-    }
-    tc_fence_before();
-    cluster_sync();          // barriers of both CTAs initialised, TMEM allocated
-    tc_fence_after();
-    const uint32_t tmem_base = *tmem_slot;
-
-    if (warp == 0) {
-        if (lane == 0) {
-            // ---------------------------------------------- TMA producer
-            int stage = 0;
-            uint32_t phase = 0;
-            int64_t issued = 0;
-            bool ok = true;
-            SegWalk walk(cluster, nclusters, dp_tiles, sk_tiles, num_kb);
-            int tile, kb0, kb1, slot;
-            bool partial;
-            while (ok && walk.next(tile, kb0, kb1, partial, slot)) {
-                int tm, tn;
-                tile_coords(tile, tiles_m, tiles_n, tm, tn);
-                for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!mbar_wait_cluster(&empty[stage], phase ^ 1u, err, abort_flag, kSiteProducerEmpty)) {
-                        ok = false;
-                        break;
-                    }
-                    if (rank == 0)
-                        mbar_arrive_expect_tx(&full[stage], STAGE_TX);
-                    const uint32_t bar0 = mapa_shared(smem_u32(&full[stage]), 0);
-                    tma_load_2d_pair(sA + stage * C::A_BYTES, &tmA, bar0, kb * kBK, tm * kBM + rank * kHalfM);
-                    tma_load_2d_pair(sB + stage * C::B_BYTES, &tmB, bar0, kb * kBK, tn * BN + rank * (BN / 2));
-                    ++issued;
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-            }
-            // Tail: wait until the MMA has released every stage this CTA
-            // filled (so no multicast arrive is still on its way here), and
-            // in CTA 0 until every load of the pair has landed.
-            for (int i = 0; i < STAGES && i < issued; ++i) {
-                int s = stage - 1 - i;
-                uint32_t ph = phase;
-                if (s < 0) {
-                    s += STAGES;
-                    ph ^= 1u;
-                }
-                if (rank == 0)
-                    mbar_wait_cluster(&full[s], ph, err, abort_flag, kSiteDrain);
-                mbar_wait_cluster(&empty[s], ph, err, abort_flag, kSiteDrain);
-            }
-        }
-    } else if (warp == 1) {
-        if (lane == 0 && rank == 0) {
-            // ------------------------------------------------ MMA issuer
-            constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN);
-            int stage = 0;
-            uint32_t phase = 0;
-            int local = 0;
-            bool ok = true;
-            SegWalk walk(cluster, nclusters, dp_tiles, sk_tiles, num_kb);
-            int tile, kb0, kb1, slot;
-            bool partial;
-            while (ok && walk.next(tile, kb0, kb1, partial, slot)) {
-                const int acc = local & 1;
-                const uint32_t acc_phase = (local >> 1) & 1;
-                ++local;
-                if (!mbar_wait_cluster(&tempty[acc], acc_phase ^ 1u, err, abort_flag, kSiteMmaTmemEmpty))
-                    break;
-                tc_fence_after();
-                const uint32_t d_tmem = tmem_base + acc * BN;
-                for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!mbar_wait_cluster(&full[stage], phase, err, abort_flag, kSiteMmaFull)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(sA + stage * C::A_BYTES));
-                    const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(sB + stage * C::B_BYTES));
-#pragma unroll
-                    for (int k = 0; k < kBK / kUmmaK; ++k) {
-                        const uint64_t koff = static_cast<uint64_t>((k * kUmmaK * 2) >> 4);
-                        mma_bf16_pair(d_tmem, adesc + koff, bdesc + koff, idesc, (kb != kb0) || (k != 0));
-                    }
-                    mma_commit_pair(&empty[stage], 0x3);
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-                if (!ok)
-                    break;
-                mma_commit_pair(&tfull[acc], 0x3);
-            }
-        }
-    } else {
-        // ---------------------------------------------------- epilogue
-        const int q = warp & 3;
-        const int64_t U = static_cast<int64_t>(sk_tiles) * num_kb;
-        int local = 0;
-        SegWalk walk(cluster, nclusters, dp_tiles, sk_tiles, num_kb);
-        int tile, kb0, kb1, slot;
-        bool partial;
-        while (walk.next(tile, kb0, kb1, partial, slot)) {
-            int tm, tn;
-            tile_coords(tile, tiles_m, tiles_n, tm, tn);
-            const int acc = local & 1;
-            const uint32_t acc_phase = (local >> 1) & 1;
-            ++local;
-            if (!mbar_wait_cluster(&tfull[acc], acc_phase, err, abort_flag, kSiteEpiTmemFull))
-                break;
-            tc_fence_after();
-            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-            const int row = tm * kBM + static_cast<int>(rank) * kHalfM + q * 32 + lane;
-            __nv_bfloat16 *drow = D + static_cast<int64_t>(row) * ldd;
-            if (!partial) {
-#pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(tbase + c * 32, r);
-                    float v[32];
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        v[j] = __uint_as_float(r[j]);
-                    if (row < M)
-                        store_row_chunk(drow, tn * BN + c * 32, N, vec_ok, v);
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
-                continue;
-            }
-            // Piece of a split tile: this warp's 32 rows x BN columns go to
-            // scratch, laid out [chunk][4-column group][lane][4] so each
-            // store moves 512 contiguous bytes.
-            const int64_t warp_elems = 32 * BN;
-            float *mine = partials + ((static_cast<int64_t>(2 * cluster + slot) * 2 + rank) * 4 + q) * warp_elems;
-#pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld32(tbase + c * 32, r);
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    reinterpret_cast<float4 *>(mine)[(c * 8 + j) * 32 + lane] =
-                        make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                    __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
-            __threadfence();
-            __syncwarp();
-            const int rel = tile;
-            const int c_first = unit_owner(static_cast<int64_t>(rel) * num_kb, U, nclusters);
-            const int c_last = unit_owner(static_cast<int64_t>(rel + 1) * num_kb - 1, U, nclusters);
-            uint32_t *counter = counters + (static_cast<int64_t>(rel) * 2 + rank) * 4 + q;
-            uint32_t old = 0;
-            if (lane == 0)
-                old = atomicAdd(counter, 1u);
-            old = __shfl_sync(0xFFFFFFFFu, old, 0);
-            if (old != static_cast<uint32_t>(c_last - c_first))
-                continue;
-            // last to arrive: add the pieces in pair order, round, store
-            __threadfence();
-#pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                float v[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    v[j] = 0.f;
-                for (int cc = c_first; cc <= c_last; ++cc) {
-                    const int first_tile = static_cast<int>((U * cc / nclusters) / num_kb);
-                    const int s2 = first_tile == tile ? 0 : 1;
-                    const float4 *src = reinterpret_cast<const float4 *>(
-                        partials + ((static_cast<int64_t>(2 * cc + s2) * 2 + rank) * 4 + q) * warp_elems);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const float4 p = __ldcg(src + (c * 8 + j) * 32 + lane);
-                        v[4 * j] += p.x;
-                        v[4 * j + 1] += p.y;
-                        v[4 * j + 2] += p.z;
-                        v[4 * j + 3] += p.w;
-                    }
-                }
-                if (row < M)
-                    store_row_chunk(drow, tn * BN + c * 32, N, vec_ok, v);
-            }
-            __syncwarp();
-            if (lane == 0)
-                *counter = 0;
-        }
-    }
-
-    __syncwarp();
-    tc_fence_before();
-    cluster_sync();          // no CTA leaves while its peer may still touch it
-    if (warp == 1) {
-        tc_fence_after();
-        tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
-    }
-}
-
-template <int BN>
-cudaError_t launch_pair(const TcArgs &a, const ErrCtx &err, cudaStream_t s)
-{
-    using C = PairCfg<BN>;
-    static_assert(C::SMEM <= 232448, "shared memory budget");
-    static_assert(2 * BN <= C::TMEM_COLS, "TMEM budget");
-    static_assert(C::B_BYTES % 1024 == 0, "B half must be whole 8-row swizzle atoms");
-    auto kern = tc2_bf16_kernel<BN>;
-    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), C::SMEM);
-    if (e != cudaSuccess)
-        return e;
-    cudaLaunchConfig_t cfg;
-    std::memset(&cfg, 0, sizeof cfg);
-    cfg.gridDim = dim3(2 * a.pairs);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = C::SMEM;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    const int vec_ok = (a.ldd % 8 == 0) && ((reinterpret_cast<uintptr_t>(a.D) & 15u) == 0);
-    note_launch();
-    e = cudaLaunchKernelEx(&cfg, kern, a.tmA, a.tmB, static_cast<__nv_bfloat16 *>(a.D), a.ldd, a.M, a.N, a.K,
-                           a.dp_tiles, a.sk_tiles, a.partials, a.counters, vec_ok, err);
-    if (e != cudaSuccess)
-        return e;
-    return cudaGetLastError();
-}
-
-}  // namespace
 
 void tc2_plan(TcArgs &a, int num_sms)
 {
     const int pairs = num_sms / 2;
     const int tiles = ((a.M + kBM - 1) / kBM) * ((a.N + a.bn - 1) / a.bn);
-    const int num_kb = (a.K + kBK - 1) / kBK;
+    const int kbe = a.kb_elems > 0 ? a.kb_elems : 64;
+    const int num_kb = (a.K + kbe - 1) / kbe;
     const int full_waves = tiles / pairs;
     int dp = tiles, sk = 0;
     if (tiles % pairs != 0) {
@@ -453,7 +35,8 @@ size_t tc2_partials_bytes(const TcArgs &a)
 
 size_t tc2_counters_bytes(const TcArgs &a)
 {
-    return static_cast<size_t>(a.sk_tiles) * 2 * 4 * sizeof(uint32_t);
+    // one counter per split tile, CTA and epilogue warp (up to 8 warps)
+    return static_cast<size_t>(a.sk_tiles) * 2 * epi_warps(true) * sizeof(uint32_t);
 }
 
 int tc2_pick_bn(int64_t M, int64_t N, int num_sms)
@@ -480,15 +63,16 @@ int tc2_pick_bn(int64_t M, int64_t N, int num_sms)
 cudaError_t launch_tc2_bf16(const TcArgs &a, int num_sms, const ErrCtx &err, cudaStream_t s)
 {
     (void)num_sms;
+    const Tc2Epi none{nullptr, nullptr, nullptr, kEpiNone};
     switch (a.bn) {
     case 256:
-        return launch_pair<256>(a, err, s);
+        return launch_pair<256, kInBf16, false>(a, none, err, s);
     case 224:
-        return launch_pair<224>(a, err, s);
+        return launch_pair<224, kInBf16, false>(a, none, err, s);
     case 192:
-        return launch_pair<192>(a, err, s);
+        return launch_pair<192, kInBf16, false>(a, none, err, s);
     default:
-        return launch_pair<128>(a, err, s);
+        return launch_pair<128, kInBf16, false>(a, none, err, s);
     }
 }
 

@@ -30,6 +30,7 @@ class Workload:
     dtype: str          # "f32", "bf16" or "mxfp4"
     a_dist: str         # description of the value distribution
     b_dist: str
+    epilogue: str | None = None   # fused GEMM (tmg_gemm_fused) epilogue, or None
 
     @property
     def flops(self) -> int:
@@ -45,6 +46,11 @@ WORKLOADS = {
     "mxfp4_8192": Workload("mxfp4_8192", 4, 8192, 8192, 8192, "mxfp4",
                            "e2m1 codes U{0..15}, e8m0 exp U[-4,4]",
                            "e2m1 codes U{0..15}, e8m0 exp U[-4,4]"),
+    # fused GEMMs: scale_a, scale_b ~ U[0.5, 1.5], bias ~ N(0,1), fp32
+    "e4m3_8192_bias_gelu": Workload("e4m3_8192_bias_gelu", 5, 8192, 8192, 8192, "e4m3",
+                                    "N(0,1) -> e4m3", "N(0,1) -> e4m3", "bias_gelu"),
+    "bf16_4096_bias_silu": Workload("bf16_4096_bias_silu", 6, 4096, 4096, 4096, "bf16",
+                                    "N(0,1)", "N(0,1)", "bias_silu"),
 }
 
 
@@ -67,11 +73,31 @@ def normal_bf16(rows: int, cols: int, seed: int, std: float = 1.0) -> torch.Tens
     return x.to(torch.bfloat16)
 
 
+def normal_e4m3(rows: int, cols: int, seed: int, std: float = 1.0) -> torch.Tensor:
+    """N(0, std^2) draws converted to OCP E4M3 (torch.float8_e4m3fn)."""
+    g = _gen(seed)
+    x = torch.randn((rows, cols), generator=g, dtype=torch.float32)
+    if std != 1.0:
+        x.mul_(std)
+    return x.to(torch.float8_e4m3fn)
+
+
+def uniform_vec(n: int, seed: int, lo: float = 0.5, hi: float = 1.5) -> torch.Tensor:
+    g = _gen(seed)
+    return torch.rand((n,), generator=g, dtype=torch.float32) * (hi - lo) + lo
+
+
+def normal_vec(n: int, seed: int, std: float = 1.0) -> torch.Tensor:
+    g = _gen(seed)
+    return torch.randn((n,), generator=g, dtype=torch.float32) * std
+
+
 def integer_valued(rows: int, cols: int, seed: int, lo: int = -2, hi: int = 2,
                    dtype: torch.dtype = torch.bfloat16) -> torch.Tensor:
-    """Integers uniform in [lo, hi], stored exactly in fp32 or bf16."""
+    """Integers uniform in [lo, hi], stored exactly in fp32, bf16 or E4M3
+    (|value| <= 16 is exact in E4M3)."""
     g = _gen(seed)
-    return torch.randint(lo, hi + 1, (rows, cols), generator=g, dtype=torch.int32).to(dtype)
+    return torch.randint(lo, hi + 1, (rows, cols), generator=g, dtype=torch.int32).to(torch.float32).to(dtype)
 
 
 def random_fp4_codes(rows: int, K: int, seed: int) -> torch.Tensor:
@@ -100,9 +126,14 @@ def pack_fp4(codes: torch.Tensor) -> torch.Tensor:
 def make_inputs(w: Workload):
     """Inputs of a workload on the CPU.
 
-    Returns (A, B) for f32/bf16 and (A, B, scaleA, scaleB) for mxfp4."""
+    Returns (A, B) for f32/bf16, (A, B, scaleA, scaleB) for mxfp4 and
+    (A, B, scale_a, scale_b, bias) for a fused workload."""
     M = w.M
     s = 1000 * w.index
+    if w.epilogue is not None:
+        gen = normal_e4m3 if w.dtype == "e4m3" else normal_bf16
+        return (gen(M, w.K, s + 0), gen(w.N, w.K, s + 1), uniform_vec(M, s + 2),
+                uniform_vec(w.N, s + 3), normal_vec(w.N, s + 4))
     if w.dtype == "f32":
         return uniform_f32(M, w.K, s + 0), uniform_f32(w.N, w.K, s + 1)
     if w.dtype == "bf16":
@@ -122,4 +153,6 @@ def bits_of(t: torch.Tensor):
         return t.contiguous().view(torch.int16).numpy().view("uint16")
     if t.dtype == torch.uint8:
         return t.contiguous().numpy()
+    if t.dtype == torch.float8_e4m3fn:
+        return t.contiguous().view(torch.uint8).numpy()
     raise TypeError(t.dtype)
