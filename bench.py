@@ -49,7 +49,7 @@ L2_BYTES = 129 * 10**6
 KERNEL_OF = {"fp32_128": "ffma_gemm_kernel", "bf16_1024": "tc_bf16_kernel",
              "bf16_4096": "tc2_gemm_kernel", "skinny_16x28672x8192": "skinny_tc_kernel",
              "mxfp4_8192": "mxfp4_pair_kernel", "e4m3_8192_bias_gelu": "tc2_gemm_kernel",
-             "bf16_4096_bias_silu": "tc2_gemm_kernel"}
+             "bf16_4096_bias_silu": "tc2_gemm_kernel", "bf16_4096_a_mn_major": "tc2_gemm_kernel"}
 
 
 def load_peaks():
@@ -185,6 +185,8 @@ def make_call(w, dev_in, out, stream):
         return lambda: tmg.gemm_fused(A, B, out, scale_a=sa, scale_b=sb, bias=bias,
                                       epilogue=w.epilogue, stream=stream)
     A, B = dev_in
+    if w.a_mn_major:
+        return lambda: tmg.gemm(A, B, out, M=w.M, N=w.N, K=w.K, layoutA=((w.M, w.K), (1, w.M)), stream=stream)
     return lambda: tmg.gemm(A, B, out, stream=stream)
 
 
@@ -321,11 +323,13 @@ def oracle_sample(w, budget_s):
             return time.perf_counter() - t0
         A, B = host
         dtype = oracle.F32 if w.dtype == "f32" else oracle.BF16
-        a = inputs.bits_of(A[:rows])
         b = inputs.bits_of(B)
+        if w.a_mn_major:            # the first rows of A are the first columns of its buffer
+            a, la = inputs.bits_of(A), oracle.make_layout((rows, w.K), (1, w.M))
+        else:
+            a, la = inputs.bits_of(A[:rows]), oracle.row_major(rows, w.K)
         t0 = time.perf_counter()
-        oracle.gemm(a, oracle.row_major(rows, w.K), b, oracle.row_major(w.N, w.K), dtype,
-                    rows, w.N, w.K)
+        oracle.gemm(a, la, b, oracle.row_major(w.N, w.K), dtype, rows, w.N, w.K)
         return time.perf_counter() - t0
 
     probe_rows = min(w.M, max(1, threads))

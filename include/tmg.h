@@ -31,7 +31,8 @@
  * call.  The library owns only: a device error word (static device memory)
  * and per-(device, stream) scratch — split-K partials for the skinny path,
  * stream-K partial tiles for the CTA-pair kernels, relaid scales for the
- * MXFP4 path — grown on demand and released by tmg_shutdown().
+ * MXFP4 path, packed operands of the general-layout path — grown on demand
+ * and released by tmg_shutdown().
  *
  * Errors: nothing is allowed to fault.  Bad arguments return
  * TMG_ERR_INVALID_ARG, valid but unhandled requests TMG_ERR_UNSUPPORTED,
@@ -84,7 +85,14 @@ typedef enum {
  *   SKINNY — tensor-core swap-AB split-K GEMM for M <= 64, bf16, K-major;
  *   SKINNY_FFMA — CUDA-core split-K dot products for M <= 16, bf16, K-major;
  *   TC_SINGLE / TC_PAIR — TC restricted to one-CTA 128-row tiles or to
- *            CTA-pair (cta_group::2) 256-row tiles; TC picks between them.
+ *            CTA-pair (cta_group::2) 256-row tiles; TC picks between them;
+ *   PACKED_TC — bf16 in any layout on the tensor cores: operands the TMA
+ *            cannot read in place (MN-major, nested, strided, broadcast) are
+ *            first gathered through their layouts into K-major workspace
+ *            copies, a D that is neither row- nor column-major is computed
+ *            into a dense workspace and scattered back.  AUTO takes it for
+ *            bf16 problems with M*N*K >= 2^27 that TC cannot read in place
+ *            (smaller ones go to FFMA).
  * Forcing a family that cannot take the arguments returns UNSUPPORTED. */
 typedef enum {
     TMG_PATH_AUTO = 0,
@@ -93,7 +101,8 @@ typedef enum {
     TMG_PATH_SKINNY = 3,
     TMG_PATH_SKINNY_FFMA = 4,
     TMG_PATH_TC_SINGLE = 5,
-    TMG_PATH_TC_PAIR = 6
+    TMG_PATH_TC_PAIR = 6,
+    TMG_PATH_PACKED_TC = 7
 } tmg_path;
 
 /* A rank-2 layout over logical coordinates (row, col).  Mode t (0 = rows,

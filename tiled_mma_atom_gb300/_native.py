@@ -17,7 +17,7 @@ STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "CUDA", 4: "TIME
 F32, BF16, E4M3 = 0, 1, 2
 EPILOGUES = {"none": 0, "bias": 1, "bias_relu": 2, "bias_silu": 3, "bias_gelu": 4}
 PATHS = {"auto": 0, "ffma": 1, "tc": 2, "skinny": 3, "skinny_ffma": 4, "tc_single": 5,
-         "tc_pair": 6}
+         "tc_pair": 6, "packed_tc": 7}
 
 # Every function include/tmg.h declares.
 EXPORTS = ("tmg_gemm", "tmg_gemm_ex", "tmg_gemm_fused", "tmg_gemm_mxfp4", "tmg_gemm_skinny_noalloc", "tmg_check", "tmg_last_error",

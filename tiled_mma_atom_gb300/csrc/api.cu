@@ -7,8 +7,11 @@
 // crd2idx((i,j)) = Σ coordinate × stride.  The host classifies each operand
 // layout:
 //   K-major dense   (rows, K):(ld, 1)  -> TMA tiles, tcgen05 K-major operand
-//   anything else (MN-major, nested, strided, broadcast) -> the CUDA-core
-//                   path, which evaluates crd2idx per element.
+//   anything else (MN-major, nested, strided, broadcast) -> for problems
+//                   large enough to pay for it, a crd2idx gather into a
+//                   K-major scratch copy (pack.cu) and then the tensor
+//                   cores; else the CUDA-core path, which evaluates
+//                   crd2idx per element.
 // D given column-major, (M,N):(1,ld), is computed as Dᵀ = B·Aᵀ with the
 // operand roles swapped, so it also reaches the tensor-core kernels.
 #include <cuda.h>
@@ -60,6 +63,8 @@ struct Scratch {
     size_t tc2_partials_bytes = 0;
     uint32_t *tc2_counters = nullptr;  // pair kernel stream-K tile counters
     size_t tc2_counters_bytes = 0;
+    void *pack[3] = {nullptr, nullptr, nullptr};   // packed A, packed B, dense D
+    size_t pack_bytes[3] = {0, 0, 0};
 };
 std::map<std::pair<int, uintptr_t>, Scratch> g_scratch;
 
@@ -458,6 +463,81 @@ tmg_status run_tc(const DeviceState &ds, const TcPlan &p, void *D, int64_t K, in
     return e == cudaSuccess ? TMG_OK : cuda_fail(e, pair ? "tc2_bf16 launch" : "tc_bf16 launch");
 }
 
+// Per-(device, stream) buffer `which` (0: packed A, 1: packed B, 2: dense D)
+// of the general-layout path, grown on demand.
+void *pack_scratch(int which, size_t bytes, cudaStream_t s, tmg_status *st)
+{
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lk(g_mu);
+    Scratch &sc = g_scratch[{dev, reinterpret_cast<uintptr_t>(s)}];
+    if (sc.pack_bytes[which] < bytes) {
+        if (sc.pack[which])
+            cudaFree(sc.pack[which]);
+        sc.pack[which] = nullptr;
+        sc.pack_bytes[which] = 0;
+        cudaError_t e = cudaMalloc(&sc.pack[which], bytes);
+        if (e != cudaSuccess) {
+            *st = cuda_fail(e, "cudaMalloc(general-layout workspace)");
+            return nullptr;
+        }
+        sc.pack_bytes[which] = bytes;
+    }
+    *st = TMG_OK;
+    return sc.pack[which];
+}
+
+tmg_status run_skinny(const DeviceState &ds, const TcPlan &p, void *D, int64_t K, cudaStream_t s);
+
+// General layouts on the tensor cores: every operand the TMA cannot read in
+// place is gathered through its layout into a dense K-major scratch copy
+// (rows padded to a multiple of 8 elements), a D that is neither row- nor
+// column-major gets a dense row-major scratch result that is scattered back
+// through its layout; the GEMM in between is the ordinary tcgen05 dispatch.
+tmg_status run_packed(const DeviceState &ds, const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K,
+                      const tmg_layout &la, const tmg_layout &lb, const tmg_layout &ld, cudaStream_t s)
+{
+    tmg_status st;
+    cudaError_t e;
+    const int64_t Kp = (K + 7) / 8 * 8;
+    const void *ops[2] = {A, B};
+    const tmg_layout *lays[2] = {&la, &lb};
+    const int64_t rows[2] = {M, N};
+    int64_t lds[2];
+    for (int i = 0; i < 2; ++i) {
+        lds[i] = row_stride_if_rowmajor(*lays[i], rows[i], K);
+        if (lds[i] > 0 && tma_ok(ops[i], lds[i], 2, rows[i], K))
+            continue;
+        void *P = pack_scratch(i, static_cast<size_t>(rows[i]) * Kp * 2, s, &st);
+        if (!P)
+            return st;
+        if ((e = launch_pack(ops[i], to_dev(*lays[i]), rows[i], K, P, Kp, ds.num_sms, s)) != cudaSuccess)
+            return cuda_fail(e, "pack launch");
+        ops[i] = P;
+        lds[i] = Kp;
+    }
+    tmg_layout pa = row_major(M, K), pb = row_major(N, K);
+    pa.stride[0][0] = lds[0];
+    pb.stride[0][0] = lds[1];
+    TcPlan p = plan_tc(ops[0], ops[1], D, M, N, K, pa, pb, ld);
+    void *dense = nullptr;
+    if (!p.ok) {
+        dense = pack_scratch(2, static_cast<size_t>(M) * N * 2, s, &st);
+        if (!dense)
+            return st;
+        p = plan_tc(ops[0], ops[1], dense, M, N, K, pa, pb, row_major(M, N));
+        if (!p.ok)
+            return fail(TMG_ERR_UNSUPPORTED, "general-layout path: extents beyond the tensor-core kernels' limits");
+    }
+    void *Dout = dense ? dense : D;
+    st = p.M <= 64 ? run_skinny(ds, p, Dout, K, s) : run_tc(ds, p, Dout, K, 0, s);
+    if (st != TMG_OK || !dense)
+        return st;
+    if ((e = launch_unpack(dense, M, N, D, to_dev(ld), ds.num_sms, s)) != cudaSuccess)
+        return cuda_fail(e, "unpack launch");
+    return TMG_OK;
+}
+
 tmg_status run_skinny(const DeviceState &ds, const TcPlan &p, void *D, int64_t K, cudaStream_t s)
 {
     SkinnyTcArgs a;
@@ -550,7 +630,7 @@ tmg_status tmg_gemm_ex(const void *A, const void *B, void *D, int64_t M, int64_t
         return fail(TMG_ERR_INVALID_ARG, "E4M3 is an input type of tmg_gemm_fused only (D is bf16 there)");
     if (dtype != TMG_F32 && dtype != TMG_BF16)
         return fail(TMG_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
-    if (path < TMG_PATH_AUTO || path > TMG_PATH_TC_PAIR)
+    if (path < TMG_PATH_AUTO || path > TMG_PATH_PACKED_TC)
         return fail(TMG_ERR_INVALID_ARG, "unknown path %d", (int)path);
     if (M < 0 || N < 0 || K < 0)
         return fail(TMG_ERR_INVALID_ARG, "negative extent M=%lld N=%lld K=%lld", (long long)M, (long long)N,
@@ -588,8 +668,11 @@ tmg_status tmg_gemm_ex(const void *A, const void *B, void *D, int64_t M, int64_t
     if (dtype == TMG_BF16)
         plan = plan_tc(A, B, D, M, N, K, la, lb, ld);
     if (use == TMG_PATH_AUTO) {
-        if (dtype == TMG_F32 || !plan.ok)
+        if (dtype == TMG_F32)
             use = TMG_PATH_FFMA;
+        else if (!plan.ok)
+            // the gather pays for itself once the product is at least 512³
+            use = static_cast<double>(M) * N * K >= 134217728.0 ? TMG_PATH_PACKED_TC : TMG_PATH_FFMA;
         else
             use = plan.M <= 64 ? TMG_PATH_SKINNY : TMG_PATH_TC;
     }
@@ -623,6 +706,10 @@ tmg_status tmg_gemm_ex(const void *A, const void *B, void *D, int64_t M, int64_t
                         "skinny path needs bf16, K-major A and B, row- or column-major D, and at most 64 rows "
                         "on the small side");
         return run_skinny(*ds, plan, D, K, s);
+    case TMG_PATH_PACKED_TC:
+        if (dtype != TMG_BF16)
+            return fail(TMG_ERR_UNSUPPORTED, "the general-layout tensor-core path takes bf16");
+        return run_packed(*ds, A, B, D, M, N, K, la, lb, ld, s);
     case TMG_PATH_SKINNY_FFMA: {
         if (dtype != TMG_BF16 || !plan.ok || plan.M > 16 || K % 8 != 0)
             return fail(TMG_ERR_UNSUPPORTED,
@@ -925,6 +1012,9 @@ void tmg_shutdown(void)
             cudaFree(kv.second.tc2_partials);
         if (kv.second.tc2_counters)
             cudaFree(kv.second.tc2_counters);
+        for (void *q : kv.second.pack)
+            if (q)
+                cudaFree(q);
     }
     g_scratch.clear();
     cudaSetDevice(cur);

@@ -18,23 +18,10 @@
 //    reduction of §7 "Reduction Patterns", on 32-lane warps).
 #include <cuda_bf16.h>
 
-#include "internal.h"
+#include "layout.cuh"
 
 namespace tmg {
 namespace {
-
-__device__ __forceinline__ int64_t mode_off(const DevLayout &L, int t, int64_t c)
-{
-    if (L.depth[t] == 1)
-        return c * L.stride[t][0];
-    const int64_t s0 = L.shape[t][0];
-    return (c % s0) * L.stride[t][0] + (c / s0) * L.stride[t][1];
-}
-
-__device__ __forceinline__ int64_t crd2idx(const DevLayout &L, int64_t r, int64_t c)
-{
-    return mode_off(L, 0, r) + mode_off(L, 1, c);
-}
 
 template <typename T>
 __device__ __forceinline__ float ld_elt(const T *p, int64_t i);

@@ -145,6 +145,15 @@ cudaError_t launch_mx_scale_relayout(const uint8_t *sA, int M, uint8_t *relA, in
                                      int N, uint8_t *relB, int groupB, int K, bool wide, int num_sms,
                                      cudaStream_t s);
 
+// ------------------------------------------- general layouts -> tcgen05
+// P (rows, ldp) dense bf16 = X read through layout L over (rows, cols),
+// zero-padded for cols <= k < ldp.
+cudaError_t launch_pack(const void *X, const DevLayout &L, int64_t rows, int64_t cols, void *P, int64_t ldp,
+                        int num_sms, cudaStream_t s);
+// D (through layout L over (rows, cols)) = S dense row-major bf16.
+cudaError_t launch_unpack(const void *S, int64_t rows, int64_t cols, void *D, const DevLayout &L, int num_sms,
+                          cudaStream_t s);
+
 // Probe kernel for the bounded wait (never signalled barrier).
 cudaError_t launch_wait_probe(const ErrCtx &err, cudaStream_t s);
 

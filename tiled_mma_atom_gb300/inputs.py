@@ -31,6 +31,7 @@ class Workload:
     a_dist: str         # description of the value distribution
     b_dist: str
     epilogue: str | None = None   # fused GEMM (tmg_gemm_fused) epilogue, or None
+    a_mn_major: bool = False      # A stored MN-major: the buffer is Aᵀ, (K, M) row-major
 
     @property
     def flops(self) -> int:
@@ -51,6 +52,9 @@ WORKLOADS = {
                                     "N(0,1) -> e4m3", "N(0,1) -> e4m3", "bias_gelu"),
     "bf16_4096_bias_silu": Workload("bf16_4096_bias_silu", 6, 4096, 4096, 4096, "bf16",
                                     "N(0,1)", "N(0,1)", "bias_silu"),
+    # general layout: A given column-major, (M,K):(1,M)
+    "bf16_4096_a_mn_major": Workload("bf16_4096_a_mn_major", 7, 4096, 4096, 4096, "bf16",
+                                     "N(0,1), stored MN-major", "N(0,1)", None, True),
 }
 
 
@@ -126,7 +130,8 @@ def pack_fp4(codes: torch.Tensor) -> torch.Tensor:
 def make_inputs(w: Workload):
     """Inputs of a workload on the CPU.
 
-    Returns (A, B) for f32/bf16, (A, B, scaleA, scaleB) for mxfp4 and
+    Returns (A, B) for f32/bf16 (A as its (K, M) buffer when the workload
+    stores it MN-major), (A, B, scaleA, scaleB) for mxfp4 and
     (A, B, scale_a, scale_b, bias) for a fused workload."""
     M = w.M
     s = 1000 * w.index
@@ -138,7 +143,10 @@ def make_inputs(w: Workload):
         return uniform_f32(M, w.K, s + 0), uniform_f32(w.N, w.K, s + 1)
     if w.dtype == "bf16":
         std_b = 0.02 if w.name.startswith("skinny") else 1.0
-        return normal_bf16(M, w.K, s + 0), normal_bf16(w.N, w.K, s + 1, std=std_b)
+        A = normal_bf16(M, w.K, s + 0)
+        if w.a_mn_major:
+            A = A.t().contiguous()
+        return A, normal_bf16(w.N, w.K, s + 1, std=std_b)
     if w.dtype == "mxfp4":
         return (random_fp4_codes(M, w.K, s + 0), random_fp4_codes(w.N, w.K, s + 1),
                 random_e8m0(M, w.K, s + 2), random_e8m0(w.N, w.K, s + 3))
