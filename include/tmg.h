@@ -139,6 +139,23 @@ tmg_status tmg_gemm_ex(const void *A, const void *B, void *D, int64_t M,
                        const tmg_layout *layoutA, const tmg_layout *layoutB,
                        const tmg_layout *layoutD, tmg_path path, void *stream);
 
+/* tmg_gemm from host memory: the same D = A·Bᵀ with row-major operands in
+ * HOST buffers (pinned memory recommended; pageable memory works, slower):
+ *   A  host, (M, K) row-major of `dtype` (TMG_F32 or TMG_BF16)
+ *   B  host, (N, K) row-major;  D  host, (M, N) row-major, written.
+ * The library copies B to device workspace, then pipelines row chunks of A
+ * and D: the upload of chunk i+1, the GEMM of chunk i (on `stream`, through
+ * the tmg_gemm dispatch) and the download of chunk i-1 overlap on two
+ * library-owned copy streams.  Asynchronous: on return the work is queued
+ * and `stream` waits for the last download; synchronise `stream` before
+ * reading D or reusing A and B.  Device pointers are rejected
+ * (INVALID_ARG).  Workspace (M·K + N·K + M·N elements), copy streams and
+ * events are per (device, stream), grown on demand, freed by tmg_shutdown().
+ * The FlyDSL pages have no host-memory entry; this is the library's
+ * end-to-end call. */
+tmg_status tmg_gemm_host(const void *A, const void *B, void *D, int64_t M,
+                         int64_t N, int64_t K, tmg_dtype dtype, void *stream);
+
 /* Fused GEMM: D[m,n] = bf16_rne( act( (sum_k a(m,k) * b(n,k)) * scale_a[m]
  * * scale_b[n] + bias[n] ) ), fp32 accumulation.  The options mirror the
  * preshuffle GEMM of "Kernel authoring guide" (rocm.github.io), §11

@@ -21,7 +21,7 @@ import torch
 from . import _native
 from ._native import (BF16, E4M3, EPILOGUES, F32, PATHS, Layout, TmgError, make_layout)  # noqa: F401
 
-__all__ = ["gemm", "gemm_fused", "gemm_mxfp4", "check", "make_layout", "Layout", "TmgError",
+__all__ = ["gemm", "gemm_host", "gemm_fused", "gemm_mxfp4", "check", "make_layout", "Layout", "TmgError",
            "set_wait_budget_ns", "debug_wait_timeout", "launch_count", "version",
            "shutdown", "PATHS"]
 
@@ -87,6 +87,30 @@ def gemm(A: torch.Tensor, B: torch.Tensor, D: torch.Tensor | None = None, *,
     L = _native.lib()
     st = L.tmg_gemm_ex(A.data_ptr(), B.data_ptr(), D.data_ptr(), M, N, K, dt,
                        la, lb, ld, PATHS[path], _stream_handle(stream))
+    _native.raise_on(st)
+    return D
+
+
+def gemm_host(A: torch.Tensor, B: torch.Tensor, D: torch.Tensor | None = None, *,
+              stream=None) -> torch.Tensor:
+    """D = A·Bᵀ from host memory: A (M,K) and B (N,K) contiguous CPU tensors
+    (float32 or bfloat16, pinned for full speed), D (M,N) a CPU tensor of the
+    same dtype (allocated pinned if not given).  The library moves the data
+    and overlaps the transfers with the GEMM; the call returns once the work
+    is queued on `stream` — synchronise it before reading D."""
+    for name, t in (("A", A), ("B", B)):
+        if t.is_cuda or not t.is_contiguous() or t.dim() != 2:
+            raise ValueError(f"{name} must be a contiguous 2-D CPU tensor")
+    if A.dtype != B.dtype or A.shape[1] != B.shape[1]:
+        raise ValueError("A (M,K) and B (N,K) must share dtype and K")
+    M, K = A.shape
+    N = B.shape[0]
+    if D is None:
+        D = torch.empty((M, N), dtype=A.dtype).pin_memory()
+    if D.is_cuda or D.dtype != A.dtype or tuple(D.shape) != (M, N) or not D.is_contiguous():
+        raise ValueError("D must be a contiguous CPU tensor of shape (M, N) and A's dtype")
+    st = _native.lib().tmg_gemm_host(A.data_ptr(), B.data_ptr(), D.data_ptr(), M, N, K, _dtype_code(A),
+                                     _stream_handle(stream))
     _native.raise_on(st)
     return D
 

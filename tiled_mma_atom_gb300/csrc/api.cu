@@ -65,6 +65,11 @@ struct Scratch {
     size_t tc2_counters_bytes = 0;
     void *pack[3] = {nullptr, nullptr, nullptr};   // packed A, packed B, dense D
     size_t pack_bytes[3] = {0, 0, 0};
+    void *host_ws[3] = {nullptr, nullptr, nullptr};  // tmg_gemm_host: device A, B, D
+    size_t host_ws_bytes[3] = {0, 0, 0};
+    cudaStream_t copy_in = nullptr, copy_out = nullptr;
+    static constexpr int kHostEvents = 2 + 3 * 16;
+    cudaEvent_t ev[kHostEvents] = {};
 };
 std::map<std::pair<int, uintptr_t>, Scratch> g_scratch;
 
@@ -489,6 +494,43 @@ void *pack_scratch(int which, size_t bytes, cudaStream_t s, tmg_status *st)
 
 tmg_status run_skinny(const DeviceState &ds, const TcPlan &p, void *D, int64_t K, cudaStream_t s);
 
+// Device workspace and copy streams of tmg_gemm_host for (device, stream).
+Scratch *host_scratch(cudaStream_t s, const size_t (&bytes)[3], tmg_status *st)
+{
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lk(g_mu);
+    Scratch &sc = g_scratch[{dev, reinterpret_cast<uintptr_t>(s)}];
+    cudaError_t e;
+    if (!sc.copy_in) {
+        if ((e = cudaStreamCreateWithFlags(&sc.copy_in, cudaStreamNonBlocking)) != cudaSuccess ||
+            (e = cudaStreamCreateWithFlags(&sc.copy_out, cudaStreamNonBlocking)) != cudaSuccess) {
+            *st = cuda_fail(e, "cudaStreamCreate(host copy streams)");
+            return nullptr;
+        }
+        for (cudaEvent_t &ev : sc.ev)
+            if ((e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming)) != cudaSuccess) {
+                *st = cuda_fail(e, "cudaEventCreate(host copy events)");
+                return nullptr;
+            }
+    }
+    for (int i = 0; i < 3; ++i) {
+        if (sc.host_ws_bytes[i] >= bytes[i])
+            continue;
+        if (sc.host_ws[i])
+            cudaFree(sc.host_ws[i]);
+        sc.host_ws[i] = nullptr;
+        sc.host_ws_bytes[i] = 0;
+        if ((e = cudaMalloc(&sc.host_ws[i], bytes[i])) != cudaSuccess) {
+            *st = cuda_fail(e, "cudaMalloc(host-buffer GEMM workspace)");
+            return nullptr;
+        }
+        sc.host_ws_bytes[i] = bytes[i];
+    }
+    *st = TMG_OK;
+    return &sc;
+}
+
 // General layouts on the tensor cores: every operand the TMA cannot read in
 // place is gathered through its layout into a dense K-major scratch copy
 // (rows padded to a multiple of 8 elements), a D that is neither row- nor
@@ -727,6 +769,86 @@ tmg_status tmg_gemm(const void *A, const void *B, void *D, int64_t M, int64_t N,
                     const tmg_layout *layoutA, const tmg_layout *layoutB, const tmg_layout *layoutD, void *stream)
 {
     return tmg_gemm_ex(A, B, D, M, N, K, dtype, layoutA, layoutB, layoutD, TMG_PATH_AUTO, stream);
+}
+
+tmg_status tmg_gemm_host(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, tmg_dtype dtype,
+                         void *stream)
+{
+    t_last_error.clear();
+    if (dtype != TMG_F32 && dtype != TMG_BF16)
+        return fail(TMG_ERR_INVALID_ARG, "tmg_gemm_host takes F32 or BF16 (got %d)", (int)dtype);
+    if (M < 0 || N < 0 || K < 0)
+        return fail(TMG_ERR_INVALID_ARG, "negative extent M=%lld N=%lld K=%lld", (long long)M, (long long)N,
+                    (long long)K);
+    if (M == 0 || N == 0)
+        return TMG_OK;
+    if (!D || (K > 0 && (!A || !B)))
+        return fail(TMG_ERR_INVALID_ARG, "null operand pointer");
+    DeviceState *ds = nullptr;
+    tmg_status st;
+    if ((st = device_state(&ds)) != TMG_OK)
+        return st;
+    for (const void *p : {A, B, static_cast<const void *>(D)}) {
+        cudaPointerAttributes pa;
+        if (p && cudaPointerGetAttributes(&pa, p) == cudaSuccess && pa.type == cudaMemoryTypeDevice)
+            return fail(TMG_ERR_INVALID_ARG, "tmg_gemm_host takes host buffers; %p is device memory", p);
+        cudaGetLastError();
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t elem = dtype == TMG_F32 ? 4 : 2;
+    const size_t bytes[3] = {static_cast<size_t>(M) * K * elem + 16, static_cast<size_t>(N) * K * elem + 16,
+                             static_cast<size_t>(M) * N * elem};
+    Scratch *sc = host_scratch(s, bytes, &st);
+    if (!sc)
+        return st;
+    char *dA = static_cast<char *>(sc->host_ws[0]);
+    char *dB = static_cast<char *>(sc->host_ws[1]);
+    char *dD = static_cast<char *>(sc->host_ws[2]);
+    cudaEvent_t *ev = sc->ev;
+    // Row chunks of A and D: each chunk's copy in, GEMM and copy out run on
+    // three streams, so chunk i's GEMM overlaps chunk i+1's upload and
+    // chunk i-1's download.  Chunks are whole 256-row pair tiles.
+    int64_t chunks = M / 512 > 0 ? M / 512 : 1;
+    if (chunks > 16)
+        chunks = 16;
+    const int64_t rows_per = ((M + chunks - 1) / chunks + 255) / 256 * 256;
+    chunks = (M + rows_per - 1) / rows_per;
+    cudaError_t e;
+    auto check = [&](cudaError_t r, const char *what) { return r == cudaSuccess ? TMG_OK : cuda_fail(r, what); };
+    // the copies start after the work already queued on the caller's stream
+    if ((st = check(cudaEventRecord(ev[0], s), "cudaEventRecord")) != TMG_OK ||
+        (st = check(cudaStreamWaitEvent(sc->copy_in, ev[0], 0), "cudaStreamWaitEvent")) != TMG_OK ||
+        (st = check(cudaStreamWaitEvent(sc->copy_out, ev[0], 0), "cudaStreamWaitEvent")) != TMG_OK)
+        return st;
+    if (K > 0 && (e = cudaMemcpyAsync(dB, B, static_cast<size_t>(N) * K * elem, cudaMemcpyHostToDevice,
+                                      sc->copy_in)) != cudaSuccess)
+        return cuda_fail(e, "cudaMemcpyAsync(B to device)");
+    for (int64_t c = 0; c < chunks; ++c) {
+        const int64_t m0 = c * rows_per, mc = (m0 + rows_per <= M ? rows_per : M - m0);
+        cudaEvent_t in = ev[2 + 3 * c], done = ev[3 + 3 * c];
+        if (K > 0 && (e = cudaMemcpyAsync(dA + m0 * K * elem, static_cast<const char *>(A) + m0 * K * elem,
+                                          static_cast<size_t>(mc) * K * elem, cudaMemcpyHostToDevice,
+                                          sc->copy_in)) != cudaSuccess)
+            return cuda_fail(e, "cudaMemcpyAsync(A rows to device)");
+        if ((st = check(cudaEventRecord(in, sc->copy_in), "cudaEventRecord")) != TMG_OK ||
+            (st = check(cudaStreamWaitEvent(s, in, 0), "cudaStreamWaitEvent")) != TMG_OK)
+            return st;
+        if ((st = tmg_gemm_ex(dA + m0 * K * elem, dB, dD + m0 * N * elem, mc, N, K, dtype, nullptr, nullptr,
+                              nullptr, TMG_PATH_AUTO, s)) != TMG_OK)
+            return st;
+        if ((st = check(cudaEventRecord(done, s), "cudaEventRecord")) != TMG_OK ||
+            (st = check(cudaStreamWaitEvent(sc->copy_out, done, 0), "cudaStreamWaitEvent")) != TMG_OK)
+            return st;
+        if ((e = cudaMemcpyAsync(static_cast<char *>(D) + m0 * N * elem, dD + m0 * N * elem,
+                                 static_cast<size_t>(mc) * N * elem, cudaMemcpyDeviceToHost, sc->copy_out)) !=
+            cudaSuccess)
+            return cuda_fail(e, "cudaMemcpyAsync(D rows to host)");
+    }
+    // the caller's stream continues once D is back on the host
+    if ((st = check(cudaEventRecord(ev[1], sc->copy_out), "cudaEventRecord")) != TMG_OK ||
+        (st = check(cudaStreamWaitEvent(s, ev[1], 0), "cudaStreamWaitEvent")) != TMG_OK)
+        return st;
+    return TMG_OK;
 }
 
 tmg_status tmg_gemm_fused(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K,
@@ -1015,6 +1137,17 @@ void tmg_shutdown(void)
         for (void *q : kv.second.pack)
             if (q)
                 cudaFree(q);
+        for (void *q : kv.second.host_ws)
+            if (q)
+                cudaFree(q);
+        if (kv.second.copy_in) {
+            cudaStreamSynchronize(kv.second.copy_in);
+            cudaStreamSynchronize(kv.second.copy_out);
+            cudaStreamDestroy(kv.second.copy_in);
+            cudaStreamDestroy(kv.second.copy_out);
+            for (cudaEvent_t ev : kv.second.ev)
+                cudaEventDestroy(ev);
+        }
     }
     g_scratch.clear();
     cudaSetDevice(cur);
