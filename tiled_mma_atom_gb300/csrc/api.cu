@@ -416,6 +416,23 @@ tmg_status tc2_scratch(int dev, cudaStream_t s, TcArgs &a)
     return TMG_OK;
 }
 
+// Tensor map for the pair kernel's TMA stores of D (rows x cols bf16, row
+// stride ld): boxes of 32 x 32, no swizzle.  Left unused (d_tma = 0) when D
+// or its row stride is not 16-byte aligned; the kernel then stores with
+// per-thread writes.
+tmg_status encode_d_store(TcArgs &a, void *D, int64_t rows, int64_t cols, int64_t ld)
+{
+    a.d_tma = 0;
+    if (!tma_ok(D, ld, 2, rows, cols))
+        return TMG_OK;
+    tmg_status st = encode_2d(&a.tmD, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, cols, rows, ld, 32, 32,
+                              CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (st != TMG_OK)
+        return st;
+    a.d_tma = 1;
+    return TMG_OK;
+}
+
 tmg_status run_tc(const DeviceState &ds, const TcPlan &p, void *D, int64_t K, int mode, cudaStream_t s)
 {
     TcArgs a;
@@ -462,6 +479,8 @@ tmg_status run_tc(const DeviceState &ds, const TcPlan &p, void *D, int64_t K, in
         int dev = 0;
         cudaGetDevice(&dev);
         if ((st = tc2_scratch(dev, s, a)) != TMG_OK)
+            return st;
+        if ((st = encode_d_store(a, D, p.M, p.N, p.ldd)) != TMG_OK)
             return st;
     }
     cudaError_t e = pair ? launch_tc2_bf16(a, ds.num_sms, err_ctx(ds), s) : launch_tc_bf16(a, ds.num_sms, err_ctx(ds), s);
@@ -905,6 +924,8 @@ tmg_status tmg_gemm_fused(const void *A, const void *B, void *D, int64_t M, int6
     int dev = 0;
     cudaGetDevice(&dev);
     if ((st = tc2_scratch(dev, s, a)) != TMG_OK)
+        return st;
+    if ((st = encode_d_store(a, D, M, N, N)) != TMG_OK)
         return st;
     cudaError_t e = launch_tc2_fused(a, epi, e4m3, err_ctx(*ds), s);
     return e == cudaSuccess ? TMG_OK : cuda_fail(e, "fused pair launch");

@@ -67,15 +67,23 @@ constexpr int kGroupM = 8;
 // Elements per K block for an input type.
 __host__ __device__ constexpr int kb_elems(int in) { return in == kInE4m3 ? 128 : 64; }
 
-template <int BN>
+// Shared memory, in order: the ring of A / B stages; per epilogue warp two
+// 32 x 32 bf16 boxes that stage its output for TMA stores; the barriers; with
+// the fused epilogue, per epilogue warp a copy of the tile's scale_b and bias
+// columns.
+template <int BN, bool EPI>
 struct PairCfg {
     static constexpr int A_BYTES = kHalfM * kKBlockBytes;       // 16 KB
     static constexpr int B_BYTES = (BN / 2) * kKBlockBytes;     // this CTA's half
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = (220 * 1024 - 2048) / STAGE_BYTES > 8 ? 8 : (220 * 1024 - 2048) / STAGE_BYTES;
+    static constexpr int BOX_BYTES = 32 * 32 * 2;                // one 32 x 32 bf16 output box
+    static constexpr int STAGING_BYTES = epi_warps(EPI) * 2 * BOX_BYTES;
+    static constexpr int COLS_BYTES = EPI ? epi_warps(EPI) * 2 * BN * 4 : 0;
+    static constexpr int RING_BUDGET = 220 * 1024 - 2048 - STAGING_BYTES - COLS_BYTES;
+    static constexpr int STAGES = RING_BUDGET / STAGE_BYTES > 8 ? 8 : RING_BUDGET / STAGE_BYTES;
     static constexpr int TMEM_COLS = 512;
     static constexpr int BAR_BYTES = (2 * STAGES + 4) * 8 + 16;
-    static constexpr int SMEM = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+    static constexpr int SMEM = STAGES * STAGE_BYTES + STAGING_BYTES + BAR_BYTES + COLS_BYTES + 1024;
 };
 
 __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int &tm, int &tn)
@@ -240,19 +248,14 @@ __device__ __forceinline__ void apply_epilogue(float (&v)[32], const Tc2Epi &e, 
     }
 }
 
-// Shared-memory bytes of the epilogue's column copies: per epilogue warp,
-// scale_b and bias for the BN columns of a tile.
-template <int BN, bool EPI>
-__host__ __device__ constexpr int epi_cols_bytes() { return EPI ? epi_warps(EPI) * 2 * BN * 4 : 0; }
-
 template <int BN, int IN, bool EPI>
 __global__ void __launch_bounds__(tc2_threads(EPI), 1)
     tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    __nv_bfloat16 *__restrict__ D, int64_t ldd, int M, int N, int K, int dp_tiles, int sk_tiles,
-                    float *__restrict__ partials, uint32_t *__restrict__ counters, int vec_ok, Tc2Epi epi,
-                    ErrCtx err)
+                    const __grid_constant__ CUtensorMap tmD, __nv_bfloat16 *__restrict__ D, int64_t ldd, int M, int N,
+                    int K, int dp_tiles, int sk_tiles, float *__restrict__ partials,
+                    uint32_t *__restrict__ counters, int vec_ok, int d_tma, Tc2Epi epi, ErrCtx err)
 {
-    using C = PairCfg<BN>;
+    using C = PairCfg<BN, EPI>;
     constexpr int KB_ELEMS = kb_elems(IN);
     constexpr int STAGES = C::STAGES;
     constexpr uint32_t STAGE_TX = 2u * C::STAGE_BYTES;
@@ -261,13 +264,14 @@ __global__ void __launch_bounds__(tc2_threads(EPI), 1)
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     uint8_t *sA = smem;
     uint8_t *sB = smem + STAGES * C::A_BYTES;
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * C::STAGE_BYTES);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * C::STAGE_BYTES + C::STAGING_BYTES);
     uint64_t *empty = full + STAGES;
     uint64_t *tfull = empty + STAGES;
     uint64_t *tempty = tfull + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    float *epi_cols = reinterpret_cast<float *>(smem + STAGES * C::STAGE_BYTES + C::BAR_BYTES);
+    uint8_t *staging = smem + STAGES * C::STAGE_BYTES;
+    float *epi_cols = reinterpret_cast<float *>(staging + C::STAGING_BYTES + C::BAR_BYTES);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const uint32_t rank = cluster_ctarank();
@@ -290,6 +294,8 @@ __global__ void __launch_bounds__(tc2_threads(EPI), 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        if (d_tma)
+            tma_prefetch_desc(&tmD);
     }
     if (warp == 1) {
         tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
@@ -398,6 +404,10 @@ __global__ void __launch_bounds__(tc2_threads(EPI), 1)
         const int e = warp - 2;                          // epilogue warp index
         const int q = warp & 3;                          // its TMEM lane quarter
         const int c_begin = (e / 4) * CHUNKS, c_end = c_begin + CHUNKS;
+        // output staging: two 32 x 32 bf16 boxes, used alternately; `nst`
+        // counts the TMA stores this warp's lane 0 has issued
+        uint8_t *boxes = staging + e * 2 * C::BOX_BYTES;
+        int nst = 0;
         const int64_t U = static_cast<int64_t>(sk_tiles) * num_kb;
         int local = 0;
         SegWalk walk(cluster, nclusters, dp_tiles, sk_tiles, num_kb);
@@ -443,8 +453,34 @@ __global__ void __launch_bounds__(tc2_threads(EPI), 1)
                         v[j] = __uint_as_float(r[j]);
                     if constexpr (EPI)
                         apply_epilogue<BN>(v, epi, sa_row, cols, c * 32);
-                    if (row < M)
-                        store_row_chunk(drow, tn * BN + c * 32, N, vec_ok, v);
+                    const int col0 = tn * BN + c * 32;
+                    const int row0 = row - lane;
+                    if (d_tma) {
+                        // stage this warp's 32 x 32 box, then one lane stores it
+                        if (row0 >= M || col0 >= N)
+                            continue;
+                        uint8_t *box = boxes + (nst & 1) * C::BOX_BYTES;
+                        if (nst >= 2) {              // the store from this buffer two boxes ago has read it
+                            if (lane == 0)
+                                bulk_wait_read<1>();
+                            __syncwarp();
+                        }
+                        uint4 *dst = reinterpret_cast<uint4 *>(box + lane * 64);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            dst[j] = make_uint4(pack_bf16x2(v[8 * j], v[8 * j + 1]), pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
+                                                pack_bf16x2(v[8 * j + 4], v[8 * j + 5]),
+                                                pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&tmD, box, col0, row0);
+                            bulk_commit();
+                        }
+                        ++nst;
+                    } else if (row < M) {
+                        store_row_chunk(drow, col0, N, vec_ok, v);
+                    }
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -514,6 +550,8 @@ __global__ void __launch_bounds__(tc2_threads(EPI), 1)
             if (lane == 0)
                 *counter = 0;
         }
+        if (lane == 0)
+            bulk_wait_all();             // this warp's TMA stores are complete
     }
 
     __syncwarp();
@@ -528,13 +566,13 @@ __global__ void __launch_bounds__(tc2_threads(EPI), 1)
 template <int BN, int IN, bool EPI>
 cudaError_t launch_pair(const TcArgs &a, const Tc2Epi &epi, const ErrCtx &err, cudaStream_t s)
 {
-    using C = PairCfg<BN>;
+    using C = PairCfg<BN, EPI>;
     static_assert(C::SMEM <= 232448, "shared memory budget");
+    static_assert(C::STAGES >= 4, "pipeline depth");
     static_assert(2 * BN <= C::TMEM_COLS, "TMEM budget");
     static_assert(C::B_BYTES % 1024 == 0, "B half must be whole 8-row swizzle atoms");
     auto kern = tc2_gemm_kernel<BN, IN, EPI>;
-    constexpr int SMEM = C::SMEM + epi_cols_bytes<BN, EPI>();
-    static_assert(SMEM <= 232448, "shared memory budget with the epilogue columns");
+    constexpr int SMEM = C::SMEM;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), SMEM);
     if (e != cudaSuccess)
         return e;
@@ -553,8 +591,8 @@ cudaError_t launch_pair(const TcArgs &a, const Tc2Epi &epi, const ErrCtx &err, c
     cfg.numAttrs = 1;
     const int vec_ok = (a.ldd % 8 == 0) && ((reinterpret_cast<uintptr_t>(a.D) & 15u) == 0);
     note_launch();
-    e = cudaLaunchKernelEx(&cfg, kern, a.tmA, a.tmB, static_cast<__nv_bfloat16 *>(a.D), a.ldd, a.M, a.N, a.K,
-                           a.dp_tiles, a.sk_tiles, a.partials, a.counters, vec_ok, epi, err);
+    e = cudaLaunchKernelEx(&cfg, kern, a.tmA, a.tmB, a.tmD, static_cast<__nv_bfloat16 *>(a.D), a.ldd, a.M, a.N,
+                           a.K, a.dp_tiles, a.sk_tiles, a.partials, a.counters, vec_ok, a.d_tma, epi, err);
     if (e != cudaSuccess)
         return e;
     return cudaGetLastError();
