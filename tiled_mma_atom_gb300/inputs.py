@@ -104,6 +104,30 @@ def integer_valued(rows: int, cols: int, seed: int, lo: int = -2, hi: int = 2,
     return torch.randint(lo, hi + 1, (rows, cols), generator=g, dtype=torch.int32).to(torch.float32).to(dtype)
 
 
+def hashed_int(rows: int, cols: int, seed: int, row0: int = 0, device="cpu",
+               dtype: torch.dtype = torch.bfloat16, lo: int = -2, hi: int = 2) -> torch.Tensor:
+    """Integers in [lo, hi] given by an integer hash of (row0 + r, c, seed):
+    the same values on any device and for any slice of rows, so a very large
+    operand can be built on the GPU in pieces while a CPU check regenerates
+    only the rows it samples."""
+    r = torch.arange(row0, row0 + rows, device=device, dtype=torch.int64)[:, None]
+    c = torch.arange(cols, device=device, dtype=torch.int64)[None, :]
+    h = (r * 7919 + c * 104729 + seed * 15485863) % 1000003
+    h = (h * h + 12345) % 999983
+    return (h % (hi - lo + 1) + lo).to(torch.float32).to(dtype)
+
+
+def hashed_int_device(rows: int, cols: int, seed: int, device, dtype: torch.dtype = torch.bfloat16,
+                      chunk_rows: int = 4096) -> torch.Tensor:
+    """hashed_int for the whole (rows, cols) matrix, built on `device` in row
+    slices (bounded temporary memory)."""
+    out = torch.empty((rows, cols), dtype=dtype, device=device)
+    for r0 in range(0, rows, chunk_rows):
+        n = min(chunk_rows, rows - r0)
+        out[r0:r0 + n] = hashed_int(n, cols, seed, row0=r0, device=device, dtype=dtype)
+    return out
+
+
 def random_fp4_codes(rows: int, K: int, seed: int) -> torch.Tensor:
     """(rows, K/2) bytes; each nibble an independent uniform e2m1 code."""
     if K % 2:
