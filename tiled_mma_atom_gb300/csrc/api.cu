@@ -989,8 +989,9 @@ tmg_status tmg_gemm_mxfp4(const void *A, const void *B, const void *scaleA, cons
     {
         int dev = 0;
         cudaGetDevice(&dev);
-        const size_t ra = mxfp4_relaid_scale_bytes(M, K, 128, pair);
-        const size_t rb = mxfp4_relaid_scale_bytes(N, K, pair ? a.bn : 128, pair);
+        const bool wide = pair && mxfp4_pair_wide_scales();
+        const size_t ra = mxfp4_relaid_scale_bytes(M, K, 128, wide);
+        const size_t rb = mxfp4_relaid_scale_bytes(N, K, pair ? a.bn : 128, wide);
         uint8_t *buf = mx_scale_scratch(dev, s, ra + rb, &st);
         if (!buf)
             return st;
@@ -998,11 +999,14 @@ tmg_status tmg_gemm_mxfp4(const void *A, const void *B, const void *scaleA, cons
         a.relB = buf + ra;
         if (pair) {
             const int nsub = (a.bn + 127) / 128;
-            if ((st = encode_2d(&a.tmSA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.relA, 256, ra / 256, 256, 256, 16,
-                                CU_TENSOR_MAP_SWIZZLE_NONE)) != TMG_OK)
+            // one K block of one group's relaid scales, as rows of 256 bytes:
+            // 4 KB (wide) or 1 KB (compact) per 128-row sub-block
+            const int rows_per_sub = wide ? 16 : 4;
+            if ((st = encode_2d(&a.tmSA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.relA, 256, ra / 256, 256, 256,
+                                rows_per_sub, CU_TENSOR_MAP_SWIZZLE_NONE)) != TMG_OK)
                 return st;
             if ((st = encode_2d(&a.tmSB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.relB, 256, rb / 256, 256, 256,
-                                16 * nsub, CU_TENSOR_MAP_SWIZZLE_NONE)) != TMG_OK)
+                                rows_per_sub * nsub, CU_TENSOR_MAP_SWIZZLE_NONE)) != TMG_OK)
                 return st;
         }
     }

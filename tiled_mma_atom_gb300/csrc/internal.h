@@ -140,6 +140,8 @@ cudaError_t launch_mxfp4(const Mxfp4Args &a, int num_sms, const ErrCtx &err, cud
 // CTA-pair kernel (256 x bn tiles), also two launches.
 cudaError_t launch_mxfp4_pair(const Mxfp4Args &a, int num_sms, const ErrCtx &err, cudaStream_t s);
 int mxfp4_pair_pick_bn(int64_t M, int64_t N, int num_sms);
+// Whether the pair kernel reads its scales in the wide (4x replicated) form.
+bool mxfp4_pair_wide_scales();
 // Relaid scale bytes for `rows` rows grouped by `group_rows`, compact or
 // wide form (see mx_common.cuh).
 size_t mxfp4_relaid_scale_bytes(int64_t rows, int64_t K, int group_rows, bool wide);

@@ -8,11 +8,15 @@
 // of the tile, so it needs every B scale).  All four loads of both CTAs are
 // TMA copies completing on CTA 0's `full` barrier.  Warp roles: 0 TMA
 // producer; 1 MMA issuer (CTA 0); 2 scale copier (CTA 0), which moves each
-// stage's scales of both CTAs into their TMEM with wide
-// tcgen05.cp.cta_group::2 copies and commits to the stage's `sready`
-// barrier; the rest epilogue.  Keeping the copies out of the MMA lane's
-// instruction stream lets it queue MMAs back to back (measured on MXFP4
-// 8192³: 218 -> 209 µs).  TMEM per CTA: the accumulator(s) plus, per stage,
+// stage's scales of both CTAs into their TMEM with tcgen05.cp.cta_group::2
+// copies and commits to the stage's `sready` barrier; the rest epilogue.
+// Keeping the copies out of the MMA lane's instruction stream lets it queue
+// MMAs back to back (measured on MXFP4 8192³: 218 -> 209 µs).  The scales
+// travel in the compact chunk order (1 KB per 128 rows and K block) and are
+// replicated across the TMEM lane quarters by the copies themselves
+// (32x128b.warpx4): a quarter of the L2 traffic and of the relayout output
+// of the 4x replicated form that three wide 128x256b copies would read
+// (209 -> 197 µs).  TMEM per CTA: the accumulator(s) plus, per stage,
 // 8 columns of A scales and 8·ceil(BN/128) columns of B scales (B rows 0-127
 // in the first 4 columns of each K-block group, rows 128.. in the next 4).
 // A stage's scale columns are rewritten only after its `full` barrier
@@ -36,6 +40,11 @@ using namespace mx;
 
 constexpr int kBM = 256;
 constexpr int kHalfM = 128;
+// Scale form in shared memory: wide (each 512-byte chunk repeated four times,
+// three tcgen05.cp 128x256b per K block) or compact (one copy of each chunk,
+// 2 + 2·NSUB tcgen05.cp 32x128b.warpx4 that replicate across the lane
+// quarters themselves).
+constexpr bool kWideScales = false;
 // warps 0-2 (producer, MMA, scale copier) + epilogue warps: 4 with two
 // accumulators, 8 with one (two warps per TMEM lane quarter, each draining
 // half the columns)
@@ -49,8 +58,8 @@ struct MxPairCfg {
     static constexpr int NSUB = (BN + 127) / 128;
     static constexpr int A_BYTES = kHalfM * kBKBytes;          // 16 KB
     static constexpr int B_BYTES = (BN / 2) * kBKBytes;
-    static constexpr int SFA_BYTES = kWideSrcBytes;
-    static constexpr int SFB_BYTES = NSUB * kWideSrcBytes;
+    static constexpr int SFA_BYTES = kWideScales ? kWideSrcBytes : kSfBlock;
+    static constexpr int SFB_BYTES = NSUB * SFA_BYTES;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
     static constexpr int SF_COLS = 8 + 8 * NSUB;                 // per stage
     static constexpr int TMEM_STAGES = (kTmemCols - ACC_BUFS * BN) / SF_COLS;
@@ -246,11 +255,26 @@ __global__ void __launch_bounds__(pair_threads(ACC_BUFS), 1)
                     // 1 + NSUB wide copies: A scales (both K-block groups),
                     // then B scales per K-block group (NSUB = 2) or both
                     // groups at once (NSUB = 1)
-                    tmem_cp_wide_pair(sfa_col, sdesc_wide_scales(smem_u32(sfA + stage * C::SFA_BYTES)));
+                    if constexpr (kWideScales) {
+                        tmem_cp_wide_pair(sfa_col, sdesc_wide_scales(smem_u32(sfA + stage * C::SFA_BYTES)));
 #pragma unroll
-                    for (int p = 0; p < NSUB; ++p)
-                        tmem_cp_wide_pair(sfb_col + 8 * p,
-                                          sdesc_wide_scales(smem_u32(sfB + stage * C::SFB_BYTES + p * kWideSrcBytes)));
+                        for (int p = 0; p < NSUB; ++p)
+                            tmem_cp_wide_pair(sfb_col + 8 * p,
+                                              sdesc_wide_scales(smem_u32(sfB + stage * C::SFB_BYTES + p * kWideSrcBytes)));
+                    } else {
+                        // chunk c (scale blocks 4c..4c+3) of sub-block s
+                        // -> columns c * 4 * NSUB + 4 s of the group
+#pragma unroll
+                        for (int c = 0; c < 2; ++c) {
+                            tmem_cp_chunk_pair(sfa_col + 4 * c,
+                                               sdesc_noswizzle_rows16(smem_u32(sfA + stage * C::SFA_BYTES + c * kSfChunk)));
+#pragma unroll
+                            for (int sb = 0; sb < NSUB; ++sb)
+                                tmem_cp_chunk_pair(sfb_col + c * 4 * NSUB + 4 * sb,
+                                                   sdesc_noswizzle_rows16(smem_u32(sfB + stage * C::SFB_BYTES +
+                                                                                   sb * kSfBlock + c * kSfChunk)));
+                        }
+                    }
                     mma_commit_pair(&sready[stage], 0x1);
                     if (++stage == STAGES) {
                         stage = 0;
@@ -368,7 +392,7 @@ cudaError_t launch_pair(const Mxfp4Args &a, int num_sms, const ErrCtx &err, cuda
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), C::SMEM);
     if (e != cudaSuccess)
         return e;
-    e = launch_mx_scale_relayout(a.sA, a.M, a.relA, kHalfM, a.sB, a.N, a.relB, BN, a.K, true, num_sms, s);
+    e = launch_mx_scale_relayout(a.sA, a.M, a.relA, kHalfM, a.sB, a.N, a.relB, BN, a.K, kWideScales, num_sms, s);
     if (e != cudaSuccess)
         return e;
     const int tiles = ((a.M + kBM - 1) / kBM) * ((a.N + BN - 1) / BN);
@@ -398,6 +422,8 @@ cudaError_t launch_pair(const Mxfp4Args &a, int num_sms, const ErrCtx &err, cuda
 }
 
 }  // namespace
+
+bool mxfp4_pair_wide_scales() { return kWideScales; }
 
 int mxfp4_pair_pick_bn(int64_t M, int64_t N, int num_sms)
 {
