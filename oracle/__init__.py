@@ -111,6 +111,12 @@ def lib():
         L.orc_gemm_fused.restype = I32
         L.orc_gemm_fused_entries.argtypes = [P, P, I32, I64, P, P, P, I32, P, P, I64, P, I32]
         L.orc_gemm_fused_entries.restype = I32
+        L.orc_decode_int4.argtypes = [ctypes.c_uint8]
+        L.orc_decode_int4.restype = I32
+        L.orc_gemm_w4a8.argtypes = [P, P, I64, I64, I64, P, I32]
+        L.orc_gemm_w4a8.restype = I32
+        L.orc_gemm_w4a8_entries.argtypes = [P, P, I64, P, P, I64, P, I32]
+        L.orc_gemm_w4a8_entries.restype = I32
         L.orc_decode_e8m0.argtypes = [ctypes.c_uint8]
         L.orc_decode_e8m0.restype = ctypes.c_double
         L.orc_round_bf16.argtypes = [ctypes.c_double]
@@ -319,3 +325,30 @@ def read_mxfp4(X: np.ndarray, S: np.ndarray, rows: int, K: int) -> np.ndarray:
 
 def max_threads() -> int:
     return lib().orc_max_threads()
+
+
+def decode_int4(nibble: int) -> int:
+    return lib().orc_decode_int4(nibble)
+
+
+def gemm_w4a8(A: np.ndarray, B: np.ndarray, M: int, N: int, K: int, threads: int = 0) -> np.ndarray:
+    """Exact int64 D = A·Bᵀ: A (M, K) int8, B (N, K/2) packed int4 (even k low nibble)."""
+    A = np.ascontiguousarray(A, dtype=np.int8)
+    B = np.ascontiguousarray(B, dtype=np.uint8)
+    D = np.empty((M, N), dtype=np.int64)
+    rc = lib().orc_gemm_w4a8(_ptr(A), _ptr(B), M, N, K, _ptr(D), threads)
+    if rc:
+        raise RuntimeError(f"orc_gemm_w4a8 failed ({rc})")
+    return D
+
+
+def gemm_w4a8_entries(A: np.ndarray, B: np.ndarray, K: int, ms, ns, threads: int = 0) -> np.ndarray:
+    A = np.ascontiguousarray(A, dtype=np.int8)
+    B = np.ascontiguousarray(B, dtype=np.uint8)
+    ms = np.ascontiguousarray(ms, dtype=np.int64)
+    ns = np.ascontiguousarray(ns, dtype=np.int64)
+    out = np.empty(ms.shape[0], dtype=np.int64)
+    rc = lib().orc_gemm_w4a8_entries(_ptr(A), _ptr(B), K, _ptr(ms), _ptr(ns), ms.shape[0], _ptr(out), threads)
+    if rc:
+        raise RuntimeError(f"orc_gemm_w4a8_entries failed ({rc})")
+    return out

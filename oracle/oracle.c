@@ -47,6 +47,13 @@
  *   relu(y) = max(y, 0); silu(y) = y / (1 + e^-y); gelu(y) = y * Phi(y)
  *   = y/2 * (1 + erf(y / sqrt 2)), the exact (erf) form of GELU, not the
  *   tanh approximation.
+ * - W4A8 (orc_gemm_w4a8): "FlyDSL Kernel Authoring Skill", §10
+ *   Troubleshooting, item 10: A is int8, B is packed int4, two values per
+ *   byte, unpacked to int8 in the kernel; the integer atoms accumulate in
+ *   int32 (§6, the i8 -> i32 and i4 -> i32 WMMA rows, signed operands).
+ *   Readings: the even k sits in the low nibble (as for fp4), a nibble is a
+ *   4-bit two's complement integer in [-8, 7], and D is the exact integer
+ *   sum (int64 here; the library returns int32).
  * - fp8 inputs: the pages' fp8 atoms use Float8E4M3FNUZ on CDNA3 ("FlyDSL
  *   Kernel Authoring Skill", §6).  The E4M3 read here is the OCP 8-bit
  *   floating point format E4M3 (bias 7, no infinities, S.1111.111 = NaN,
@@ -458,6 +465,59 @@ int orc_gemm_fused_entries(const void *A, const void *B, int dtype, int64_t K,
             s += a * b;
         }
         out[i] = epilogue(s, m, n, sa, sb, bias, epi);
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------ W4A8 */
+
+/* Signed 4-bit two's complement: 0..7 -> 0..7, 8..15 -> -8..-1. */
+int orc_decode_int4(uint8_t nibble)
+{
+    nibble &= 0x0F;
+    return nibble >= 8 ? (int)nibble - 16 : (int)nibble;
+}
+
+/* Element (n, k) of a packed (N, K/2)-byte int4 matrix, row-major. */
+static int fetch_int4(const uint8_t *B, int64_t K, int64_t n, int64_t k)
+{
+    uint8_t byte = B[n * (K / 2) + k / 2];
+    return orc_decode_int4((k & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0x0F));
+}
+
+/* D (M x N, int64) = sum_k a(m,k) * b(n,k), exactly: A (M, K) int8
+ * row-major, B (N, K/2) packed int4 row-major. */
+int orc_gemm_w4a8(const int8_t *A, const uint8_t *B, int64_t M, int64_t N,
+                  int64_t K, int64_t *D, int nthreads)
+{
+    if (!A || !B || !D || M < 0 || N < 0 || K < 0 || K % 2)
+        return 1;
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) {
+            int64_t s = 0;
+            for (int64_t k = 0; k < K; ++k)
+                s += (int64_t)A[m * K + k] * fetch_int4(B, K, n, k);
+            D[m * N + n] = s;
+        }
+    return 0;
+}
+
+/* Selected outputs of orc_gemm_w4a8. */
+int orc_gemm_w4a8_entries(const int8_t *A, const uint8_t *B, int64_t K,
+                          const int64_t *ms, const int64_t *ns, int64_t count,
+                          int64_t *out, int nthreads)
+{
+    if (!A || !B || !ms || !ns || !out || count < 0 || K % 2)
+        return 1;
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t i = 0; i < count; ++i) {
+        int64_t s = 0;
+        for (int64_t k = 0; k < K; ++k)
+            s += (int64_t)A[ms[i] * K + k] * fetch_int4(B, K, ns[i], k);
+        out[i] = s;
     }
     return 0;
 }

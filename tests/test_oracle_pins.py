@@ -443,3 +443,38 @@ def test_fused_matches_numpy_and_entries():
     ms, ns = np.array([0, 36, 5, 17]), np.array([0, 28, 11, 3])
     ent = oracle.gemm_fused_entries(A, B, oracle.E4M3, M, N, K, ms, ns, sa, sb, bias, "bias_gelu")
     np.testing.assert_allclose(ent, got[ms, ns], rtol=1e-13, atol=1e-13)
+
+
+# ----------------------------------------------------------------- W4A8
+
+def test_int4_decode_matches_arithmetic_shift():
+    """A nibble placed in the top half of an int8 and shifted right
+    arithmetically (numpy) gives the two's complement value."""
+    ref = (np.arange(16, dtype=np.uint8) << 4).view(np.int8) >> 4
+    assert [oracle.decode_int4(n) for n in range(16)] == ref.tolist()
+
+
+def test_w4a8_hand_example():
+    """A = [[1,-2],[127,-128]], B = [[3,-1],[-8,7]] packed even-k-low:
+    bytes 0xF3 and 0x78; D = [[5,-22],[509,-1912]].  A swapped nibble order
+    or an unsigned decode fails."""
+    A = np.array([[1, -2], [127, -128]], dtype=np.int8)
+    B = np.array([[0xF3], [0x78]], dtype=np.uint8)
+    assert oracle.gemm_w4a8(A, B, 2, 2, 2).tolist() == [[5, -22], [509, -1912]]
+
+
+def test_w4a8_matches_numpy_int64():
+    """Random int8 x packed int4 against numpy's int64 matmul of an
+    independently unpacked B; the entry form against the full form."""
+    M, N, K = 23, 31, 66
+    A = inputs.random_int8(M, K, 91).numpy()
+    Bp = inputs.random_int4_packed(N, K, 92).numpy()
+    lo = (Bp << 4).view(np.int8) >> 4
+    hi = Bp.view(np.int8) >> 4
+    Bk = np.empty((N, K), dtype=np.int64)
+    Bk[:, 0::2], Bk[:, 1::2] = lo, hi
+    ref = A.astype(np.int64) @ Bk.T
+    got = oracle.gemm_w4a8(A, Bp, M, N, K)
+    assert np.array_equal(got, ref)
+    ms, ns = np.array([0, 22, 7]), np.array([30, 0, 11])
+    assert np.array_equal(oracle.gemm_w4a8_entries(A, Bp, K, ms, ns), ref[ms, ns])

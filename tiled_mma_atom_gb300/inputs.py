@@ -128,6 +128,21 @@ def hashed_int_device(rows: int, cols: int, seed: int, device, dtype: torch.dtyp
     return out
 
 
+def random_int8(rows: int, cols: int, seed: int) -> torch.Tensor:
+    """Uniform int8 in [-128, 127]."""
+    g = _gen(seed)
+    return torch.randint(-128, 128, (rows, cols), generator=g, dtype=torch.int32).to(torch.int8)
+
+
+def random_int4_packed(rows: int, K: int, seed: int) -> torch.Tensor:
+    """(rows, K/2) bytes; each nibble an independent uniform 4-bit code
+    (a two's complement int4 in [-8, 7])."""
+    if K % 2:
+        raise ValueError("K must be even for packed int4")
+    g = _gen(seed)
+    return torch.randint(0, 256, (rows, K // 2), generator=g, dtype=torch.int32).to(torch.uint8)
+
+
 def random_fp4_codes(rows: int, K: int, seed: int) -> torch.Tensor:
     """(rows, K/2) bytes; each nibble an independent uniform e2m1 code."""
     if K % 2:
