@@ -42,14 +42,16 @@ FP8_OVER_BF16 = 4.5 / 2.25
 # fp32 FFMA peak: 152 SMs x 128 FMA/clk x 2 flop x 2.07 GHz
 FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 # GB300 nominal dense peaks (context beside the measured denominators)
-NOMINAL = {"bf16": 2250.0, "e4m3": 4500.0, "mxfp4": 13500.0, "hbm": 7900.0, "alu": FP32_ALU_TFLOPS}
+NOMINAL = {"bf16": 2250.0, "e4m3": 4500.0, "mxfp4": 13500.0, "w4a8": 2250.0, "hbm": 7900.0,
+           "alu": FP32_ALU_TFLOPS}
 L2_FLUSH_BYTES = 512 << 20
 L2_CLEAN_BYTES = 320 << 20
 L2_BYTES = 129 * 10**6
 KERNEL_OF = {"fp32_128": "ffma_gemm_kernel", "bf16_1024": "tc_bf16_kernel",
              "bf16_4096": "tc2_gemm_kernel", "skinny_16x28672x8192": "skinny_tc_kernel",
              "mxfp4_8192": "mxfp4_pair_kernel", "e4m3_8192_bias_gelu": "tc2_gemm_kernel",
-             "bf16_4096_bias_silu": "tc2_gemm_kernel", "bf16_4096_a_mn_major": "tc2_gemm_kernel"}
+             "bf16_4096_bias_silu": "tc2_gemm_kernel", "bf16_4096_a_mn_major": "tc2_gemm_kernel",
+             "w4a8_8192": "tc2_gemm_kernel"}
 
 
 def load_peaks():
@@ -138,6 +140,8 @@ class ClockSampler:
 def input_bytes(w):
     if w.dtype == "mxfp4":
         return (w.M + w.N) * (w.K // 2 + w.K // 32)
+    if w.dtype == "w4a8":
+        return w.M * w.K + w.N * w.K // 2
     elem = {"f32": 4, "bf16": 2, "e4m3": 1}[w.dtype]
     return (w.M + w.N) * w.K * elem
 
@@ -180,6 +184,9 @@ def make_call(w, dev_in, out, stream):
     if w.dtype == "mxfp4":
         A, B, sA, sB = dev_in
         return lambda: tmg.gemm_mxfp4(A, B, sA, sB, out, stream=stream)
+    if w.dtype == "w4a8":
+        A, B = dev_in
+        return lambda: tmg.gemm_w4a8(A, B, out, stream=stream)
     if w.epilogue is not None:
         A, B, sa, sb, bias = dev_in
         return lambda: tmg.gemm_fused(A, B, out, scale_a=sa, scale_b=sb, bias=bias,
@@ -213,6 +220,8 @@ def roofline(w, ms_per_launch, peaks, peak_kind, traffic):
         elif w.dtype == "e4m3":
             peak = peak * FP8_OVER_BF16
             src = f"{peak_kind} bf16 burst x nominal fp8/bf16 ratio 2"
+        if w.dtype == "w4a8":
+            src = f"{peak_kind} bf16 burst (the integer products run on the bf16 tensor cores)"
         r = {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
              "peak_source": src}
     r["frac"] = r["achieved"] / r["peak"]
@@ -229,7 +238,7 @@ def time_device(w, steps, warmup, dev, stream, flush):
     import torch
     import tiled_mma_atom_gb300 as tmg
     host, dev_in = device_inputs(w, dev)
-    dt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+    dt = {"f32": torch.float32, "w4a8": torch.int32}.get(w.dtype, torch.bfloat16)
     out = torch.empty((w.M, w.N), dtype=dt, device=dev)
     call = make_call(w, dev_in, out, stream)
     do_flush, _ = l2_policy(w)
@@ -267,7 +276,7 @@ def time_e2e(w, steps, dev, stream):
     import tiled_mma_atom_gb300 as tmg
     from tiled_mma_atom_gb300 import inputs
     host = [t.pin_memory() for t in inputs.make_inputs(w)]
-    dt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+    dt = {"f32": torch.float32, "w4a8": torch.int32}.get(w.dtype, torch.bfloat16)
     out_host = torch.empty((w.M, w.N), dtype=dt).pin_memory()
     if w.dtype in ("f32", "bf16") and w.epilogue is None and not w.a_mn_major:
         def step():
@@ -318,6 +327,11 @@ def oracle_sample(w, budget_s):
             A, B, sA, sB = [t.numpy() for t in host]
             t0 = time.perf_counter()
             oracle.gemm_mxfp4(A[:rows], B, sA[:rows], sB, rows, w.N, w.K)
+            return time.perf_counter() - t0
+        if w.dtype == "w4a8":
+            A, B = [t.numpy() for t in host]
+            t0 = time.perf_counter()
+            oracle.gemm_w4a8(A[:rows], B, rows, w.N, w.K)
             return time.perf_counter() - t0
         if w.epilogue is not None:
             A, B, sa, sb, bias = host
@@ -499,7 +513,9 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16" if w.dtype == "bf16" else w.dtype, "data": "synthetic",
             "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
-                       "a": w.a_dist, "b": w.b_dist, "accumulate": "fp32",
+                       "a": w.a_dist, "b": w.b_dist,
+                       "accumulate": ("exact integer: fp32 within K segments of 4096, int32 across them"
+                                      if w.dtype == "w4a8" else "fp32"),
                        **({"epilogue": w.epilogue} if w.epilogue else {}),
                        "l2": l2_policy(w)[1],
                        "timing": "CUDA events around each library call on its stream",

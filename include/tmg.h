@@ -183,6 +183,23 @@ tmg_status tmg_gemm_fused(const void *A, const void *B, void *D, int64_t M,
                           const float *bias, tmg_epilogue epilogue,
                           void *stream);
 
+/* W4A8 GEMM: D[m,n] = sum_k a(m,k) * b(n,k), exact, as int32.
+ *   A  device, (M, K) int8 row-major.
+ *   B  device, (N, K/2) bytes row-major: packed signed int4 (two's
+ *      complement, -8..7), the even k in the low nibble (bits 0-3).
+ *   D  device, int32 (M, N) row-major.
+ * "FlyDSL Kernel Authoring Skill", §10 Troubleshooting, item 10 (int8 A,
+ * packed int4 B unpacked in the kernel) and §6 (i8 / i4 atoms accumulating
+ * in i32).  K must be even (else INVALID_ARG); K == 0 writes zeros; results
+ * wrap like int32 arithmetic only if |D| >= 2^31 (K > 2^21 with extreme
+ * values).  GB300 has no integer tensor-core MMA: both operands are unpacked
+ * to bf16 (exact) into per-(device, stream) workspace ((M + N) x K bf16),
+ * multiplied on the bf16 tensor cores in K segments of at most 4096 — where
+ * every fp32 partial sum is an integer below 2^22, hence exact — and each
+ * segment is added into D as int32. */
+tmg_status tmg_gemm_w4a8(const void *A, const void *B, void *D, int64_t M,
+                         int64_t N, int64_t K, void *stream);
+
 /* MXFP4 GEMM: D[m,n] = sum_k a(m,k) * b(n,k) with
  *   a(m,k) = e2m1(code of A at (m,k)) * 2^(scaleA[m, k/32] - 127), same for b.
  *   A       device, (M, K/2) bytes row-major: two e2m1 codes per byte, the

@@ -113,3 +113,12 @@ def test_fused_rejects_bad_arguments_before_device_work(native):
     assert lib.tmg_gemm_fused(16, 16, 16, 0, 4, 64, native.BF16, None, None, None, 0, None) == native.OK
     # E4M3 is not an element type of tmg_gemm (its D would be E4M3)
     assert _call(native, 4, 4, 4, dtype=native.E4M3) == native.ERR_INVALID_ARG
+
+
+def test_w4a8_rejects_bad_arguments_before_device_work(native):
+    lib = native.lib()
+    assert lib.tmg_gemm_w4a8(16, 16, 16, 4, 4, 7, None) == native.ERR_INVALID_ARG      # odd K
+    assert "odd" in lib.tmg_last_error().decode()
+    assert lib.tmg_gemm_w4a8(16, 16, 16, -1, 4, 8, None) == native.ERR_INVALID_ARG
+    assert lib.tmg_gemm_w4a8(16, 16, 16, 0, 4, 8, None) == native.OK
+    assert lib.tmg_gemm_w4a8(None, None, 16, 4, 4, 8, None) == native.ERR_INVALID_ARG

@@ -21,7 +21,7 @@ import torch
 from . import _native
 from ._native import (BF16, E4M3, EPILOGUES, F32, PATHS, Layout, TmgError, make_layout)  # noqa: F401
 
-__all__ = ["gemm", "gemm_host", "gemm_fused", "gemm_mxfp4", "check", "make_layout", "Layout", "TmgError",
+__all__ = ["gemm", "gemm_host", "gemm_fused", "gemm_w4a8", "gemm_mxfp4", "check", "make_layout", "Layout", "TmgError",
            "set_wait_budget_ns", "debug_wait_timeout", "launch_count", "version",
            "shutdown", "PATHS"]
 
@@ -160,6 +160,26 @@ def gemm_fused(A: torch.Tensor, B: torch.Tensor, D: torch.Tensor | None = None, 
                                       _fp32_vec(bias, N, "bias", A.device),
                                       EPILOGUES[epilogue], _stream_handle(stream))
     _native.raise_on(st)
+    return D
+
+
+def gemm_w4a8(A: torch.Tensor, B: torch.Tensor, D: torch.Tensor | None = None, *,
+              stream=None) -> torch.Tensor:
+    """W4A8 GEMM, exact: A (M,K) int8, B (N, K/2) uint8 holding two signed
+    int4 per byte (even k in the low nibble), D (M,N) int32.  All contiguous
+    on the GPU."""
+    if A.dtype != torch.int8 or A.dim() != 2 or not A.is_contiguous() or not A.is_cuda:
+        raise ValueError("A must be a contiguous CUDA int8 tensor of shape (M, K)")
+    M, K = A.shape
+    if B.dtype != torch.uint8 or B.dim() != 2 or B.shape[1] * 2 != K or not B.is_contiguous() or not B.is_cuda:
+        raise ValueError("B must be a contiguous CUDA uint8 tensor of shape (N, K/2)")
+    N = B.shape[0]
+    if D is None:
+        D = torch.empty((M, N), dtype=torch.int32, device=A.device)
+    if D.dtype != torch.int32 or tuple(D.shape) != (M, N) or not D.is_contiguous():
+        raise ValueError("D must be a contiguous int32 tensor of shape (M, N)")
+    _native.raise_on(_native.lib().tmg_gemm_w4a8(A.data_ptr(), B.data_ptr(), D.data_ptr(), M, N, K,
+                                                  _stream_handle(stream)))
     return D
 
 

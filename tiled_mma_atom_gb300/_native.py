@@ -20,7 +20,7 @@ PATHS = {"auto": 0, "ffma": 1, "tc": 2, "skinny": 3, "skinny_ffma": 4, "tc_singl
          "tc_pair": 6, "packed_tc": 7}
 
 # Every function include/tmg.h declares.
-EXPORTS = ("tmg_gemm", "tmg_gemm_ex", "tmg_gemm_host", "tmg_gemm_fused", "tmg_gemm_mxfp4", "tmg_gemm_skinny_noalloc", "tmg_check", "tmg_last_error",
+EXPORTS = ("tmg_gemm", "tmg_gemm_ex", "tmg_gemm_host", "tmg_gemm_fused", "tmg_gemm_w4a8", "tmg_gemm_mxfp4", "tmg_gemm_skinny_noalloc", "tmg_check", "tmg_last_error",
            "tmg_set_wait_budget_ns", "tmg_debug_wait_timeout", "tmg_launch_count",
            "tmg_version", "tmg_shutdown")
 
@@ -82,6 +82,8 @@ def lib():
     L.tmg_gemm_host.restype = ctypes.c_int
     L.tmg_gemm_fused.argtypes = [P, P, P, I64, I64, I64, ctypes.c_int, P, P, P, ctypes.c_int, P]
     L.tmg_gemm_fused.restype = ctypes.c_int
+    L.tmg_gemm_w4a8.argtypes = [P, P, P, I64, I64, I64, P]
+    L.tmg_gemm_w4a8.restype = ctypes.c_int
     L.tmg_gemm_mxfp4.argtypes = [P, P, P, P, P, I64, I64, I64, P]
     L.tmg_gemm_mxfp4.restype = ctypes.c_int
     L.tmg_gemm_skinny_noalloc.argtypes = [P, P, P, I64, I64, I64, I64, I64, I64, P]

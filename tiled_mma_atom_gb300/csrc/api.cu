@@ -895,7 +895,7 @@ tmg_status tmg_gemm_fused(const void *A, const void *B, void *D, int64_t M, int6
     if ((st = device_state(&ds)) != TMG_OK)
         return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const Tc2Epi epi{scale_a, scale_b, bias, static_cast<int>(epilogue)};
+    const Tc2Epi epi{scale_a, scale_b, bias, static_cast<int>(epilogue), 0};
     if (K == 0) {
         cudaError_t e = launch_fused_k0(D, M, N, epi, s);
         return e == cudaSuccess ? TMG_OK : cuda_fail(e, "fused K=0 launch");
@@ -929,6 +929,72 @@ tmg_status tmg_gemm_fused(const void *A, const void *B, void *D, int64_t M, int6
         return st;
     cudaError_t e = launch_tc2_fused(a, epi, e4m3, err_ctx(*ds), s);
     return e == cudaSuccess ? TMG_OK : cuda_fail(e, "fused pair launch");
+}
+
+tmg_status tmg_gemm_w4a8(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, void *stream)
+{
+    t_last_error.clear();
+    if (M < 0 || N < 0 || K < 0)
+        return fail(TMG_ERR_INVALID_ARG, "negative extent M=%lld N=%lld K=%lld", (long long)M, (long long)N,
+                    (long long)K);
+    if (K % 2)
+        return fail(TMG_ERR_INVALID_ARG, "K=%lld is odd (B packs two int4 values per byte)", (long long)K);
+    if (M == 0 || N == 0)
+        return TMG_OK;
+    if (!D || (K > 0 && (!A || !B)))
+        return fail(TMG_ERR_INVALID_ARG, "null operand pointer");
+    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX)
+        return fail(TMG_ERR_UNSUPPORTED, "extents beyond 2^31");
+    DeviceState *ds = nullptr;
+    tmg_status st;
+    if ((st = device_state(&ds)) != TMG_OK)
+        return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (K == 0) {
+        e = cudaMemsetAsync(D, 0, static_cast<size_t>(M) * N * sizeof(int32_t), s);
+        return e == cudaSuccess ? TMG_OK : cuda_fail(e, "cudaMemsetAsync(W4A8 D)");
+    }
+    const int64_t ldp = (K + 7) / 8 * 8;
+    void *PA = pack_scratch(0, static_cast<size_t>(M) * ldp * 2, s, &st);
+    if (!PA)
+        return st;
+    void *PB = pack_scratch(1, static_cast<size_t>(N) * ldp * 2, s, &st);
+    if (!PB)
+        return st;
+    if ((e = launch_unpack_w4a8(A, B, M, N, K, PA, PB, ldp, ds->num_sms, s)) != cudaSuccess)
+        return cuda_fail(e, "W4A8 unpack launch");
+    // K segments of at most 4096: every partial sum of a segment is an integer
+    // of magnitude <= 128 * 8 * 4096 = 2^22, exact in the fp32 accumulator;
+    // the first segment stores its int32 result, the others add to it.
+    constexpr int64_t kSeg = 4096;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    for (int64_t k0 = 0; k0 < K; k0 += kSeg) {
+        const int64_t kc = K - k0 < kSeg ? K - k0 : kSeg;
+        TcArgs a;
+        std::memset(&a, 0, sizeof a);
+        a.bn = tc2_fused_pick_bn(N);
+        a.kb_elems = 64;
+        const uint16_t *pa = static_cast<const uint16_t *>(PA) + k0, *pb = static_cast<const uint16_t *>(PB) + k0;
+        if ((st = encode_2d(&a.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pa, kc, M, ldp, 64, 128)) != TMG_OK)
+            return st;
+        if ((st = encode_2d(&a.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pb, kc, N, ldp, 64, a.bn / 2)) != TMG_OK)
+            return st;
+        a.D = D;
+        a.ldd = N;
+        a.M = static_cast<int>(M);
+        a.N = static_cast<int>(N);
+        a.K = static_cast<int>(kc);
+        a.d_tma = 0;
+        tc2_plan(a, ds->num_sms);
+        if ((st = tc2_scratch(dev, s, a)) != TMG_OK)
+            return st;
+        const Tc2Epi epi{nullptr, nullptr, nullptr, kEpiNone, k0 == 0 ? 1 : 2};
+        if ((e = launch_tc2_fused(a, epi, false, err_ctx(*ds), s)) != cudaSuccess)
+            return cuda_fail(e, "W4A8 GEMM launch");
+    }
+    return TMG_OK;
 }
 
 tmg_status tmg_gemm_mxfp4(const void *A, const void *B, const void *scaleA, const void *scaleB, void *D, int64_t M,

@@ -78,6 +78,7 @@ struct Tc2Epi {
     const float *scale_b;
     const float *bias;
     int epi;
+    int out_i32;       // 0: bf16 D; 1: int32 D = round(y); 2: int32 D += round(y) (no TMA stores)
 };
 // Pair kernel with the fused epilogue (tc2_fused.cu); bf16 or E4M3 inputs
 // (tmA/tmB over bytes for E4M3, box {128, rows}; a.kb_elems = 128);
@@ -85,6 +86,10 @@ struct Tc2Epi {
 cudaError_t launch_tc2_fused(const TcArgs &a, const Tc2Epi &e, bool in_e4m3, const ErrCtx &err,
                              cudaStream_t s);
 int tc2_fused_pick_bn(int64_t N);
+// W4A8 operands: A (M, K) int8 and B (N, K/2) packed int4 unpacked to bf16
+// (M, ldp) and (N, ldp), zero-padded past K; ldp a multiple of 8.
+cudaError_t launch_unpack_w4a8(const void *A, const void *B, int64_t M, int64_t N, int64_t K, void *PA, void *PB,
+                               int64_t ldp, int num_sms, cudaStream_t s);
 // D[m,n] = bf16(act(bias[n])) (or 0 without a bias): the fused GEMM at K = 0.
 cudaError_t launch_fused_k0(void *D, int64_t M, int64_t N, const Tc2Epi &e, cudaStream_t s);
 // Fill pairs / dp_tiles / sk_tiles for a.M, a.N, a.K, a.bn.

@@ -63,7 +63,7 @@ int tc2_pick_bn(int64_t M, int64_t N, int num_sms)
 cudaError_t launch_tc2_bf16(const TcArgs &a, int num_sms, const ErrCtx &err, cudaStream_t s)
 {
     (void)num_sms;
-    const Tc2Epi none{nullptr, nullptr, nullptr, kEpiNone};
+    const Tc2Epi none{nullptr, nullptr, nullptr, kEpiNone, 0};
     switch (a.bn) {
     case 256:
         return launch_pair<256, kInBf16, false>(a, none, err, s);

@@ -175,6 +175,31 @@ __device__ __forceinline__ void store_row_chunk(__nv_bfloat16 *drow, int col0, i
     }
 }
 
+// 32 integer-valued fp32 results of one row as int32 at drow[col0 ..]
+// (bounded by N), stored or added to what D holds (the W4A8 GEMM's K
+// segments).  The values are exact integers, so rounding is exact.
+__device__ __forceinline__ void store_row_i32(int32_t *drow, int col0, int N, int vec_ok, const float (&v)[32],
+                                              bool accumulate)
+{
+    if (vec_ok && col0 + 32 <= N) {
+        int4 *dst = reinterpret_cast<int4 *>(drow + col0);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            int4 o = accumulate ? dst[j] : make_int4(0, 0, 0, 0);
+            o.x += __float2int_rn(v[4 * j]);
+            o.y += __float2int_rn(v[4 * j + 1]);
+            o.z += __float2int_rn(v[4 * j + 2]);
+            o.w += __float2int_rn(v[4 * j + 3]);
+            dst[j] = o;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (col0 + j < N)
+                drow[col0 + j] = (accumulate ? drow[col0 + j] : 0) + __float2int_rn(v[j]);
+    }
+}
+
 // GELU(y) = y * Phi(y), Phi(y) = erfc(-y / sqrt 2) / 2, with erfc from
 // Abramowitz & Stegun, Handbook of Mathematical Functions, formula 7.1.26:
 // erfc(x) = t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) e^(-x^2),
@@ -455,6 +480,14 @@ __global__ void __launch_bounds__(tc2_threads(EPI), 1)
                         apply_epilogue<BN>(v, epi, sa_row, cols, c * 32);
                     const int col0 = tn * BN + c * 32;
                     const int row0 = row - lane;
+                    if constexpr (EPI) {
+                        if (epi.out_i32) {
+                            if (row < M)
+                                store_row_i32(reinterpret_cast<int32_t *>(D) + static_cast<int64_t>(row) * ldd, col0, N,
+                                              vec_ok, v, epi.out_i32 == 2);
+                            continue;
+                        }
+                    }
                     if (d_tma) {
                         // stage this warp's 32 x 32 box, then one lane stores it
                         if (row0 >= M || col0 >= N)
@@ -541,8 +574,15 @@ __global__ void __launch_bounds__(tc2_threads(EPI), 1)
                         v[4 * j + 3] += p.w;
                     }
                 }
-                if constexpr (EPI)
+                if constexpr (EPI) {
                     apply_epilogue<BN>(v, epi, sa_row, cols, c * 32);
+                    if (epi.out_i32) {
+                        if (row < M)
+                            store_row_i32(reinterpret_cast<int32_t *>(D) + static_cast<int64_t>(row) * ldd,
+                                          tn * BN + c * 32, N, vec_ok, v, epi.out_i32 == 2);
+                        continue;
+                    }
+                }
                 if (row < M)
                     store_row_chunk(drow, tn * BN + c * 32, N, vec_ok, v);
             }

@@ -52,6 +52,9 @@ WORKLOADS = {
                                     "N(0,1) -> e4m3", "N(0,1) -> e4m3", "bias_gelu"),
     "bf16_4096_bias_silu": Workload("bf16_4096_bias_silu", 6, 4096, 4096, 4096, "bf16",
                                     "N(0,1)", "N(0,1)", "bias_silu"),
+    # W4A8: int8 A x packed int4 B -> int32
+    "w4a8_8192": Workload("w4a8_8192", 8, 8192, 8192, 8192, "w4a8", "int8 U[-128,127]",
+                          "int4 U[-8,7], packed"),
     # general layout: A given column-major, (M,K):(1,M)
     "bf16_4096_a_mn_major": Workload("bf16_4096_a_mn_major", 7, 4096, 4096, 4096, "bf16",
                                      "N(0,1), stored MN-major", "N(0,1)", None, True),
@@ -186,6 +189,8 @@ def make_inputs(w: Workload):
         if w.a_mn_major:
             A = A.t().contiguous()
         return A, normal_bf16(w.N, w.K, s + 1, std=std_b)
+    if w.dtype == "w4a8":
+        return random_int8(M, w.K, s + 0), random_int4_packed(w.N, w.K, s + 1)
     if w.dtype == "mxfp4":
         return (random_fp4_codes(M, w.K, s + 0), random_fp4_codes(w.N, w.K, s + 1),
                 random_e8m0(M, w.K, s + 2), random_e8m0(w.N, w.K, s + 3))
