@@ -51,7 +51,7 @@ KERNEL_OF = {"fp32_128": "ffma_gemm_kernel", "bf16_1024": "tc_bf16_kernel",
              "bf16_4096": "tc2_gemm_kernel", "skinny_16x28672x8192": "skinny_tc_kernel",
              "mxfp4_8192": "mxfp4_pair_kernel", "e4m3_8192_bias_gelu": "tc2_gemm_kernel",
              "bf16_4096_bias_silu": "tc2_gemm_kernel", "bf16_4096_a_mn_major": "tc2_gemm_kernel",
-             "w4a8_8192": "tc2_gemm_kernel"}
+             "w4a8_8192": "tc2_gemm_kernel", "w4a8_16x28672x8192": "w4a8_skinny_kernel"}
 
 
 def load_peaks():
@@ -199,8 +199,11 @@ def make_call(w, dev_in, out, stream):
 
 def roofline(w, ms_per_launch, peaks, peak_kind, traffic):
     t = ms_per_launch * 1e-3
-    if w.name.startswith("skinny"):
-        alg = (w.M * w.K + w.N * w.K + w.M * w.N) * 2
+    if w.name.startswith("skinny") or (w.dtype == "w4a8" and w.M <= 64):
+        if w.dtype == "w4a8":    # int8 A, 4-bit B, int32 D
+            alg = w.M * w.K + w.N * w.K // 2 + w.M * w.N * 4
+        else:
+            alg = (w.M * w.K + w.N * w.K + w.M * w.N) * 2
         ach = alg / t / 1e9
         peak = peaks["hbm_gbs"]
         r = {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",

@@ -69,3 +69,47 @@ def test_w4a8_workload_sampled(tmg):
     ns = np.concatenate([rng.integers(0, w.N, 3000), [w.N - 1, 0]])
     ref = oracle.gemm_w4a8_entries(A.numpy(), B.numpy(), w.K, ms, ns)
     assert np.array_equal(D.cpu().numpy()[ms, ns].astype(np.int64), ref)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1000, 128), (16, 1024, 4096), (17, 777, 1280), (64, 2048, 2048)])
+def test_w4a8_decode_exact(tmg, M, N, K):
+    """Decode shapes (M <= 64, K a multiple of 128): the weights stay 4-bit
+    until shared memory; ragged N, several partial (stream-K) tiles."""
+    A, B = inputs.random_int8(M, K, 711), inputs.random_int4_packed(N, K, 712)
+    assert np.array_equal(_run(tmg, A, B), oracle.gemm_w4a8(A.numpy(), B.numpy(), M, N, K))
+
+
+def test_w4a8_decode_extreme_values_at_max_k(tmg):
+    """K = 32768, the decode kernel's limit: a = -128 (hi = -8, lo = 0) times
+    b = -8 gives column sums of 64 K = 2^21 and D = 2^25; a = 127 (hi = 7,
+    lo = 15) times b = 7: D = 127 * 7 * K."""
+    M, N, K = 16, 384, 32768
+    A = torch.full((M, K), -128, dtype=torch.int8)
+    B = torch.full((N, K // 2), 0x88, dtype=torch.uint8)
+    assert (_run(tmg, A, B) == 1024 * K).all()
+    A2 = torch.full((M, K), 127, dtype=torch.int8)
+    B2 = torch.full((N, K // 2), 0x77, dtype=torch.uint8)
+    assert (_run(tmg, A2, B2) == 127 * 7 * K).all()
+
+
+def test_w4a8_decode_and_general_paths_agree(tmg, monkeypatch):
+    """The same decode-shaped problem through both paths: identical int32."""
+    M, N, K = 32, 1536, 2048
+    A, B = inputs.random_int8(M, K, 721), inputs.random_int4_packed(N, K, 722)
+    d1 = _run(tmg, A, B)
+    monkeypatch.setenv("TMG_W4A8_PATH", "general")
+    d2 = _run(tmg, A, B)
+    assert np.array_equal(d1, d2)
+    assert np.array_equal(d1, oracle.gemm_w4a8(A.numpy(), B.numpy(), M, N, K))
+
+
+def test_w4a8_decode_workload_sampled(tmg):
+    w = inputs.WORKLOADS["w4a8_16x28672x8192"]
+    A, B = inputs.make_inputs(w)
+    D = tmg.gemm_w4a8(A.to(DEV), B.to(DEV))
+    tmg.check()
+    rng = np.random.default_rng(12)
+    ms = rng.integers(0, w.M, 4000)
+    ns = np.concatenate([rng.integers(0, w.N, 3998), [0, w.N - 1]])
+    ref = oracle.gemm_w4a8_entries(A.numpy(), B.numpy(), w.K, ms, ns)
+    assert np.array_equal(D.cpu().numpy()[ms, ns].astype(np.int64), ref)

@@ -23,8 +23,6 @@
 #include <cstdlib>
 #include <cstring>
 #include <map>
-#include <set>
-#include <tuple>
 #include <unordered_map>
 #include <mutex>
 #include <string>
@@ -633,22 +631,29 @@ void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 cudaError_t ensure_smem_attr(const void *func, int bytes)
 {
+    // The attribute is an upper bound on the dynamic shared memory of later
+    // launches, so it only ever grows: remember the largest value set per
+    // (device, kernel) — kernels whose size depends on the problem launch
+    // with several sizes.
     static std::mutex mu;
-    static std::set<std::tuple<int, const void *, int>> done;
+    static std::map<std::pair<int, const void *>, int> largest;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
-    const auto key = std::make_tuple(dev, func, bytes);
+    const auto key = std::make_pair(dev, func);
     {
         std::lock_guard<std::mutex> lk(mu);
-        if (done.count(key))
+        auto it = largest.find(key);
+        if (it != largest.end() && it->second >= bytes)
             return cudaSuccess;
     }
     e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e == cudaSuccess) {
         std::lock_guard<std::mutex> lk(mu);
-        done.insert(key);
+        int &v = largest[key];
+        if (v < bytes)
+            v = bytes;
     }
     return e;
 }
@@ -954,6 +959,42 @@ tmg_status tmg_gemm_w4a8(const void *A, const void *B, void *D, int64_t M, int64
     if (K == 0) {
         e = cudaMemsetAsync(D, 0, static_cast<size_t>(M) * N * sizeof(int32_t), s);
         return e == cudaSuccess ? TMG_OK : cuda_fail(e, "cudaMemsetAsync(W4A8 D)");
+    }
+    // Decode shapes: the weights stay 4-bit until shared memory.
+    bool decode = M <= 64 && K % 128 == 0 && K <= 32768;
+    if (const char *f = getenv("TMG_W4A8_PATH")) {      // testing aid: "general" | "decode"
+        if (!strcmp(f, "general"))
+            decode = false;
+    }
+    if (decode && tma_ok(B, K / 2, 1, N, K / 2)) {
+        W4a8SkinnyArgs w;
+        std::memset(&w, 0, sizeof w);
+        w.mp = static_cast<int>((M + 15) / 16 * 16);
+        uint8_t *Ap = static_cast<uint8_t *>(pack_scratch(0, static_cast<size_t>(2 * w.mp) * K, s, &st));
+        if (!Ap)
+            return st;
+        if ((st = encode_2d(&w.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, K / 2, N, K / 2, 64, 128,
+                            CU_TENSOR_MAP_SWIZZLE_NONE)) != TMG_OK)
+            return st;
+        if ((st = encode_2d(&w.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Ap, K, 2 * w.mp, K, 128, 2 * w.mp)) != TMG_OK)
+            return st;
+        w.grid = w4a8_skinny_grid(N, K, ds->num_sms);
+        int dev = 0;
+        cudaGetDevice(&dev);
+        Scratch *sc = skinny_scratch(dev, s, skinny_partials_bytes(w.grid, w.mp), skinny_counters_bytes(N), &st);
+        if (!sc)
+            return st;
+        w.partials = reinterpret_cast<int32_t *>(sc->partials);
+        w.counters = sc->counters;
+        w.A = A;
+        w.Ap = Ap;
+        w.D = static_cast<int32_t *>(D);
+        w.ldd = N;
+        w.M = static_cast<int>(M);
+        w.N = static_cast<int>(N);
+        w.K = static_cast<int>(K);
+        e = launch_w4a8_skinny(w, err_ctx(*ds), s);
+        return e == cudaSuccess ? TMG_OK : cuda_fail(e, "W4A8 decode launch");
     }
     const int64_t ldp = (K + 7) / 8 * 8;
     void *PA = pack_scratch(0, static_cast<size_t>(M) * ldp * 2, s, &st);

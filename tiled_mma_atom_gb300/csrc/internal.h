@@ -90,6 +90,25 @@ int tc2_fused_pick_bn(int64_t N);
 // (M, ldp) and (N, ldp), zero-padded past K; ldp a multiple of 8.
 cudaError_t launch_unpack_w4a8(const void *A, const void *B, int64_t M, int64_t N, int64_t K, void *PA, void *PB,
                                int64_t ldp, int num_sms, cudaStream_t s);
+// Decode-shaped W4A8 (w4a8_skinny.cu): M <= 64, K a multiple of 128 and at
+// most 32768.  tmB: packed weights (N, K/2) u8, box {64, 128}, no swizzle;
+// tmA: the split activations A' (2 mp, K) E4M3 (written by the launch's
+// pre-pass into Ap), box {128, 2 mp}, 128-byte swizzle.
+struct W4a8SkinnyArgs {
+    CUtensorMap tmB;
+    CUtensorMap tmA;
+    const void *A;        // (M, K) int8
+    uint8_t *Ap;          // scratch: 2 mp x K bytes
+    int32_t *D;           // (M, N) int32 row-major, row stride ldd
+    int64_t ldd;
+    int M, N, K, mp;
+    int32_t *partials;    // skinny_partials_bytes(grid, mp)
+    uint32_t *counters;   // skinny_counters_bytes(N), zero on entry
+    int grid;
+};
+int w4a8_skinny_grid(int64_t N, int64_t K, int num_sms);
+cudaError_t launch_w4a8_skinny(const W4a8SkinnyArgs &a, const ErrCtx &err, cudaStream_t s);
+
 // D[m,n] = bf16(act(bias[n])) (or 0 without a bias): the fused GEMM at K = 0.
 cudaError_t launch_fused_k0(void *D, int64_t M, int64_t N, const Tc2Epi &e, cudaStream_t s);
 // Fill pairs / dp_tiles / sk_tiles for a.M, a.N, a.K, a.bn.

@@ -55,6 +55,8 @@ WORKLOADS = {
     # W4A8: int8 A x packed int4 B -> int32
     "w4a8_8192": Workload("w4a8_8192", 8, 8192, 8192, 8192, "w4a8", "int8 U[-128,127]",
                           "int4 U[-8,7], packed"),
+    "w4a8_16x28672x8192": Workload("w4a8_16x28672x8192", 9, 16, 28672, 8192, "w4a8", "int8 U[-128,127]",
+                                   "int4 U[-8,7], packed"),
     # general layout: A given column-major, (M,K):(1,M)
     "bf16_4096_a_mn_major": Workload("bf16_4096_a_mn_major", 7, 4096, 4096, 4096, "bf16",
                                      "N(0,1), stored MN-major", "N(0,1)", None, True),
