@@ -71,25 +71,28 @@ def test_w4a8_workload_sampled(tmg):
     assert np.array_equal(D.cpu().numpy()[ms, ns].astype(np.int64), ref)
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 1000, 128), (16, 1024, 4096), (17, 777, 1280), (64, 2048, 2048)])
+@pytest.mark.parametrize("M,N,K", [(1, 1000, 128), (16, 1024, 4096), (17, 777, 1280), (64, 2048, 2048),
+                                   (5, 300, 1056), (33, 129, 32)])
 def test_w4a8_decode_exact(tmg, M, N, K):
-    """Decode shapes (M <= 64, K a multiple of 128): the weights stay 4-bit
-    until shared memory; ragged N, several partial (stream-K) tiles."""
+    """Decode shapes (M <= 64, K a multiple of 32): the weights stay 4-bit
+    until the kernel; ragged N, a ragged last K block of 256, several
+    partial (stream-K) tiles."""
     A, B = inputs.random_int8(M, K, 711), inputs.random_int4_packed(N, K, 712)
     assert np.array_equal(_run(tmg, A, B), oracle.gemm_w4a8(A.numpy(), B.numpy(), M, N, K))
 
 
 def test_w4a8_decode_extreme_values_at_max_k(tmg):
-    """K = 32768, the decode kernel's limit: a = -128 (hi = -8, lo = 0) times
-    b = -8 gives column sums of 64 K = 2^21 and D = 2^25; a = 127 (hi = 7,
-    lo = 15) times b = 7: D = 127 * 7 * K."""
+    """K = 32768, the decode kernel's limit, with the values that drive its
+    fp32 column sums furthest from zero: the kernel splits a = 16 hi + lo
+    (hi = (a + 8) >> 4, lo in [-8, 7]) and offsets b by 8 (u = b + 8 in
+    0..15), so hi = +-8 or lo = -8 against u = 15 give |sum| = 120 K, just
+    below 2^22; a = -128 against b = -8 (u = 0) puts all of D = 2^25 in the
+    row-sum correction."""
     M, N, K = 16, 384, 32768
-    A = torch.full((M, K), -128, dtype=torch.int8)
-    B = torch.full((N, K // 2), 0x88, dtype=torch.uint8)
-    assert (_run(tmg, A, B) == 1024 * K).all()
-    A2 = torch.full((M, K), 127, dtype=torch.int8)
-    B2 = torch.full((N, K // 2), 0x77, dtype=torch.uint8)
-    assert (_run(tmg, A2, B2) == 127 * 7 * K).all()
+    for a, byte, b in [(-128, 0x88, -8), (127, 0x77, 7), (-128, 0x77, 7), (8, 0x77, 7)]:
+        A = torch.full((M, K), a, dtype=torch.int8)
+        B = torch.full((N, K // 2), byte, dtype=torch.uint8)
+        assert (_run(tmg, A, B) == a * b * K).all(), (a, b)
 
 
 def test_w4a8_decode_and_general_paths_agree(tmg, monkeypatch):

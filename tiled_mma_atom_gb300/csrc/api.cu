@@ -961,7 +961,7 @@ tmg_status tmg_gemm_w4a8(const void *A, const void *B, void *D, int64_t M, int64
         return e == cudaSuccess ? TMG_OK : cuda_fail(e, "cudaMemsetAsync(W4A8 D)");
     }
     // Decode shapes: the weights stay 4-bit until shared memory.
-    bool decode = M <= 64 && K % 128 == 0 && K <= 32768;
+    bool decode = M <= 64 && K % 32 == 0 && K <= 32768;
     if (const char *f = getenv("TMG_W4A8_PATH")) {      // testing aid: "general" | "decode"
         if (!strcmp(f, "general"))
             decode = false;
@@ -970,11 +970,12 @@ tmg_status tmg_gemm_w4a8(const void *A, const void *B, void *D, int64_t M, int64
         W4a8SkinnyArgs w;
         std::memset(&w, 0, sizeof w);
         w.mp = static_cast<int>((M + 15) / 16 * 16);
-        uint8_t *Ap = static_cast<uint8_t *>(pack_scratch(0, static_cast<size_t>(2 * w.mp) * K, s, &st));
+        // A' (2 mp rows of K bytes), then the mp int32 row sums
+        const size_t ap_bytes = static_cast<size_t>(2 * w.mp) * K;
+        uint8_t *Ap = static_cast<uint8_t *>(pack_scratch(0, ap_bytes + 4 * static_cast<size_t>(w.mp), s, &st));
         if (!Ap)
             return st;
-        if ((st = encode_2d(&w.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, K / 2, N, K / 2, 64, 128,
-                            CU_TENSOR_MAP_SWIZZLE_NONE)) != TMG_OK)
+        if ((st = encode_2d(&w.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, K / 2, N, K / 2, 128, 128)) != TMG_OK)
             return st;
         if ((st = encode_2d(&w.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Ap, K, 2 * w.mp, K, 128, 2 * w.mp)) != TMG_OK)
             return st;
@@ -988,6 +989,7 @@ tmg_status tmg_gemm_w4a8(const void *A, const void *B, void *D, int64_t M, int64
         w.counters = sc->counters;
         w.A = A;
         w.Ap = Ap;
+        w.R = reinterpret_cast<int32_t *>(Ap + ap_bytes);
         w.D = static_cast<int32_t *>(D);
         w.ldd = N;
         w.M = static_cast<int>(M);

@@ -90,15 +90,16 @@ int tc2_fused_pick_bn(int64_t N);
 // (M, ldp) and (N, ldp), zero-padded past K; ldp a multiple of 8.
 cudaError_t launch_unpack_w4a8(const void *A, const void *B, int64_t M, int64_t N, int64_t K, void *PA, void *PB,
                                int64_t ldp, int num_sms, cudaStream_t s);
-// Decode-shaped W4A8 (w4a8_skinny.cu): M <= 64, K a multiple of 128 and at
-// most 32768.  tmB: packed weights (N, K/2) u8, box {64, 128}, no swizzle;
-// tmA: the split activations A' (2 mp, K) E4M3 (written by the launch's
-// pre-pass into Ap), box {128, 2 mp}, 128-byte swizzle.
+// Decode-shaped W4A8 (w4a8_skinny.cu): M <= 64, K a multiple of 32 and at
+// most 32768.  tmB: packed weights (N, K/2) u8, box {128, 128}, 128-byte
+// swizzle; tmA: the split activations A' (2 mp, K) E4M3 (written by the
+// launch's pre-pass into Ap), box {128, 2 mp}, 128-byte swizzle.
 struct W4a8SkinnyArgs {
     CUtensorMap tmB;
     CUtensorMap tmA;
     const void *A;        // (M, K) int8
     uint8_t *Ap;          // scratch: 2 mp x K bytes
+    int32_t *R;           // scratch: mp row sums of A
     int32_t *D;           // (M, N) int32 row-major, row stride ldd
     int64_t ldd;
     int M, N, K, mp;

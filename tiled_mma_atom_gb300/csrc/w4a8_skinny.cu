@@ -4,27 +4,36 @@
 //
 // The pages' W4A8 kernel unpacks the int4 B to int8 in the kernel and uses
 // an i8 x i8 -> i32 atom ("FlyDSL Kernel Authoring Skill", §10 item 10; §6
-// integer WMMA rows).  GB300 has no integer tensor-core MMA, so here the
-// unpack targets E4M3, which holds every int4 value exactly, and the MMA is
-// tcgen05 kind::f8f6f4 with fp32 accumulation:
-//   * each weight tile (128 rows of B x 128 k, 8 KB packed) lands in shared
-//     memory by TMA; converter warps turn its nibbles into E4M3 bytes (a
-//     16-entry lookup done with byte permutes) written in the 128-byte
-//     swizzled K-major layout the MMA reads;
-//   * an int8 activation a = 16 hi + lo with hi in [-8, 7] and lo in [0, 15],
-//     both exact in E4M3: a small pre-pass writes A' (2 mp rows: hi rows,
-//     then lo rows), and the MMA's N covers both (swap-AB as in skinny.cu:
-//     the 128-row MMA dimension runs over weight rows);
-//   * each fp32 column sum is an integer of magnitude <= 120 K < 2^22 for
-//     K <= 32768, hence exact; the epilogue forms 16 S_hi + S_lo in int32.
+// integer WMMA rows).  GB300 has no integer tensor-core MMA, so the product
+// runs as tcgen05 kind::f8f6f4 (E4M3 operands, fp32 accumulation) on values
+// that E4M3 holds exactly:
+//   * weights in offset binary: u = v + 8 = nibble XOR 8, in 0..15.  The
+//     E4M3 codes 0..15 (exponent field 0 or 1) are exactly c * 2^-9, so the
+//     byte holding u IS the E4M3 code of u * 2^-9: the conversion spreads
+//     nibbles to bytes with two logic ops per four values;
+//   * an int8 activation a = 16 hi + lo with hi = (a + 8) >> 4 in [-8, 8]
+//     and lo in [-8, 7], both exact in E4M3 (normal codes); a small
+//     pre-pass writes A' (2 mp rows: hi rows, then lo rows) and the row sums
+//     R[m] = sum_k A[m, k];
+//   * sum_k a v = 2^9 (16 S_hi + S_lo) - 8 R[m], where S_hi, S_lo are the
+//     fp32 column sums; each is an integer multiple of 2^-9 of magnitude at
+//     most 120 K 2^-9 (K <= 32768 keeps the integer part below 2^22), hence
+//     exact.
+// The converted weights never touch shared memory: converter warps write
+// them to tensor memory (tcgen05.st) and the MMA reads its A operand from
+// there (swap-AB as in skinny.cu: the 128-row MMA dimension runs over
+// weight rows, N = 2 mp over the A' rows).  Inside each group of 8 k the
+// converters emit the even k first, then the odd k; the pre-pass writes A'
+// in the same order, so the products pair up.
 // Work split, partial tiles and their fixed-order fix-up follow skinny.cu
 // (stream-K over (tile, K block) units, per-tile counters per lane quarter).
 //
 // Warps: 0 TMA producer; 1 MMA issuer and TMEM owner; 2..5 epilogue (one
-// per TMEM lane quarter); 6..13 converters.  Shared memory: a ring of
-// STAGES staging slots (packed weights + A' tile), and a ring of kConvBufs
-// converted weight tiles, each with its own barriers.
-#include <cuda_bf16.h>
+// per TMEM lane quarter); 6..13 converters (two per lane quarter, each 32 of
+// a K block's 64 weight columns).  Shared memory: a ring of staging slots
+// (packed weights, 128-byte swizzled rows, and two A' boxes).  TMEM: two
+// accumulators (columns 0-255) and four converted weight buffers (256-511).
+#include <cuda_fp8.h>
 
 #include <cstring>
 
@@ -33,28 +42,34 @@
 namespace tmg {
 namespace {
 
-constexpr int kTileN = 128;                       // weight rows per tile (MMA M)
-constexpr int kBK = 128;                          // k per K block: 128 E4M3 bytes per row
-constexpr int kPackedBytes = kTileN * kBK / 2;    // 8 KB of int4 per tile and K block
-constexpr int kConvBytes = kTileN * kBK;          // 16 KB of E4M3
-constexpr int kConvBufs = 4;
+constexpr int kTileN = 128;                       // weight rows per tile (MMA M, TMEM lanes)
+constexpr int kBK = 256;                          // k per K block
+constexpr int kPackedBytes = kTileN * kBK / 2;    // 16 KB: 128 rows x 128 bytes of nibbles
+constexpr int kABoxK = 128;                       // k (bytes) per A' box row: one 128-byte swizzle span
+constexpr int kWCols = kBK / 4;                   // TMEM columns of E4M3 weights per K block (64)
+constexpr int kWBufs = 4;
+constexpr int kAccCols = 128;                     // one accumulator: 2 mp <= 128 columns
+constexpr int kWCol0 = 2 * kAccCols;              // first weight column
+constexpr int kTmemCols = 512;
 constexpr int kMaxMP = 64;
 constexpr int kConvWarps = 8;
-constexpr int kThreads = 32 * (6 + kConvWarps);   // 448
-constexpr int kTmemCols = 256;                    // two accumulators of up to 2 x 64 columns
+constexpr int kFirstConvWarp = 6;
+constexpr int kThreads = 32 * (kFirstConvWarp + kConvWarps);   // 448
 constexpr int kMaxStages = 16;
 constexpr int kSmemBudget = 225 * 1024;
 
-// Staging slot: packed weights, then A' (2 mp rows x 128 bytes, 1 KB aligned).
-__host__ __device__ constexpr int stage_bytes(int mp) { return kPackedBytes + 2 * mp * kBK; }
-__host__ __device__ constexpr int conv_region() { return kConvBufs * kConvBytes; }
-__host__ __device__ constexpr int bar_bytes() { return (2 * kMaxStages + 2 * kConvBufs + 4) * 8 + 16; }
+static_assert(kWCol0 + kWBufs * kWCols <= kTmemCols, "TMEM columns");
+
+// Staging slot: packed weights, then two A' boxes (2 mp rows x 128 bytes each).
+__host__ __device__ constexpr int a_box_bytes(int mp) { return 2 * mp * kABoxK; }
+__host__ __device__ constexpr int stage_bytes(int mp) { return kPackedBytes + 2 * a_box_bytes(mp); }
+__host__ __device__ constexpr int bar_bytes() { return (2 * kMaxStages + 2 * kWBufs + 4) * 8 + 16; }
 int stages_for(int mp)
 {
-    int s = (kSmemBudget - conv_region() - bar_bytes() - 1024) / stage_bytes(mp);
+    int s = (kSmemBudget - bar_bytes() - 1024) / stage_bytes(mp);
     return s > kMaxStages ? kMaxStages : s;
 }
-int smem_for(int mp) { return stages_for(mp) * stage_bytes(mp) + conv_region() + bar_bytes() + 1024; }
+int smem_for(int mp) { return stages_for(mp) * stage_bytes(mp) + bar_bytes() + 1024; }
 
 __device__ __forceinline__ int64_t unit_start(int c, int64_t U, int G) { return (static_cast<int64_t>(c) * U) / G; }
 
@@ -68,96 +83,111 @@ __device__ __forceinline__ int unit_owner(int64_t u, int64_t U, int G)
     return static_cast<int>(((u + 1) * G - 1) / U);
 }
 
-// E4M3 codes of the int4 values: nibble n (two's complement) -> code.
-// Non-negative v = 1..7 are (1 + m/8) 2^e with bias 7: 1 = 0x38, 2 = 0x40,
-// 3 = 0x44, 4 = 0x48, 5 = 0x4A, 6 = 0x4C, 7 = 0x4E; -v sets the sign bit;
-// -8 = -(1.0 x 2^3) = 0xD0.  Packed four per word, little-endian.
-constexpr uint32_t kLut0 = 0x44403800u;   // n = 0..3  ->  0, 1, 2, 3
-constexpr uint32_t kLut1 = 0x4E4C4A48u;   // n = 4..7  ->  4, 5, 6, 7
-constexpr uint32_t kLut2 = 0xCACCCED0u;   // n = 8..11 -> -8, -7, -6, -5
-constexpr uint32_t kLut3 = 0xB8C0C4C8u;   // n = 12..15 -> -4, -3, -2, -1
-
-// Four nibbles (bits 0-15 of sel, nibble i -> output byte i) to four codes.
-__device__ __forceinline__ uint32_t int4x4_to_e4m3(uint32_t sel)
+// Programmatic dependent launch: the pre-pass lets the GEMM start early;
+// the GEMM waits for the pre-pass's results only where it reads them.
+__device__ __forceinline__ void griddep_launch_dependents()
 {
-    const uint32_t lo = __byte_perm(kLut0, kLut1, sel & 0x7777u);   // codes for n & 7, n < 8
-    const uint32_t hi = __byte_perm(kLut2, kLut3, sel & 0x7777u);   // codes for n & 7, n >= 8
-    const uint32_t pick = 0x3210u | (((sel >> 3) & 0x1111u) << 2);  // byte i from hi when n_i >= 8
-    return __byte_perm(lo, hi, pick);
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Offset of 16-byte chunk j of row r in a 128-byte-swizzled K-major tile.
-__device__ __forceinline__ uint32_t sw128_offset(int r, int j) { return r * 128 + ((j ^ (r & 7)) << 4); }
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-// E4M3 codes of 0..15 (the low part of an activation): 0..7 as above, then
-// 8..15 = (1 + m/8) 2^3 = 0x50..0x57.
-constexpr uint32_t kLoLut2 = 0x53525150u;   // 8..11
-constexpr uint32_t kLoLut3 = 0x57565554u;   // 12..15
-
-__device__ __forceinline__ uint32_t uint4x4_to_e4m3(uint32_t sel)
-{
-    const uint32_t lo = __byte_perm(kLut0, kLut1, sel & 0x7777u);
-    const uint32_t hi = __byte_perm(kLoLut2, kLoLut3, sel & 0x7777u);
-    const uint32_t pick = 0x3210u | (((sel >> 3) & 0x1111u) << 2);
-    return __byte_perm(lo, hi, pick);
-}
-
-// D[tmem] (+)= A[smem] . B[smem]^T, E4M3 operands, one CTA (kind::f8f6f4,
-// K = 32 per instruction).
-__device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                         uint32_t accumulate)
+// D[tmem] (+)= A[tmem] . B[smem]^T, E4M3 operands, one CTA (kind::f8f6f4,
+// K = 32 per instruction: 8 TMEM columns of A per row).
+__device__ __forceinline__ void mma_e4m3_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate)
 {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
-// A' (2 mp rows x K, E4M3): row m < M holds the codes of hi = a >> 4, row
-// mp + m those of lo = a & 15, for a = A[m, k]; padding rows are zero.  One
-// thread per 4 consecutive k.
-__global__ void split_activations_kernel(const int8_t *__restrict__ A, int M, int K, int mp, uint8_t *__restrict__ Ap)
+// registers -> TMEM: 32 lanes x 32 consecutive columns (thread i writes lane
+// base + i), then wait until the stores are done.
+__device__ __forceinline__ void tmem_st32_wait(uint32_t taddr, const uint32_t (&r)[32])
 {
-    const int64_t words_per_row = K / 4;
-    const int64_t total = 2 * static_cast<int64_t>(mp) * words_per_row;
-    for (int64_t w = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; w < total;
-         w += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int rr = static_cast<int>(w / words_per_row);
-        const int64_t k0 = (w % words_per_row) * 4;
-        const bool lo_part = rr >= mp;
-        const int m = lo_part ? rr - mp : rr;
-        uint32_t out = 0;
-        if (m < M) {
-            uint32_t sel = 0;
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};\n\t"
+        "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+// Position of k (mod 8) inside its group of 8 in the MMA's k order: the even
+// k first, then the odd k (the order the converters emit).
+__host__ __device__ constexpr int k_slot(int j) { return (j >> 1) + 4 * (j & 1); }
+
+// A' (2 mp rows x K, E4M3) and R: one block per activation row m < mp.
+// Row m holds the codes of hi = (a + 8) >> 4, row mp + m those of
+// lo = a - 16 hi, for a = A[m, k], each group of 8 k in k_slot order; rows
+// m >= M are zero.  R[m] = sum_k A[m, k].
+constexpr int kSplitThreads = 256;
+
+__global__ void __launch_bounds__(kSplitThreads)
+    split_activations_kernel(const int8_t *__restrict__ A, int M, int K, int mp, uint8_t *__restrict__ Ap,
+                             int32_t *__restrict__ R)
+{
+    griddep_launch_dependents();
+    __shared__ int warp_sums[kSplitThreads / 32];
+    const int m = blockIdx.x;
+    const int groups = K / 8;
+    uint8_t *hi_row = Ap + static_cast<int64_t>(m) * K;
+    uint8_t *lo_row = Ap + static_cast<int64_t>(mp + m) * K;
+    int sum = 0;
+    for (int g = threadIdx.x; g < groups; g += kSplitThreads) {
+        uint8_t hc[8], lc[8];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int a = A[static_cast<int64_t>(m) * K + k0 + i];
-                const uint32_t nib = lo_part ? static_cast<uint32_t>(a & 15) : static_cast<uint32_t>((a >> 4) & 15);
-                sel |= nib << (4 * i);
-            }
-            out = lo_part ? uint4x4_to_e4m3(sel) : int4x4_to_e4m3(sel);
+        for (int j = 0; j < 8; ++j) {
+            const int a = m < M ? static_cast<int>(A[static_cast<int64_t>(m) * K + 8 * g + j]) : 0;
+            const int hi = (a + 8) >> 4;
+            const int lo = a - 16 * hi;
+            sum += a;
+            hc[k_slot(j)] = __nv_cvt_float_to_fp8(static_cast<float>(hi), __NV_SATFINITE, __NV_E4M3);
+            lc[k_slot(j)] = __nv_cvt_float_to_fp8(static_cast<float>(lo), __NV_SATFINITE, __NV_E4M3);
         }
-        *reinterpret_cast<uint32_t *>(Ap + static_cast<int64_t>(rr) * K + k0) = out;
+        uint2 hw, lw;
+        std::memcpy(&hw, hc, 8);
+        std::memcpy(&lw, lc, 8);
+        *reinterpret_cast<uint2 *>(hi_row + 8 * g) = hw;
+        *reinterpret_cast<uint2 *>(lo_row + 8 * g) = lw;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
+    if (threadIdx.x % 32 == 0)
+        warp_sums[threadIdx.x / 32] = sum;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int total = 0;
+        for (int w = 0; w < kSplitThreads / 32; ++w)
+            total += warp_sums[w];
+        R[m] = total;
     }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
     w4a8_skinny_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmA,
-                       int32_t *__restrict__ D, int64_t ldd, int M, int N, int K, int mp, int stages,
-                       int32_t *__restrict__ partials, uint32_t *__restrict__ counters, ErrCtx err)
+                       int32_t *__restrict__ D, int64_t ldd, const int32_t *__restrict__ R, int M, int N, int K,
+                       int mp, int stages, int32_t *__restrict__ partials, uint32_t *__restrict__ counters,
+                       ErrCtx err)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     const int sbytes = stage_bytes(mp);
-    uint8_t *conv = smem + stages * sbytes;                   // kConvBufs x 16 KB
-    uint64_t *full = reinterpret_cast<uint64_t *>(conv + conv_region());
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + stages * sbytes);
     uint64_t *empty = full + kMaxStages;
-    uint64_t *cready = empty + kMaxStages;                     // converted tile ready (converter warps)
-    uint64_t *cfree = cready + kConvBufs;                      // converted tile consumed (MMA commit)
-    uint64_t *tfull = cfree + kConvBufs;
+    uint64_t *cready = empty + kMaxStages;                     // converted weights in TMEM (converters)
+    uint64_t *cfree = cready + kWBufs;                         // converted weights consumed (MMA commit)
+    uint64_t *tfull = cfree + kWBufs;
     uint64_t *tempty = tfull + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
@@ -165,17 +195,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int G = gridDim.x, c = blockIdx.x;
     const int tiles = (N + kTileN - 1) / kTileN;
-    const int KB = K / kBK;                                    // K is a multiple of kBK
+    const int KB = (K + kBK - 1) / kBK;                        // a ragged last K block reads zeros
     const int64_t U = static_cast<int64_t>(tiles) * KB;
     const int64_t u_begin = unit_start(c, U, G), u_end = unit_start(c + 1, U, G);
-    const uint32_t a_bytes = static_cast<uint32_t>(2 * mp * kBK);
+    const int abox = a_box_bytes(mp);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], kConvWarps + 1);              // every converter warp + the MMA commit
         }
-        for (int b = 0; b < kConvBufs; ++b) {
+        for (int b = 0; b < kWBufs; ++b) {
             mbar_init(&cready[b], kConvWarps);
             mbar_init(&cfree[b], 1);
         }
@@ -202,50 +232,54 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         if (lane == 0) {
             // ---------------------------------------------- TMA producer
+            // The weights do not depend on the pre-pass: the first ring's
+            // worth is requested before waiting for A'.
             const uint64_t keep_a = policy_evict_last();    // A' is re-read by every CTA
             const uint64_t stream_b = policy_evict_first();  // the weights are read once
-            int stage = 0;
-            uint32_t phase = 0;
-            int64_t issued = 0;
-            bool ok = true;
-            for (int64_t u = u_begin; u < u_end && ok;) {
-                const int tile = static_cast<int>(u / KB);
-                const int kb0 = static_cast<int>(u % KB);
-                const int kb1 = seg_end(kb0, KB, u_end - u);
-                for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1u, err, abort_flag, kSiteProducerEmpty)) {
-                        ok = false;
-                        break;
-                    }
-                    uint8_t *st = smem + stage * sbytes;
-                    mbar_arrive_expect_tx(&full[stage], kPackedBytes + a_bytes);
-                    tma_load_2d_hint(st, &tmB, &full[stage], kb * (kBK / 2), tile * kTileN, stream_b);
-                    tma_load_2d_hint(st + kPackedBytes, &tmA, &full[stage], kb * kBK, 0, keep_a);
-                    ++issued;
-                    if (++stage == stages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-                u += kb1 - kb0;
+            const uint32_t tx = static_cast<uint32_t>(kPackedBytes + 2 * abox);
+            const int64_t n = u_end - u_begin;
+            const int64_t pre = n < stages ? n : stages;
+            for (int64_t i = 0; i < pre; ++i) {
+                const int64_t u = u_begin + i;
+                uint8_t *st = smem + i * sbytes;
+                mbar_arrive_expect_tx(&full[i], tx);
+                tma_load_2d_hint(st, &tmB, &full[i], static_cast<int>(u % KB) * (kBK / 2),
+                                 static_cast<int>(u / KB) * kTileN, stream_b);
             }
-            for (int i = 0; i < stages && i < issued; ++i) {
-                int s = stage - 1 - i;
-                uint32_t ph = phase;
-                if (s < 0) {
-                    s += stages;
-                    ph ^= 1u;
-                }
-                mbar_wait(&full[s], ph, err, nullptr, kSiteDrain);
+            griddep_wait();
+            for (int64_t i = 0; i < pre; ++i) {
+                const int kb = static_cast<int>((u_begin + i) % KB);
+                uint8_t *st = smem + i * sbytes + kPackedBytes;
+                tma_load_2d_hint(st, &tmA, &full[i], kb * kBK, 0, keep_a);
+                tma_load_2d_hint(st + abox, &tmA, &full[i], kb * kBK + kABoxK, 0, keep_a);
             }
+            int64_t issued = pre;
+            for (int64_t i = pre; i < n; ++i) {
+                const int stage = static_cast<int>(i % stages);
+                const uint32_t phase = static_cast<uint32_t>((i / stages) & 1);
+                if (!mbar_wait(&empty[stage], phase ^ 1u, err, abort_flag, kSiteProducerEmpty))
+                    break;
+                ++issued;
+                const int64_t u = u_begin + i;
+                const int kb = static_cast<int>(u % KB);
+                uint8_t *st = smem + stage * sbytes;
+                mbar_arrive_expect_tx(&full[stage], tx);
+                tma_load_2d_hint(st, &tmB, &full[stage], kb * (kBK / 2), static_cast<int>(u / KB) * kTileN,
+                                 stream_b);
+                tma_load_2d_hint(st + kPackedBytes, &tmA, &full[stage], kb * kBK, 0, keep_a);
+                tma_load_2d_hint(st + kPackedBytes + abox, &tmA, &full[stage], kb * kBK + kABoxK, 0, keep_a);
+            }
+            // before leaving, let every load this thread requested land
+            for (int64_t i = issued - 1; i >= 0 && i >= issued - stages; --i)
+                mbar_wait(&full[i % stages], static_cast<uint32_t>((i / stages) & 1), err, nullptr, kSiteDrain);
         }
     } else if (warp == 1) {
         if (lane == 0) {
             // ------------------------------------------------ MMA issuer
-            // MMA A = converted weights (128 rows), MMA B = A' (2 mp rows)
+            // MMA A = converted weights (TMEM, 128 rows), MMA B = A' (2 mp rows)
             const uint32_t idesc = idesc_e4m3_f32(kTileN, 2 * mp);
-            int stage = 0, cb = 0, seg = 0;
-            uint32_t phase = 0, cphase = 0;
+            int stage = 0, wb = 0, seg = 0;
+            uint32_t phase = 0, wphase = 0;
             bool ok = true;
             for (int64_t u = u_begin; u < u_end && ok; ++seg) {
                 const int kb0 = static_cast<int>(u % KB);
@@ -254,30 +288,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!mbar_wait(&tempty[acc], ((seg >> 1) & 1) ^ 1u, err, abort_flag, kSiteMmaTmemEmpty))
                     break;
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + acc * (kTmemCols / 2);
+                const uint32_t d_tmem = tmem_base + acc * kAccCols;
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(&full[stage], phase, err, abort_flag, kSiteMmaFull) ||
-                        !mbar_wait(&cready[cb], cphase, err, abort_flag, kSiteMmaFull)) {
+                        !mbar_wait(&cready[wb], wphase, err, abort_flag, kSiteMmaFull)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t wdesc = sdesc_kmajor_sw128(smem_u32(conv + cb * kConvBytes));
-                    const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(smem + stage * sbytes + kPackedBytes));
+                    const uint32_t a_src = tmem_base + kWCol0 + wb * kWCols;
+                    const uint64_t bdesc0 = sdesc_kmajor_sw128(smem_u32(smem + stage * sbytes + kPackedBytes));
+                    const uint64_t bdesc1 = sdesc_kmajor_sw128(smem_u32(smem + stage * sbytes + kPackedBytes + abox));
 #pragma unroll
                     for (int k = 0; k < kBK / 32; ++k) {
-                        const uint64_t koff = static_cast<uint64_t>((k * 32) >> 4);   // 32 bytes per MMA
-                        mma_e4m3(d_tmem, wdesc + koff, adesc + koff, idesc, (kb != kb0) || (k != 0));
+                        const uint64_t bdesc = (k < 4 ? bdesc0 : bdesc1) + static_cast<uint64_t>(((k & 3) * 32) >> 4);
+                        mma_e4m3_ts(d_tmem, a_src + 8 * k, bdesc, idesc, (kb != kb0) || (k != 0));
                     }
                     mma_commit(&empty[stage]);
-                    mma_commit(&cfree[cb]);
+                    mma_commit(&cfree[wb]);
                     if (++stage == stages) {
                         stage = 0;
                         phase ^= 1u;
                     }
-                    if (++cb == kConvBufs) {
-                        cb = 0;
-                        cphase ^= 1u;
+                    if (++wb == kWBufs) {
+                        wb = 0;
+                        wphase ^= 1u;
                     }
                 }
                 if (!ok)
@@ -286,57 +321,63 @@ __global__ void __launch_bounds__(kThreads, 1)
                 u += kb1 - kb0;
             }
         }
-    } else if (warp >= 6) {
+    } else if (warp >= kFirstConvWarp) {
         // ------------------------------------------------- converters
-        // Each K block: 128 rows x 64 bytes of nibbles -> 128 rows x 128
-        // E4M3 bytes in the swizzled layout; a thread converts 16-byte
-        // pieces (32 nibbles -> two 16-byte chunks of codes).
-        const int ct = threadIdx.x - 6 * 32;
-        int stage = 0, cb = 0;
-        uint32_t phase = 0, cphase = 0;
-        bool ok = true;
-        for (int64_t u = u_begin; u < u_end && ok;) {
-            const int kb0 = static_cast<int>(u % KB);
-            const int kb1 = seg_end(kb0, KB, u_end - u);
-            for (int kb = kb0; kb < kb1; ++kb) {
-                if (!mbar_wait(&full[stage], phase, err, abort_flag, kSiteMmaFull) ||
-                    !mbar_wait(&cfree[cb], cphase ^ 1u, err, abort_flag, kSiteProducerEmpty)) {
-                    ok = false;
-                    break;
-                }
-                const uint8_t *src = smem + stage * sbytes;
-                uint8_t *dst = conv + cb * kConvBytes;
-                for (int it = ct; it < kTileN * 4; it += kConvWarps * 32) {
-                    const int r = it >> 2, p = it & 3;           // row, 32-k piece
-                    const uint4 w = *reinterpret_cast<const uint4 *>(src + r * 64 + p * 16);
-                    const uint4 c0 = make_uint4(int4x4_to_e4m3(w.x & 0xFFFFu), int4x4_to_e4m3(w.x >> 16),
-                                                int4x4_to_e4m3(w.y & 0xFFFFu), int4x4_to_e4m3(w.y >> 16));
-                    const uint4 c1 = make_uint4(int4x4_to_e4m3(w.z & 0xFFFFu), int4x4_to_e4m3(w.z >> 16),
-                                                int4x4_to_e4m3(w.w & 0xFFFFu), int4x4_to_e4m3(w.w >> 16));
-                    *reinterpret_cast<uint4 *>(dst + sw128_offset(r, 2 * p)) = c0;
-                    *reinterpret_cast<uint4 *>(dst + sw128_offset(r, 2 * p + 1)) = c1;
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&cready[cb]);
-                if (++stage == stages) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
-                if (++cb == kConvBufs) {
-                    cb = 0;
-                    cphase ^= 1u;
+        // Thread = weight row r of the tile = TMEM lane r.  Per K block it
+        // reads 4 of its row's 8 swizzled 16-byte chunks (the half `half`
+        // of the block's k), releases the staging slot, spreads the
+        // nibbles to offset-binary E4M3 bytes and stores 32 TMEM columns.
+        const int q = warp & 3;
+        const int half = (warp - kFirstConvWarp) >> 2;
+        const int r = q * 32 + lane;
+        const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + kWCol0 + 32 * half;
+        int stage = 0, wb = 0;
+        uint32_t phase = 0, wphase = 0;
+        for (int64_t u = u_begin; u < u_end; ++u) {
+            if (!mbar_wait(&full[stage], phase, err, abort_flag, kSiteMmaFull) ||
+                !mbar_wait(&cfree[wb], wphase ^ 1u, err, abort_flag, kSiteProducerEmpty))
+                break;
+            tc_fence_after();
+            const uint8_t *src = smem + stage * sbytes + r * 128;
+            uint4 w[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                w[i] = *reinterpret_cast<const uint4 *>(src + (((4 * half + i) ^ (r & 7)) << 4));
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&empty[stage]);
+            uint32_t out[32];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t words[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t y = words[j] ^ 0x88888888u;   // offset binary: v + 8
+                    out[8 * i + 2 * j] = y & 0x0F0F0F0Fu;       // even k
+                    out[8 * i + 2 * j + 1] = (y >> 4) & 0x0F0F0F0Fu;   // odd k
                 }
             }
-            u += kb1 - kb0;
+            tmem_st32_wait(t_row + wb * kWCols, out);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&cready[wb]);
+            if (++stage == stages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+            if (++wb == kWBufs) {
+                wb = 0;
+                wphase ^= 1u;
+            }
         }
     } else {
         // -------------------------------------------------- epilogue
         // thread owns weight row n_local = 32 q + lane; TMEM columns m and
-        // mp + m hold the hi and lo sums of activation row m
+        // mp + m hold the hi and lo sums of activation row m (scaled 2^-9)
         const int q = warp & 3;
         const int n_local = q * 32 + lane;
+        griddep_wait();                                        // R comes from the pre-pass
         int seg = 0;
         for (int64_t u = u_begin; u < u_end; ++seg) {
             const int tile = static_cast<int>(u / KB);
@@ -347,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(&tfull[acc], (seg >> 1) & 1, err, abort_flag, kSiteEpiTmemFull))
                 break;
             tc_fence_after();
-            const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * (kTmemCols / 2);
+            const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccCols;
             int32_t v[kMaxMP];
 #pragma unroll
             for (int ch = 0; ch < kMaxMP / 16; ++ch) {
@@ -357,7 +398,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld16(tb + mp + ch * 16, l);
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
-                        v[ch * 16 + j] = 16 * __float2int_rn(__uint_as_float(h[j])) + __float2int_rn(__uint_as_float(l[j]));
+                        v[ch * 16 + j] = 16 * __float2int_rn(__uint_as_float(h[j]) * 512.0f) +
+                                         __float2int_rn(__uint_as_float(l[j]) * 512.0f);
                 } else {
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
@@ -375,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int m = 0; m < kMaxMP; ++m)
                         if (m < M)
-                            D[static_cast<int64_t>(m) * ldd + n] = v[m];
+                            D[static_cast<int64_t>(m) * ldd + n] = v[m] - 8 * R[m];
                 }
                 continue;
             }
@@ -417,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int m = 0; m < kMaxMP; ++m)
                         if (m < M)
-                            D[static_cast<int64_t>(m) * ldd + n] = sum[m];
+                            D[static_cast<int64_t>(m) * ldd + n] = sum[m] - 8 * R[m];
                 }
                 __syncwarp();
                 if (lane == 0)
@@ -439,20 +481,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 int w4a8_skinny_grid(int64_t N, int64_t K, int num_sms)
 {
-    const int64_t units = ((N + kTileN - 1) / kTileN) * (K / kBK);
+    const int64_t units = ((N + kTileN - 1) / kTileN) * ((K + kBK - 1) / kBK);
     return static_cast<int>(units < num_sms ? units : num_sms);
 }
 
 cudaError_t launch_w4a8_skinny(const W4a8SkinnyArgs &a, const ErrCtx &err, cudaStream_t s)
 {
-    // the activation split (one small launch), then the GEMM
-    const int64_t words = 2 * static_cast<int64_t>(a.mp) * (a.K / 4);
-    int64_t blocks = (words + 255) / 256;
-    if (blocks > 1024)
-        blocks = 1024;
+    // the activation split (one block per A' row pair), then the GEMM as a
+    // programmatic dependent launch: its set-up and first weight loads
+    // overlap the split
     note_launch();
-    split_activations_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(static_cast<const int8_t *>(a.A), a.M, a.K,
-                                                                           a.mp, a.Ap);
+    split_activations_kernel<<<static_cast<unsigned>(a.mp), kSplitThreads, 0, s>>>(
+        static_cast<const int8_t *>(a.A), a.M, a.K, a.mp, a.Ap, a.R);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return e;
@@ -460,10 +500,20 @@ cudaError_t launch_w4a8_skinny(const W4a8SkinnyArgs &a, const ErrCtx &err, cudaS
     const int smem = smem_for(a.mp);
     if ((e = ensure_smem_attr(reinterpret_cast<const void *>(w4a8_skinny_kernel), smem)) != cudaSuccess)
         return e;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3(static_cast<unsigned>(a.grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     note_launch();
-    w4a8_skinny_kernel<<<a.grid, kThreads, smem, s>>>(a.tmB, a.tmA, a.D, a.ldd, a.M, a.N, a.K, a.mp, stages,
-                                                      a.partials, a.counters, err);
-    return cudaGetLastError();
+    return cudaLaunchKernelEx(&cfg, w4a8_skinny_kernel, a.tmB, a.tmA, a.D, a.ldd, static_cast<const int32_t *>(a.R),
+                              a.M, a.N, a.K, a.mp, stages, a.partials, a.counters, err);
 }
 
 }  // namespace tmg
