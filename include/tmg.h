@@ -44,6 +44,7 @@
 #ifndef TMG_H
 #define TMG_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -192,13 +193,48 @@ tmg_status tmg_gemm_fused(const void *A, const void *B, void *D, int64_t M,
  * packed int4 B unpacked in the kernel) and §6 (i8 / i4 atoms accumulating
  * in i32).  K must be even (else INVALID_ARG); K == 0 writes zeros; results
  * wrap like int32 arithmetic only if |D| >= 2^31 (K > 2^21 with extreme
- * values).  GB300 has no integer tensor-core MMA: both operands are unpacked
- * to bf16 (exact) into per-(device, stream) workspace ((M + N) x K bf16),
- * multiplied on the bf16 tensor cores in K segments of at most 4096 — where
- * every fp32 partial sum is an integer below 2^22, hence exact — and each
- * segment is added into D as int32. */
+ * values).  GB300 has no integer tensor-core MMA, so exact integer sums are
+ * formed on floating-point tensor cores:
+ *   decode shapes (M <= 64, K a multiple of 32, K <= 32768): the weights
+ *     stay 4-bit until the kernel, which turns them into offset-binary E4M3
+ *     codes (u = b + 8; code u is exactly u * 2^-9) in tensor memory, splits
+ *     a = 16 hi + lo (both exact in E4M3) and multiplies on the fp8 tensor
+ *     cores; every fp32 column sum is an integer multiple of 2^-9 below 2^22
+ *     in magnitude, and the epilogue subtracts 8 * sum_k a(m,k); CTAs that
+ *     share an output tile add their int32 shares into D.  Workspace:
+ *     2 * round_up(M, 16) * K + 4 * round_up(M, 16) bytes per (device,
+ *     stream);
+ *   otherwise: both operands are unpacked to bf16 (exact) into workspace
+ *     ((M + N) x K bf16), multiplied on the bf16 tensor cores in K segments
+ *     of at most 4096 — where every fp32 partial sum is an integer below
+ *     2^22, hence exact — and each segment is added into D as int32. */
 tmg_status tmg_gemm_w4a8(const void *A, const void *B, void *D, int64_t M,
                          int64_t N, int64_t K, void *stream);
+
+/* Pre-shuffled W4A8 weights ("FlyDSL Kernel Authoring Skill", §6 GEMM
+ * Pattern (Preshuffle): B is rearranged once, offline, so that each tile the
+ * kernel reads is contiguous).  The image is a sequence of 16 KB blocks, one
+ * per (t, kb) = (128 weight rows, 256 k), block t * ceil(K / 256) + kb; in a
+ * block, row r (weight row 128 t + r) takes bytes r * 128 .. r * 128 + 127,
+ * and its 16-byte chunk c (k = 256 kb + 32 c .. + 31, packed as in B) sits
+ * at chunk slot c XOR (r mod 8).  Rows past N and k past K are zero.
+ *
+ * tmg_w4a8_preshuffled_bytes: size of the image, 0 unless N > 0, K > 0 and
+ *   K is a multiple of 32.  Host only.
+ * tmg_w4a8_preshuffle: B (N, K/2) device, row-major packed int4 -> Bs
+ *   (device, tmg_w4a8_preshuffled_bytes(N, K) bytes, caller-owned).  Both
+ *   16-byte aligned (else INVALID_ARG); K a multiple of 32 (else
+ *   INVALID_ARG); N == 0 or K == 0 does nothing.  Asynchronous on `stream`.
+ * tmg_gemm_w4a8_preshuffled: tmg_gemm_w4a8 with the pre-shuffled image Bs
+ *   in place of B, same results; K a multiple of 32 and Bs 16-byte aligned
+ *   (else INVALID_ARG).  The decode kernel then reads each CTA's share of the
+ *   weights as one contiguous stream. */
+size_t tmg_w4a8_preshuffled_bytes(int64_t N, int64_t K);
+tmg_status tmg_w4a8_preshuffle(const void *B, void *Bs, int64_t N, int64_t K,
+                               void *stream);
+tmg_status tmg_gemm_w4a8_preshuffled(const void *A, const void *Bs, void *D,
+                                     int64_t M, int64_t N, int64_t K,
+                                     void *stream);
 
 /* MXFP4 GEMM: D[m,n] = sum_k a(m,k) * b(n,k) with
  *   a(m,k) = e2m1(code of A at (m,k)) * 2^(scaleA[m, k/32] - 127), same for b.

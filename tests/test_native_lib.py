@@ -122,3 +122,28 @@ def test_w4a8_rejects_bad_arguments_before_device_work(native):
     assert lib.tmg_gemm_w4a8(16, 16, 16, -1, 4, 8, None) == native.ERR_INVALID_ARG
     assert lib.tmg_gemm_w4a8(16, 16, 16, 0, 4, 8, None) == native.OK
     assert lib.tmg_gemm_w4a8(None, None, 16, 4, 4, 8, None) == native.ERR_INVALID_ARG
+
+
+def test_w4a8_preshuffled_bytes_is_host_arithmetic(native):
+    """One 16 KB block per (128 weight rows, 256 k), ragged edges rounded up;
+    0 for shapes the pre-shuffled layout does not take."""
+    lib = native.lib()
+    assert lib.tmg_w4a8_preshuffled_bytes(28672, 8192) == 28672 * 8192 // 2
+    assert lib.tmg_w4a8_preshuffled_bytes(129, 288) == 2 * 2 * 16384
+    assert lib.tmg_w4a8_preshuffled_bytes(1, 32) == 16384
+    assert lib.tmg_w4a8_preshuffled_bytes(128, 48) == 0          # K not a multiple of 32
+    assert lib.tmg_w4a8_preshuffled_bytes(0, 256) == 0
+    assert lib.tmg_w4a8_preshuffled_bytes(128, 0) == 0
+
+
+def test_w4a8_preshuffle_rejects_bad_arguments_before_device_work(native):
+    lib = native.lib()
+    assert lib.tmg_w4a8_preshuffle(16, 16, 4, 48, None) == native.ERR_INVALID_ARG      # K % 32
+    assert "multiple of 32" in lib.tmg_last_error().decode()
+    assert lib.tmg_w4a8_preshuffle(16, 16, -1, 64, None) == native.ERR_INVALID_ARG
+    assert lib.tmg_w4a8_preshuffle(None, None, 0, 64, None) == native.OK               # empty
+    assert lib.tmg_w4a8_preshuffle(None, 16, 4, 64, None) == native.ERR_INVALID_ARG
+    assert lib.tmg_w4a8_preshuffle(8, 16, 4, 64, None) == native.ERR_INVALID_ARG        # misaligned
+    assert lib.tmg_gemm_w4a8_preshuffled(16, 16, 16, 4, 4, 48, None) == native.ERR_INVALID_ARG
+    assert lib.tmg_gemm_w4a8_preshuffled(16, 24, 16, 4, 4, 64, None) == native.ERR_INVALID_ARG
+    assert lib.tmg_gemm_w4a8_preshuffled(16, 16, 16, 0, 4, 64, None) == native.OK

@@ -116,3 +116,94 @@ def test_w4a8_decode_workload_sampled(tmg):
     ns = np.concatenate([rng.integers(0, w.N, 3998), [0, w.N - 1]])
     ref = oracle.gemm_w4a8_entries(A.numpy(), B.numpy(), w.K, ms, ns)
     assert np.array_equal(D.cpu().numpy()[ms, ns].astype(np.int64), ref)
+
+
+def _preshuffle_reference(B: np.ndarray, N: int, K: int) -> np.ndarray:
+    """The pre-shuffled image, restated from its definition: 16 KB blocks
+    (t, kb) of 128 rows x 256 k in order t * KB + kb; inside a block row r's
+    16-byte chunk c at r * 128 + 16 * (c ^ (r % 8)); zero padding."""
+    T, KB = -(-N // 128), -(-K // 256)
+    padded = np.zeros((T * 128, KB * 128), np.uint8)
+    padded[:N, :K // 2] = B
+    blocks = padded.reshape(T, 128, KB, 8, 16).transpose(0, 2, 1, 3, 4)   # (t, kb, r, c, byte)
+    out = np.zeros_like(blocks)
+    for r in range(128):
+        for c in range(8):
+            out[:, :, r, c ^ (r % 8)] = blocks[:, :, r, c]
+    return out.reshape(-1)
+
+
+@pytest.mark.parametrize("N,K", [(128, 256), (300, 1056), (1000, 32)])
+def test_w4a8_preshuffle_layout(tmg, N, K):
+    B = inputs.random_int4_packed(N, K, 731)
+    Bs = tmg.w4a8_preshuffle(B.to(DEV))
+    tmg.check()
+    assert Bs.numel() == tmg.w4a8_preshuffled_bytes(N, K)
+    assert np.array_equal(Bs.cpu().numpy(), _preshuffle_reference(B.numpy(), N, K))
+
+
+def _run_shuffled(tmg, A, B):
+    N = B.shape[0]
+    Bs = tmg.w4a8_preshuffle(B.to(DEV))
+    D = tmg.gemm_w4a8_preshuffled(A.to(DEV), Bs, N)
+    tmg.check()
+    return D.cpu().numpy().astype(np.int64)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1000, 128), (16, 1024, 4096), (17, 777, 1280), (64, 2048, 2048),
+                                   (5, 300, 1056), (200, 330, 544), (1, 40, 32)])
+def test_w4a8_preshuffled_exact(tmg, M, N, K):
+    """Pre-shuffled weights: decode shapes (the contiguous-stream kernel) and
+    a larger M (the general path unpacking from the image), bit-exact."""
+    A, B = inputs.random_int8(M, K, 741), inputs.random_int4_packed(N, K, 742)
+    assert np.array_equal(_run_shuffled(tmg, A, B), oracle.gemm_w4a8(A.numpy(), B.numpy(), M, N, K))
+
+
+def test_w4a8_preshuffled_extreme_values_at_max_k(tmg):
+    M, N, K = 16, 256, 32768
+    for a, byte, b in [(127, 0x77, 7), (8, 0x77, 7), (-128, 0x88, -8)]:
+        A = torch.full((M, K), a, dtype=torch.int8)
+        B = torch.full((N, K // 2), byte, dtype=torch.uint8)
+        assert (_run_shuffled(tmg, A, B) == a * b * K).all(), (a, b)
+
+
+def test_w4a8_preshuffled_decode_workload_sampled(tmg):
+    w = inputs.WORKLOADS["w4a8_16x28672x8192"]
+    A, B = inputs.make_inputs(w)
+    Bs = tmg.w4a8_preshuffle(B.to(DEV))
+    D = tmg.gemm_w4a8_preshuffled(A.to(DEV), Bs, w.N)
+    tmg.check()
+    rng = np.random.default_rng(13)
+    ms = rng.integers(0, w.M, 4000)
+    ns = np.concatenate([rng.integers(0, w.N, 3998), [0, w.N - 1]])
+    ref = oracle.gemm_w4a8_entries(A.numpy(), B.numpy(), w.K, ms, ns)
+    assert np.array_equal(D.cpu().numpy()[ms, ns].astype(np.int64), ref)
+
+
+def _biased_operands(M, N, K, a_lo, a_hi, b_lo, b_hi, seed):
+    """int8 A uniform in [a_lo, a_hi] and int4 B uniform in [b_lo, b_hi],
+    packed two per byte (even k low): inputs whose products all share a
+    sign and a size, so the kernels' fp32 column sums grow to millions while
+    keeping random low-order bits."""
+    g = torch.Generator().manual_seed(seed)
+    A = torch.randint(a_lo, a_hi + 1, (M, K), generator=g, dtype=torch.int32).to(torch.int8)
+    v = torch.randint(b_lo, b_hi + 1, (N, K), generator=g, dtype=torch.int32) & 15
+    B = (v[:, 0::2] | (v[:, 1::2] << 4)).to(torch.uint8)
+    return A, B
+
+
+@pytest.mark.parametrize("path", ["decode", "general"])
+def test_w4a8_large_sums_keep_low_bits(tmg, monkeypatch, path):
+    """Exactness where it is hardest: column sums near the kernels' bound
+    (about 2^21 to 2^22) with random low-order bits.  A tensor core that
+    dropped accumulator bits would fail here although the uniform-value
+    tests pass (their partial sums are multiples of large powers of two)."""
+    if path == "general":
+        monkeypatch.setenv("TMG_W4A8_PATH", "general")
+        M, N, K = 64, 256, 8192
+    else:
+        M, N, K = 16, 256, 32768
+    for a_lo, a_hi, b_lo, b_hi in [(120, 127, 6, 7), (-128, -100, -8, -6), (-128, 127, -8, 7)]:
+        A, B = _biased_operands(M, N, K, a_lo, a_hi, b_lo, b_hi, 751 + a_lo)
+        ref = oracle.gemm_w4a8(A.numpy(), B.numpy(), M, N, K)
+        assert np.array_equal(_run(tmg, A, B), ref), (path, a_lo, b_lo)

@@ -21,7 +21,8 @@ import torch
 from . import _native
 from ._native import (BF16, E4M3, EPILOGUES, F32, PATHS, Layout, TmgError, make_layout)  # noqa: F401
 
-__all__ = ["gemm", "gemm_host", "gemm_fused", "gemm_w4a8", "gemm_mxfp4", "check", "make_layout", "Layout", "TmgError",
+__all__ = ["gemm", "gemm_host", "gemm_fused", "gemm_w4a8", "gemm_w4a8_preshuffled", "w4a8_preshuffle",
+           "w4a8_preshuffled_bytes", "gemm_mxfp4", "check", "make_layout", "Layout", "TmgError",
            "set_wait_budget_ns", "debug_wait_timeout", "launch_count", "version",
            "shutdown", "PATHS"]
 
@@ -180,6 +181,46 @@ def gemm_w4a8(A: torch.Tensor, B: torch.Tensor, D: torch.Tensor | None = None, *
         raise ValueError("D must be a contiguous int32 tensor of shape (M, N)")
     _native.raise_on(_native.lib().tmg_gemm_w4a8(A.data_ptr(), B.data_ptr(), D.data_ptr(), M, N, K,
                                                   _stream_handle(stream)))
+    return D
+
+
+def w4a8_preshuffled_bytes(N: int, K: int) -> int:
+    """Size of the pre-shuffled image of (N, K/2) packed int4 weights; 0
+    unless N > 0, K > 0 and K is a multiple of 32."""
+    return int(_native.lib().tmg_w4a8_preshuffled_bytes(N, K))
+
+
+def w4a8_preshuffle(B: torch.Tensor, *, stream=None) -> torch.Tensor:
+    """Pre-shuffle packed int4 weights B (N, K/2) uint8 into the decode
+    kernel's tile order (16 KB blocks of 128 rows x 256 k, each contiguous);
+    returns the 1-D uint8 image for gemm_w4a8_preshuffled.  K % 32 == 0."""
+    if B.dtype != torch.uint8 or B.dim() != 2 or not B.is_contiguous() or not B.is_cuda:
+        raise ValueError("B must be a contiguous CUDA uint8 tensor of shape (N, K/2)")
+    N, K = B.shape[0], B.shape[1] * 2
+    nbytes = w4a8_preshuffled_bytes(N, K)
+    if nbytes == 0:
+        raise ValueError(f"pre-shuffled weights need N > 0 and K a positive multiple of 32 (N={N}, K={K})")
+    Bs = torch.empty(nbytes, dtype=torch.uint8, device=B.device)
+    _native.raise_on(_native.lib().tmg_w4a8_preshuffle(B.data_ptr(), Bs.data_ptr(), N, K, _stream_handle(stream)))
+    return Bs
+
+
+def gemm_w4a8_preshuffled(A: torch.Tensor, Bs: torch.Tensor, N: int, D: torch.Tensor | None = None, *,
+                          stream=None) -> torch.Tensor:
+    """gemm_w4a8 with the weights given as w4a8_preshuffle's image Bs of an
+    (N, K/2) matrix; same exact int32 result."""
+    if A.dtype != torch.int8 or A.dim() != 2 or not A.is_contiguous() or not A.is_cuda:
+        raise ValueError("A must be a contiguous CUDA int8 tensor of shape (M, K)")
+    M, K = A.shape
+    if Bs.dtype != torch.uint8 or not Bs.is_contiguous() or not Bs.is_cuda or \
+            Bs.numel() != w4a8_preshuffled_bytes(N, K):
+        raise ValueError("Bs must be the contiguous CUDA image w4a8_preshuffle made of (N, K/2) weights")
+    if D is None:
+        D = torch.empty((M, N), dtype=torch.int32, device=A.device)
+    if D.dtype != torch.int32 or tuple(D.shape) != (M, N) or not D.is_contiguous():
+        raise ValueError("D must be a contiguous int32 tensor of shape (M, N)")
+    _native.raise_on(_native.lib().tmg_gemm_w4a8_preshuffled(A.data_ptr(), Bs.data_ptr(), D.data_ptr(), M, N, K,
+                                                              _stream_handle(stream)))
     return D
 
 

@@ -20,7 +20,8 @@ PATHS = {"auto": 0, "ffma": 1, "tc": 2, "skinny": 3, "skinny_ffma": 4, "tc_singl
          "tc_pair": 6, "packed_tc": 7}
 
 # Every function include/tmg.h declares.
-EXPORTS = ("tmg_gemm", "tmg_gemm_ex", "tmg_gemm_host", "tmg_gemm_fused", "tmg_gemm_w4a8", "tmg_gemm_mxfp4", "tmg_gemm_skinny_noalloc", "tmg_check", "tmg_last_error",
+EXPORTS = ("tmg_gemm", "tmg_gemm_ex", "tmg_gemm_host", "tmg_gemm_fused", "tmg_gemm_w4a8",
+           "tmg_gemm_w4a8_preshuffled", "tmg_w4a8_preshuffle", "tmg_w4a8_preshuffled_bytes", "tmg_gemm_mxfp4", "tmg_gemm_skinny_noalloc", "tmg_check", "tmg_last_error",
            "tmg_set_wait_budget_ns", "tmg_debug_wait_timeout", "tmg_launch_count",
            "tmg_version", "tmg_shutdown")
 
@@ -84,6 +85,12 @@ def lib():
     L.tmg_gemm_fused.restype = ctypes.c_int
     L.tmg_gemm_w4a8.argtypes = [P, P, P, I64, I64, I64, P]
     L.tmg_gemm_w4a8.restype = ctypes.c_int
+    L.tmg_gemm_w4a8_preshuffled.argtypes = [P, P, P, I64, I64, I64, P]
+    L.tmg_gemm_w4a8_preshuffled.restype = ctypes.c_int
+    L.tmg_w4a8_preshuffle.argtypes = [P, P, I64, I64, P]
+    L.tmg_w4a8_preshuffle.restype = ctypes.c_int
+    L.tmg_w4a8_preshuffled_bytes.argtypes = [I64, I64]
+    L.tmg_w4a8_preshuffled_bytes.restype = ctypes.c_size_t
     L.tmg_gemm_mxfp4.argtypes = [P, P, P, P, P, I64, I64, I64, P]
     L.tmg_gemm_mxfp4.restype = ctypes.c_int
     L.tmg_gemm_skinny_noalloc.argtypes = [P, P, P, I64, I64, I64, I64, I64, I64, P]

@@ -936,7 +936,12 @@ tmg_status tmg_gemm_fused(const void *A, const void *B, void *D, int64_t M, int6
     return e == cudaSuccess ? TMG_OK : cuda_fail(e, "fused pair launch");
 }
 
-tmg_status tmg_gemm_w4a8(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, void *stream)
+namespace {
+
+// Both W4A8 entry points: B is the row-major packed int4 matrix, or (when
+// `shuffled`) its pre-shuffled image.
+tmg_status gemm_w4a8_impl(const void *A, const void *B, bool shuffled, void *D, int64_t M, int64_t N, int64_t K,
+                          void *stream)
 {
     t_last_error.clear();
     if (M < 0 || N < 0 || K < 0)
@@ -944,6 +949,10 @@ tmg_status tmg_gemm_w4a8(const void *A, const void *B, void *D, int64_t M, int64
                     (long long)K);
     if (K % 2)
         return fail(TMG_ERR_INVALID_ARG, "K=%lld is odd (B packs two int4 values per byte)", (long long)K);
+    if (shuffled && K % 32)
+        return fail(TMG_ERR_INVALID_ARG, "K=%lld is not a multiple of 32 (pre-shuffled weights)", (long long)K);
+    if (shuffled && reinterpret_cast<uintptr_t>(B) % 16)
+        return fail(TMG_ERR_INVALID_ARG, "pre-shuffled weights not 16-byte aligned");
     if (M == 0 || N == 0)
         return TMG_OK;
     if (!D || (K > 0 && (!A || !B)))
@@ -966,7 +975,7 @@ tmg_status tmg_gemm_w4a8(const void *A, const void *B, void *D, int64_t M, int64
         if (!strcmp(f, "general"))
             decode = false;
     }
-    if (decode && tma_ok(B, K / 2, 1, N, K / 2)) {
+    if (decode && (shuffled || tma_ok(B, K / 2, 1, N, K / 2))) {
         W4a8SkinnyArgs w;
         std::memset(&w, 0, sizeof w);
         w.mp = static_cast<int>((M + 15) / 16 * 16);
@@ -975,18 +984,13 @@ tmg_status tmg_gemm_w4a8(const void *A, const void *B, void *D, int64_t M, int64
         uint8_t *Ap = static_cast<uint8_t *>(pack_scratch(0, ap_bytes + 4 * static_cast<size_t>(w.mp), s, &st));
         if (!Ap)
             return st;
-        if ((st = encode_2d(&w.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, K / 2, N, K / 2, 128, 128)) != TMG_OK)
+        if (shuffled)
+            w.Bs = static_cast<const uint8_t *>(B);       // 1-D bulk copies; tmB stays unused
+        else if ((st = encode_2d(&w.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, K / 2, N, K / 2, 128, 128)) != TMG_OK)
             return st;
         if ((st = encode_2d(&w.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Ap, K, 2 * w.mp, K, 128, 2 * w.mp)) != TMG_OK)
             return st;
         w.grid = w4a8_skinny_grid(N, K, ds->num_sms);
-        int dev = 0;
-        cudaGetDevice(&dev);
-        Scratch *sc = skinny_scratch(dev, s, skinny_partials_bytes(w.grid, w.mp), skinny_counters_bytes(N), &st);
-        if (!sc)
-            return st;
-        w.partials = reinterpret_cast<int32_t *>(sc->partials);
-        w.counters = sc->counters;
         w.A = A;
         w.Ap = Ap;
         w.R = reinterpret_cast<int32_t *>(Ap + ap_bytes);
@@ -1005,7 +1009,7 @@ tmg_status tmg_gemm_w4a8(const void *A, const void *B, void *D, int64_t M, int64
     void *PB = pack_scratch(1, static_cast<size_t>(N) * ldp * 2, s, &st);
     if (!PB)
         return st;
-    if ((e = launch_unpack_w4a8(A, B, M, N, K, PA, PB, ldp, ds->num_sms, s)) != cudaSuccess)
+    if ((e = launch_unpack_w4a8(A, B, M, N, K, PA, PB, ldp, ds->num_sms, s, shuffled)) != cudaSuccess)
         return cuda_fail(e, "W4A8 unpack launch");
     // K segments of at most 4096: every partial sum of a segment is an integer
     // of magnitude <= 128 * 8 * 4096 = 2^22, exact in the fp32 accumulator;
@@ -1038,6 +1042,49 @@ tmg_status tmg_gemm_w4a8(const void *A, const void *B, void *D, int64_t M, int64
             return cuda_fail(e, "W4A8 GEMM launch");
     }
     return TMG_OK;
+}
+
+}  // namespace
+
+tmg_status tmg_gemm_w4a8(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, void *stream)
+{
+    return gemm_w4a8_impl(A, B, false, D, M, N, K, stream);
+}
+
+tmg_status tmg_gemm_w4a8_preshuffled(const void *A, const void *Bs, void *D, int64_t M, int64_t N, int64_t K,
+                                     void *stream)
+{
+    return gemm_w4a8_impl(A, Bs, true, D, M, N, K, stream);
+}
+
+size_t tmg_w4a8_preshuffled_bytes(int64_t N, int64_t K)
+{
+    if (N <= 0 || K <= 0 || K % 32)
+        return 0;
+    return w4a8_preshuffled_bytes(N, K);
+}
+
+tmg_status tmg_w4a8_preshuffle(const void *B, void *Bs, int64_t N, int64_t K, void *stream)
+{
+    t_last_error.clear();
+    if (N < 0 || K < 0)
+        return fail(TMG_ERR_INVALID_ARG, "negative extent N=%lld K=%lld", (long long)N, (long long)K);
+    if (K % 32)
+        return fail(TMG_ERR_INVALID_ARG, "K=%lld is not a multiple of 32 (pre-shuffled weights)", (long long)K);
+    if (N == 0 || K == 0)
+        return TMG_OK;
+    if (!B || !Bs)
+        return fail(TMG_ERR_INVALID_ARG, "null pointer");
+    if (reinterpret_cast<uintptr_t>(B) % 16 || reinterpret_cast<uintptr_t>(Bs) % 16)
+        return fail(TMG_ERR_INVALID_ARG, "B and Bs must be 16-byte aligned");
+    if (N > INT32_MAX || K > INT32_MAX)
+        return fail(TMG_ERR_UNSUPPORTED, "extents beyond 2^31");
+    DeviceState *ds = nullptr;
+    tmg_status st;
+    if ((st = device_state(&ds)) != TMG_OK)
+        return st;
+    const cudaError_t e = launch_w4a8_preshuffle(B, N, K, Bs, ds->num_sms, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TMG_OK : cuda_fail(e, "W4A8 pre-shuffle launch");
 }
 
 tmg_status tmg_gemm_mxfp4(const void *A, const void *B, const void *scaleA, const void *scaleB, void *D, int64_t M,

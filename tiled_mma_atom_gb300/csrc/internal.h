@@ -89,7 +89,7 @@ int tc2_fused_pick_bn(int64_t N);
 // W4A8 operands: A (M, K) int8 and B (N, K/2) packed int4 unpacked to bf16
 // (M, ldp) and (N, ldp), zero-padded past K; ldp a multiple of 8.
 cudaError_t launch_unpack_w4a8(const void *A, const void *B, int64_t M, int64_t N, int64_t K, void *PA, void *PB,
-                               int64_t ldp, int num_sms, cudaStream_t s);
+                               int64_t ldp, int num_sms, cudaStream_t s, bool b_preshuffled = false);
 // Decode-shaped W4A8 (w4a8_skinny.cu): M <= 64, K a multiple of 32 and at
 // most 32768.  tmB: packed weights (N, K/2) u8, box {128, 128}, 128-byte
 // swizzle; tmA: the split activations A' (2 mp, K) E4M3 (written by the
@@ -100,14 +100,30 @@ struct W4a8SkinnyArgs {
     const void *A;        // (M, K) int8
     uint8_t *Ap;          // scratch: 2 mp x K bytes
     int32_t *R;           // scratch: mp row sums of A
+    const uint8_t *Bs;    // pre-shuffled weights, or null: read B through tmB
     int32_t *D;           // (M, N) int32 row-major, row stride ldd
     int64_t ldd;
     int M, N, K, mp;
-    int32_t *partials;    // skinny_partials_bytes(grid, mp)
-    uint32_t *counters;   // skinny_counters_bytes(N), zero on entry
     int grid;
 };
 int w4a8_skinny_grid(int64_t N, int64_t K, int num_sms);
+
+// Pre-shuffled W4A8 weights: block (t, kb) of 128 rows x 256 k (16 KB) at
+// (t * KB + kb) * 16 KB, KB = ceil(K / 256); row r's 128 bytes at r * 128,
+// its 16-byte chunk c at chunk slot c XOR (r mod 8); K a multiple of 32.
+constexpr int kW4TileN = 128;
+constexpr int kW4BK = 256;
+size_t w4a8_preshuffled_bytes(int64_t N, int64_t K);
+cudaError_t launch_w4a8_preshuffle(const void *B, int64_t N, int64_t K, void *Bs, int num_sms, cudaStream_t s);
+
+// Offset in the pre-shuffled image of the 4 bytes holding k0 .. k0 + 7 of
+// weight row n (k0 a multiple of 8).
+__host__ __device__ inline int64_t w4a8_preshuffled_offset(int64_t n, int64_t k0, int64_t KB)
+{
+    const int64_t r = n % kW4TileN;
+    const int64_t byte = (k0 % kW4BK) / 2;
+    return (((n / kW4TileN) * KB + k0 / kW4BK) * kW4TileN + r) * 128 + 16 * ((byte / 16) ^ (r & 7)) + byte % 16;
+}
 cudaError_t launch_w4a8_skinny(const W4a8SkinnyArgs &a, const ErrCtx &err, cudaStream_t s);
 
 // D[m,n] = bf16(act(bias[n])) (or 0 without a bias): the fused GEMM at K = 0.

@@ -14,7 +14,8 @@
 //
 // unpack: P[r * ldp + k] = bf16(X(r, k)) for k < K, 0 for K <= k < ldp, with
 // X either int8 (X(r, k) = A[r * K + k]) or packed int4 (two's complement
-// nibbles, the even k in the low nibble of byte r * K/2 + k/2).  Each thread
+// nibbles, the even k in the low nibble of byte r * K/2 + k/2, or of the
+// pre-shuffled image's byte holding (r, k)).  Each thread
 // converts 8 consecutive k: 8 bytes of int8 or 4 bytes of int4 in, 16 bytes
 // of bf16 out.  HBM-bound.
 #include <cuda_bf16.h>
@@ -38,19 +39,28 @@ __device__ __forceinline__ int int4_at(uint32_t word, int j)   // nibble j (0..7
     return static_cast<int>(static_cast<int32_t>(word << (28 - 4 * j)) >> 28);
 }
 
-template <bool INT4>
+// SHUF: X is the pre-shuffled int4 image (K a multiple of 32, so a group
+// of 8 k is either whole or entirely past K).
+template <bool INT4, bool SHUF = false>
 __global__ void __launch_bounds__(kUnpackThreads)
     unpack_kernel(const uint8_t *__restrict__ X, int64_t rows, int64_t K, uint16_t *__restrict__ P, int64_t ldp,
                   int vec_ok)
 {
     const int64_t groups_per_row = ldp / 8;
     const int64_t total = rows * groups_per_row;
+    const int64_t KB = (K + kW4BK - 1) / kW4BK;
     for (int64_t g = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; g < total;
          g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t r = g / groups_per_row;
         const int64_t k0 = (g % groups_per_row) * 8;
         int v[8];
-        if (vec_ok && k0 + 8 <= K) {
+        if constexpr (SHUF) {
+            const uint32_t w =
+                k0 < K ? *reinterpret_cast<const uint32_t *>(X + w4a8_preshuffled_offset(r, k0, KB)) : 0u;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                v[j] = int4_at(w, j);
+        } else if (vec_ok && k0 + 8 <= K) {
             if constexpr (INT4) {
                 const uint32_t w = *reinterpret_cast<const uint32_t *>(X + r * (K / 2) + k0 / 2);
 #pragma unroll
@@ -93,7 +103,7 @@ unsigned grid_for(int64_t work, int num_sms)
 }  // namespace
 
 cudaError_t launch_unpack_w4a8(const void *A, const void *B, int64_t M, int64_t N, int64_t K, void *PA, void *PB,
-                               int64_t ldp, int num_sms, cudaStream_t s)
+                               int64_t ldp, int num_sms, cudaStream_t s, bool b_preshuffled)
 {
     const uintptr_t pa = reinterpret_cast<uintptr_t>(A), pb = reinterpret_cast<uintptr_t>(B);
     const int vec_a = (K % 8 == 0) && (pa % 8 == 0);
@@ -105,8 +115,12 @@ cudaError_t launch_unpack_w4a8(const void *A, const void *B, int64_t M, int64_t 
     if (e != cudaSuccess)
         return e;
     note_launch();
-    unpack_kernel<true><<<grid_for(N * (ldp / 8), num_sms), kUnpackThreads, 0, s>>>(
-        static_cast<const uint8_t *>(B), N, K, static_cast<uint16_t *>(PB), ldp, vec_b);
+    if (b_preshuffled)
+        unpack_kernel<true, true><<<grid_for(N * (ldp / 8), num_sms), kUnpackThreads, 0, s>>>(
+            static_cast<const uint8_t *>(B), N, K, static_cast<uint16_t *>(PB), ldp, 1);
+    else
+        unpack_kernel<true><<<grid_for(N * (ldp / 8), num_sms), kUnpackThreads, 0, s>>>(
+            static_cast<const uint8_t *>(B), N, K, static_cast<uint16_t *>(PB), ldp, vec_b);
     return cudaGetLastError();
 }
 

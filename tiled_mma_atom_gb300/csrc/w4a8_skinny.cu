@@ -25,8 +25,12 @@
 // weight rows, N = 2 mp over the A' rows).  Inside each group of 8 k the
 // converters emit the even k first, then the odd k; the pre-pass writes A'
 // in the same order, so the products pair up.
-// Work split, partial tiles and their fixed-order fix-up follow skinny.cu
-// (stream-K over (tile, K block) units, per-tile counters per lane quarter).
+// Work split as in skinny.cu: stream-K over (tile, K block) units.  The
+// results are exact integers, so the CTAs sharing a tile simply add their
+// int32 shares into D (red.add; integer addition is exact in any order, so
+// the result is deterministic): the pre-pass zeroes the columns of D of the
+// tiles that are shared, and the CTA holding a tile's first K block also
+// adds the row-sum correction.  No partial buffers, counters or fix-up.
 //
 // Warps: 0 TMA producer; 1 MMA issuer and TMEM owner; 2..5 epilogue (one
 // per TMEM lane quarter); 6..13 converters (two per lane quarter, each 32 of
@@ -59,6 +63,7 @@ constexpr int kMaxStages = 16;
 constexpr int kSmemBudget = 225 * 1024;
 
 static_assert(kWCol0 + kWBufs * kWCols <= kTmemCols, "TMEM columns");
+static_assert(kTileN == kW4TileN && kBK == kW4BK, "pre-shuffled block shape");
 
 // Staging slot: packed weights, then two A' boxes (2 mp rows x 128 bytes each).
 __host__ __device__ constexpr int a_box_bytes(int mp) { return 2 * mp * kABoxK; }
@@ -71,16 +76,9 @@ int stages_for(int mp)
 }
 int smem_for(int mp) { return stages_for(mp) * stage_bytes(mp) + bar_bytes() + 1024; }
 
-__device__ __forceinline__ int64_t unit_start(int c, int64_t U, int G) { return (static_cast<int64_t>(c) * U) / G; }
-
 __device__ __forceinline__ int seg_end(int kb0, int KB, int64_t left)
 {
     return left < static_cast<int64_t>(KB - kb0) ? kb0 + static_cast<int>(left) : KB;
-}
-
-__device__ __forceinline__ int unit_owner(int64_t u, int64_t U, int G)
-{
-    return static_cast<int>(((u + 1) * G - 1) / U);
 }
 
 // Programmatic dependent launch: the pre-pass lets the GEMM start early;
@@ -91,6 +89,18 @@ __device__ __forceinline__ void griddep_launch_dependents()
 }
 
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Contiguous bulk copy global -> shared with an L2 eviction-priority hint;
+// both addresses 16-byte aligned, `bytes` a multiple of 16.
+__device__ __forceinline__ void bulk_load_hint(void *smem_dst, const void *gsrc, uint32_t bytes, uint64_t *bar,
+                                               uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+            "r"(smem_u32(smem_dst)),
+        "l"(gsrc), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
 
 // D[tmem] (+)= A[tmem] . B[smem]^T, E4M3 operands, one CTA (kind::f8f6f4,
 // K = 32 per instruction: 8 TMEM columns of A per row).
@@ -125,17 +135,41 @@ __device__ __forceinline__ void tmem_st32_wait(uint32_t taddr, const uint32_t (&
 // k first, then the odd k (the order the converters emit).
 __host__ __device__ constexpr int k_slot(int j) { return (j >> 1) + 4 * (j & 1); }
 
-// A' (2 mp rows x K, E4M3) and R: one block per activation row m < mp.
+__device__ __forceinline__ int64_t unit_start(int c, int64_t U, int G) { return (static_cast<int64_t>(c) * U) / G; }
+
+// A' (2 mp rows x K, E4M3) and R: blocks m < mp, one per activation row.
 // Row m holds the codes of hi = (a + 8) >> 4, row mp + m those of
 // lo = a - 16 hi, for a = A[m, k], each group of 8 k in k_slot order; rows
 // m >= M are zero.  R[m] = sum_k A[m, k].
+// Blocks mp .. mp + kZeroBlocks - 1 zero D (rows < M) in the tiles that the
+// GEMM's G CTAs share, which take red.adds: a tile is shared exactly when a
+// CTA's first unit c U / G (1 <= c < G) falls inside it, not at its start.
 constexpr int kSplitThreads = 256;
+constexpr int kZeroBlocks = 16;
 
 __global__ void __launch_bounds__(kSplitThreads)
-    split_activations_kernel(const int8_t *__restrict__ A, int M, int K, int mp, uint8_t *__restrict__ Ap,
-                             int32_t *__restrict__ R)
+    split_activations_kernel(const int8_t *__restrict__ A, int M, int N, int K, int mp, uint8_t *__restrict__ Ap,
+                             int32_t *__restrict__ R, int32_t *__restrict__ D, int64_t ldd, int G)
 {
     griddep_launch_dependents();
+    if (blockIdx.x >= mp) {
+        const int KB = (K + kBK - 1) / kBK;
+        const int64_t U = static_cast<int64_t>((N + kTileN - 1) / kTileN) * KB;
+        const int warps = kZeroBlocks * kSplitThreads / 32;
+        const int wid = (blockIdx.x - mp) * (kSplitThreads / 32) + threadIdx.x / 32;
+        for (int cb = 1 + wid; cb < G; cb += warps) {
+            const int64_t b = unit_start(cb, U, G);
+            if (b % KB == 0)
+                continue;                                      // the boundary is a tile start
+            const int64_t t = b / KB;
+            for (int i = threadIdx.x % 32; i < M * kTileN; i += 32) {
+                const int64_t n = t * kTileN + i % kTileN;
+                if (n < N)
+                    D[static_cast<int64_t>(i / kTileN) * ldd + n] = 0;
+            }
+        }
+        return;
+    }
     __shared__ int warp_sums[kSplitThreads / 32];
     const int m = blockIdx.x;
     const int groups = K / 8;
@@ -175,9 +209,8 @@ __global__ void __launch_bounds__(kSplitThreads)
 
 __global__ void __launch_bounds__(kThreads, 1)
     w4a8_skinny_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmA,
-                       int32_t *__restrict__ D, int64_t ldd, const int32_t *__restrict__ R, int M, int N, int K,
-                       int mp, int stages, int32_t *__restrict__ partials, uint32_t *__restrict__ counters,
-                       ErrCtx err)
+                       const uint8_t *__restrict__ Bs, int32_t *__restrict__ D, int64_t ldd,
+                       const int32_t *__restrict__ R, int M, int N, int K, int mp, int stages, ErrCtx err)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -239,12 +272,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t tx = static_cast<uint32_t>(kPackedBytes + 2 * abox);
             const int64_t n = u_end - u_begin;
             const int64_t pre = n < stages ? n : stages;
+            // weights of unit u: the pre-shuffled block u (16 KB, contiguous),
+            // else a 128 x 128-byte box of the row-major B
+            auto load_weights = [&](uint8_t *st, uint64_t *bar, int64_t u) {
+                if (Bs)
+                    bulk_load_hint(st, Bs + u * kPackedBytes, kPackedBytes, bar, stream_b);
+                else
+                    tma_load_2d_hint(st, &tmB, bar, static_cast<int>(u % KB) * (kBK / 2),
+                                     static_cast<int>(u / KB) * kTileN, stream_b);
+            };
             for (int64_t i = 0; i < pre; ++i) {
-                const int64_t u = u_begin + i;
-                uint8_t *st = smem + i * sbytes;
                 mbar_arrive_expect_tx(&full[i], tx);
-                tma_load_2d_hint(st, &tmB, &full[i], static_cast<int>(u % KB) * (kBK / 2),
-                                 static_cast<int>(u / KB) * kTileN, stream_b);
+                load_weights(smem + i * sbytes, &full[i], u_begin + i);
             }
             griddep_wait();
             for (int64_t i = 0; i < pre; ++i) {
@@ -264,8 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int kb = static_cast<int>(u % KB);
                 uint8_t *st = smem + stage * sbytes;
                 mbar_arrive_expect_tx(&full[stage], tx);
-                tma_load_2d_hint(st, &tmB, &full[stage], kb * (kBK / 2), static_cast<int>(u / KB) * kTileN,
-                                 stream_b);
+                load_weights(st, &full[stage], u);
                 tma_load_2d_hint(st + kPackedBytes, &tmA, &full[stage], kb * kBK, 0, keep_a);
                 tma_load_2d_hint(st + kPackedBytes + abox, &tmA, &full[stage], kb * kBK + kABoxK, 0, keep_a);
             }
@@ -387,6 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int acc = seg & 1;
             if (!mbar_wait(&tfull[acc], (seg >> 1) & 1, err, abort_flag, kSiteEpiTmemFull))
                 break;
+            __syncwarp();
             tc_fence_after();
             const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccCols;
             int32_t v[kMaxMP];
@@ -412,59 +451,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(&tempty[acc]);
 
             const int n = tile * kTileN + n_local;
-            if (kb0 == 0 && kb1 == KB) {
-                if (n < N) {
-#pragma unroll
-                    for (int m = 0; m < kMaxMP; ++m)
-                        if (m < M)
-                            D[static_cast<int64_t>(m) * ldd + n] = v[m] - 8 * R[m];
-                }
-                continue;
-            }
-            // Partial tile: integer partial sums; the last CTA to arrive for
-            // (tile, quarter) adds them in CTA order and writes D.
-            const int slot = 2 * c + (seg == 0 ? 0 : 1);
-            int32_t *mine = partials + static_cast<int64_t>(slot) * mp * kTileN;
-#pragma unroll
-            for (int m = 0; m < kMaxMP; ++m)
-                if (m < mp)
-                    mine[m * kTileN + n_local] = v[m];
-            __threadfence();
-            __syncwarp();
-            const int64_t t_first = static_cast<int64_t>(tile) * KB;
-            const int c_first = unit_owner(t_first, U, G);
-            const int c_last = unit_owner(t_first + KB - 1, U, G);
-            uint32_t old = 0;
-            if (lane == 0)
-                old = atomicAdd(&counters[tile * 4 + q], 1u);
-            old = __shfl_sync(0xFFFFFFFFu, old, 0);
-            if (old == static_cast<uint32_t>(c_last - c_first)) {
-                __threadfence();
-                int32_t sum[kMaxMP];
+            int32_t *d = D + n;
+            if (n < N && kb0 == 0 && kb1 == KB) {
+                // the whole tile is this CTA's: plain stores
 #pragma unroll
                 for (int m = 0; m < kMaxMP; ++m)
-                    sum[m] = 0;
-                // every contribution, this CTA's included, is read back from
-                // scratch, so only one array of sums is live here
-                for (int cc = c_first; cc <= c_last; ++cc) {
-                    const int first_tile = static_cast<int>(unit_start(cc, U, G) / KB);
-                    const int s2 = 2 * cc + (first_tile == tile ? 0 : 1);
-                    const int32_t *p = partials + static_cast<int64_t>(s2) * mp * kTileN;
+                    if (m < M)
+                        d[static_cast<int64_t>(m) * ldd] = v[m] - 8 * R[m];
+            } else if (n < N) {
+                // a share of a tile: add into the zeroed D; the first K
+                // block's holder adds the correction too
+                const int corr = kb0 == 0 ? 8 : 0;
 #pragma unroll
-                    for (int m = 0; m < kMaxMP; ++m)
-                        if (m < mp)
-                            sum[m] += __ldcg(p + m * kTileN + n_local);
-                }
-                if (n < N) {
-#pragma unroll
-                    for (int m = 0; m < kMaxMP; ++m)
-                        if (m < M)
-                            D[static_cast<int64_t>(m) * ldd + n] = sum[m] - 8 * R[m];
-                }
-                __syncwarp();
-                if (lane == 0)
-                    counters[tile * 4 + q] = 0;
+                for (int m = 0; m < kMaxMP; ++m)
+                    if (m < M)
+                        atomicAdd(d + static_cast<int64_t>(m) * ldd, v[m] - corr * R[m]);
             }
+            __syncwarp();
         }
     }
 
@@ -477,7 +480,56 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// Pre-shuffled weights ("FlyDSL Kernel Authoring Skill", §6 GEMM Pattern
+// (Preshuffle): B rearranged once so that the kernel's tiles are
+// contiguous).  Block (t, kb) = 128 weight rows x 256 k, 16 KB, sits at
+// ((t * KB) + kb) * 16 KB: row r's 128 bytes at r * 128, its 16-byte chunk
+// c (k = kb * 256 + 32 c .. + 31, even k in the low nibble) at chunk slot
+// c XOR (r mod 8) — exactly the image the 128-byte swizzled tensor-map load
+// leaves in shared memory.  Rows past N and chunks past K are zero.  One
+// thread per 16-byte chunk; K a multiple of 32, so a chunk is either whole
+// or entirely past K.
+__global__ void __launch_bounds__(256)
+    w4a8_preshuffle_kernel(const uint8_t *__restrict__ B, int64_t N, int64_t K, uint8_t *__restrict__ Bs,
+                           int64_t chunks)
+{
+    const int64_t KB = (K + kBK - 1) / kBK;
+    const int64_t row_bytes = K / 2;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < chunks;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t blk = i / (kTileN * 8);
+        const int r = static_cast<int>((i / 8) % kTileN);
+        const int slot = static_cast<int>(i % 8);
+        const int64_t n = (blk / KB) * kTileN + r;
+        const int64_t byte0 = (blk % KB) * (kBK / 2) + 16 * (slot ^ (r & 7));
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (n < N && byte0 < row_bytes)
+            v = *reinterpret_cast<const uint4 *>(B + n * row_bytes + byte0);
+        *reinterpret_cast<uint4 *>(Bs + 16 * i) = v;
+    }
+}
+
 }  // namespace
+
+size_t w4a8_preshuffled_bytes(int64_t N, int64_t K)
+{
+    return static_cast<size_t>((N + kTileN - 1) / kTileN) * static_cast<size_t>((K + kBK - 1) / kBK) * kPackedBytes;
+}
+
+cudaError_t launch_w4a8_preshuffle(const void *B, int64_t N, int64_t K, void *Bs, int num_sms, cudaStream_t s)
+{
+    const int64_t chunks = static_cast<int64_t>(w4a8_preshuffled_bytes(N, K) / 16);
+    int64_t blocks = (chunks + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+    if (blocks > cap)
+        blocks = cap;
+    if (blocks < 1)
+        blocks = 1;
+    note_launch();
+    w4a8_preshuffle_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(static_cast<const uint8_t *>(B), N, K,
+                                                                        static_cast<uint8_t *>(Bs), chunks);
+    return cudaGetLastError();
+}
 
 int w4a8_skinny_grid(int64_t N, int64_t K, int num_sms)
 {
@@ -491,8 +543,8 @@ cudaError_t launch_w4a8_skinny(const W4a8SkinnyArgs &a, const ErrCtx &err, cudaS
     // programmatic dependent launch: its set-up and first weight loads
     // overlap the split
     note_launch();
-    split_activations_kernel<<<static_cast<unsigned>(a.mp), kSplitThreads, 0, s>>>(
-        static_cast<const int8_t *>(a.A), a.M, a.K, a.mp, a.Ap, a.R);
+    split_activations_kernel<<<static_cast<unsigned>(a.mp + kZeroBlocks), kSplitThreads, 0, s>>>(
+        static_cast<const int8_t *>(a.A), a.M, a.N, a.K, a.mp, a.Ap, a.R, a.D, a.ldd, a.grid);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return e;
@@ -512,8 +564,8 @@ cudaError_t launch_w4a8_skinny(const W4a8SkinnyArgs &a, const ErrCtx &err, cudaS
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     note_launch();
-    return cudaLaunchKernelEx(&cfg, w4a8_skinny_kernel, a.tmB, a.tmA, a.D, a.ldd, static_cast<const int32_t *>(a.R),
-                              a.M, a.N, a.K, a.mp, stages, a.partials, a.counters, err);
+    return cudaLaunchKernelEx(&cfg, w4a8_skinny_kernel, a.tmB, a.tmA, a.Bs, a.D, a.ldd,
+                              static_cast<const int32_t *>(a.R), a.M, a.N, a.K, a.mp, stages, err);
 }
 
 }  // namespace tmg
