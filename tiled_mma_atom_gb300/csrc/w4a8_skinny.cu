@@ -32,11 +32,13 @@
 // tiles that are shared, and the CTA holding a tile's first K block also
 // adds the row-sum correction.  No partial buffers, counters or fix-up.
 //
-// Warps: 0 TMA producer; 1 MMA issuer and TMEM owner; 2..5 epilogue (one
+// Warps: 0 weight producer; 1 MMA issuer and TMEM owner; 2..5 epilogue (one
 // per TMEM lane quarter); 6..13 converters (two per lane quarter, each 32 of
-// a K block's 64 weight columns).  Shared memory: a ring of staging slots
-// (packed weights, 128-byte swizzled rows, and two A' boxes).  TMEM: two
-// accumulators (columns 0-255) and four converted weight buffers (256-511).
+// a K block's 64 weight columns); 14 A' producer.  Shared memory: a ring of
+// packed-weight slots (128-byte swizzled rows), released once the
+// converters have read them, and a ring of A' slots (two boxes each),
+// released by the MMAs.  TMEM: two accumulators (columns 0-255) and four
+// converted weight buffers (256-511).
 #include <cuda_fp8.h>
 
 #include <cstring>
@@ -58,23 +60,35 @@ constexpr int kTmemCols = 512;
 constexpr int kMaxMP = 64;
 constexpr int kConvWarps = 8;
 constexpr int kFirstConvWarp = 6;
-constexpr int kThreads = 32 * (kFirstConvWarp + kConvWarps);   // 448
-constexpr int kMaxStages = 16;
+constexpr int kAProducerWarp = kFirstConvWarp + kConvWarps;       // 14
+constexpr int kThreads = 32 * (kAProducerWarp + 1);               // 480
+constexpr int kMaxWStages = 16;
+constexpr int kMaxAStages = 8;
 constexpr int kSmemBudget = 225 * 1024;
 
 static_assert(kWCol0 + kWBufs * kWCols <= kTmemCols, "TMEM columns");
 static_assert(kTileN == kW4TileN && kBK == kW4BK, "pre-shuffled block shape");
 
-// Staging slot: packed weights, then two A' boxes (2 mp rows x 128 bytes each).
+// Two rings in shared memory: weight slots (16 KB of packed weights each),
+// freed as soon as the converters have read them, and A' slots (two boxes
+// of 2 mp rows x 128 bytes), freed when the MMAs that read them complete.
 __host__ __device__ constexpr int a_box_bytes(int mp) { return 2 * mp * kABoxK; }
-__host__ __device__ constexpr int stage_bytes(int mp) { return kPackedBytes + 2 * a_box_bytes(mp); }
-__host__ __device__ constexpr int bar_bytes() { return (2 * kMaxStages + 2 * kWBufs + 4) * 8 + 16; }
-int stages_for(int mp)
+__host__ __device__ constexpr int a_stage_bytes(int mp) { return 2 * a_box_bytes(mp); }
+__host__ __device__ constexpr int bar_bytes() { return (2 * kMaxWStages + 2 * kMaxAStages + 2 * kWBufs + 4) * 8 + 16; }
+int a_stages_for(int mp)
 {
-    int s = (kSmemBudget - bar_bytes() - 1024) / stage_bytes(mp);
-    return s > kMaxStages ? kMaxStages : s;
+    const int s = 48 * 1024 / a_stage_bytes(mp);
+    return s < 3 ? 3 : (s > kMaxAStages ? kMaxAStages : s);
 }
-int smem_for(int mp) { return stages_for(mp) * stage_bytes(mp) + bar_bytes() + 1024; }
+int w_stages_for(int mp)
+{
+    const int s = (kSmemBudget - bar_bytes() - 1024 - a_stages_for(mp) * a_stage_bytes(mp)) / kPackedBytes;
+    return s > kMaxWStages ? kMaxWStages : s;
+}
+int smem_for(int mp)
+{
+    return w_stages_for(mp) * kPackedBytes + a_stages_for(mp) * a_stage_bytes(mp) + bar_bytes() + 1024;
+}
 
 __device__ __forceinline__ int seg_end(int kb0, int KB, int64_t left)
 {
@@ -175,12 +189,24 @@ __global__ void __launch_bounds__(kSplitThreads)
     const int groups = K / 8;
     uint8_t *hi_row = Ap + static_cast<int64_t>(m) * K;
     uint8_t *lo_row = Ap + static_cast<int64_t>(mp + m) * K;
+    const bool vec = (reinterpret_cast<uintptr_t>(A) & 7u) == 0;    // K is a multiple of 32
     int sum = 0;
+#pragma unroll 4
     for (int g = threadIdx.x; g < groups; g += kSplitThreads) {
+        int8_t av[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        if (m < M) {
+            const int8_t *src = A + static_cast<int64_t>(m) * K + 8 * g;
+            if (vec)
+                std::memcpy(av, __builtin_assume_aligned(src, 8), 8);
+            else
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    av[j] = src[j];
+        }
         uint8_t hc[8], lc[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            const int a = m < M ? static_cast<int>(A[static_cast<int64_t>(m) * K + 8 * g + j]) : 0;
+            const int a = av[j];
             const int hi = (a + 8) >> 4;
             const int lo = a - 16 * hi;
             sum += a;
@@ -210,15 +236,19 @@ __global__ void __launch_bounds__(kSplitThreads)
 __global__ void __launch_bounds__(kThreads, 1)
     w4a8_skinny_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmA,
                        const uint8_t *__restrict__ Bs, int32_t *__restrict__ D, int64_t ldd,
-                       const int32_t *__restrict__ R, int M, int N, int K, int mp, int stages, ErrCtx err)
+                       const int32_t *__restrict__ R, int M, int N, int K, int mp, int wstages, int astages,
+                       ErrCtx err)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
-    uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-    const int sbytes = stage_bytes(mp);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + stages * sbytes);
-    uint64_t *empty = full + kMaxStages;
-    uint64_t *cready = empty + kMaxStages;                     // converted weights in TMEM (converters)
+    uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);   // weight ring
+    const int abytes = a_stage_bytes(mp);
+    uint8_t *aring = smem + wstages * kPackedBytes;                     // A' ring
+    uint64_t *wfull = reinterpret_cast<uint64_t *>(aring + astages * abytes);
+    uint64_t *wempty = wfull + kMaxWStages;
+    uint64_t *afull = wempty + kMaxWStages;
+    uint64_t *aempty = afull + kMaxAStages;
+    uint64_t *cready = aempty + kMaxAStages;                   // converted weights in TMEM (converters)
     uint64_t *cfree = cready + kWBufs;                         // converted weights consumed (MMA commit)
     uint64_t *tfull = cfree + kWBufs;
     uint64_t *tempty = tfull + 2;
@@ -234,9 +264,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int abox = a_box_bytes(mp);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < stages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kConvWarps + 1);              // every converter warp + the MMA commit
+        for (int s = 0; s < wstages; ++s) {
+            mbar_init(&wfull[s], 1);
+            mbar_init(&wempty[s], kConvWarps);                 // every converter warp
+        }
+        for (int s = 0; s < astages; ++s) {
+            mbar_init(&afull[s], 1);
+            mbar_init(&aempty[s], 1);                          // the MMA commit
         }
         for (int b = 0; b < kWBufs; ++b) {
             mbar_init(&cready[b], kConvWarps);
@@ -262,62 +296,62 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
+    const int64_t n_units = u_end - u_begin;
     if (warp == 0) {
         if (lane == 0) {
-            // ---------------------------------------------- TMA producer
-            // The weights do not depend on the pre-pass: the first ring's
-            // worth is requested before waiting for A'.
-            const uint64_t keep_a = policy_evict_last();    // A' is re-read by every CTA
+            // ------------------------------------------ weight producer
+            // The weights do not depend on the pre-pass.  Unit u's weights:
+            // the pre-shuffled block u (16 KB, contiguous), else a 128 x
+            // 128-byte box of the row-major B.
             const uint64_t stream_b = policy_evict_first();  // the weights are read once
-            const uint32_t tx = static_cast<uint32_t>(kPackedBytes + 2 * abox);
-            const int64_t n = u_end - u_begin;
-            const int64_t pre = n < stages ? n : stages;
-            // weights of unit u: the pre-shuffled block u (16 KB, contiguous),
-            // else a 128 x 128-byte box of the row-major B
-            auto load_weights = [&](uint8_t *st, uint64_t *bar, int64_t u) {
-                if (Bs)
-                    bulk_load_hint(st, Bs + u * kPackedBytes, kPackedBytes, bar, stream_b);
-                else
-                    tma_load_2d_hint(st, &tmB, bar, static_cast<int>(u % KB) * (kBK / 2),
-                                     static_cast<int>(u / KB) * kTileN, stream_b);
-            };
-            for (int64_t i = 0; i < pre; ++i) {
-                mbar_arrive_expect_tx(&full[i], tx);
-                load_weights(smem + i * sbytes, &full[i], u_begin + i);
-            }
-            griddep_wait();
-            for (int64_t i = 0; i < pre; ++i) {
-                const int kb = static_cast<int>((u_begin + i) % KB);
-                uint8_t *st = smem + i * sbytes + kPackedBytes;
-                tma_load_2d_hint(st, &tmA, &full[i], kb * kBK, 0, keep_a);
-                tma_load_2d_hint(st + abox, &tmA, &full[i], kb * kBK + kABoxK, 0, keep_a);
-            }
-            int64_t issued = pre;
-            for (int64_t i = pre; i < n; ++i) {
-                const int stage = static_cast<int>(i % stages);
-                const uint32_t phase = static_cast<uint32_t>((i / stages) & 1);
-                if (!mbar_wait(&empty[stage], phase ^ 1u, err, abort_flag, kSiteProducerEmpty))
+            int64_t issued = 0;
+            for (int64_t i = 0; i < n_units; ++i) {
+                const int ws = static_cast<int>(i % wstages);
+                const uint32_t ph = static_cast<uint32_t>((i / wstages) & 1);
+                if (!mbar_wait(&wempty[ws], ph ^ 1u, err, abort_flag, kSiteProducerEmpty))
                     break;
-                ++issued;
                 const int64_t u = u_begin + i;
-                const int kb = static_cast<int>(u % KB);
-                uint8_t *st = smem + stage * sbytes;
-                mbar_arrive_expect_tx(&full[stage], tx);
-                load_weights(st, &full[stage], u);
-                tma_load_2d_hint(st + kPackedBytes, &tmA, &full[stage], kb * kBK, 0, keep_a);
-                tma_load_2d_hint(st + kPackedBytes + abox, &tmA, &full[stage], kb * kBK + kABoxK, 0, keep_a);
+                uint8_t *st = smem + ws * kPackedBytes;
+                mbar_arrive_expect_tx(&wfull[ws], kPackedBytes);
+                if (Bs)
+                    bulk_load_hint(st, Bs + u * kPackedBytes, kPackedBytes, &wfull[ws], stream_b);
+                else
+                    tma_load_2d_hint(st, &tmB, &wfull[ws], static_cast<int>(u % KB) * (kBK / 2),
+                                     static_cast<int>(u / KB) * kTileN, stream_b);
+                ++issued;
             }
             // before leaving, let every load this thread requested land
-            for (int64_t i = issued - 1; i >= 0 && i >= issued - stages; --i)
-                mbar_wait(&full[i % stages], static_cast<uint32_t>((i / stages) & 1), err, nullptr, kSiteDrain);
+            for (int64_t i = issued - 1; i >= 0 && i >= issued - wstages; --i)
+                mbar_wait(&wfull[i % wstages], static_cast<uint32_t>((i / wstages) & 1), err, nullptr, kSiteDrain);
+        }
+    } else if (warp == kAProducerWarp) {
+        if (lane == 0) {
+            // ---------------------------------------------- A' producer
+            const uint64_t keep_a = policy_evict_last();    // A' is re-read by every CTA
+            griddep_wait();                                  // A' comes from the pre-pass
+            int64_t issued = 0;
+            for (int64_t i = 0; i < n_units; ++i) {
+                const int as = static_cast<int>(i % astages);
+                const uint32_t ph = static_cast<uint32_t>((i / astages) & 1);
+                if (!mbar_wait(&aempty[as], ph ^ 1u, err, abort_flag, kSiteProducerEmpty))
+                    break;
+                const int kb = static_cast<int>((u_begin + i) % KB);
+                uint8_t *st = aring + as * abytes;
+                mbar_arrive_expect_tx(&afull[as], static_cast<uint32_t>(abytes));
+                tma_load_2d_hint(st, &tmA, &afull[as], kb * kBK, 0, keep_a);
+                tma_load_2d_hint(st + abox, &tmA, &afull[as], kb * kBK + kABoxK, 0, keep_a);
+                ++issued;
+            }
+            for (int64_t i = issued - 1; i >= 0 && i >= issued - astages; --i)
+                mbar_wait(&afull[i % astages], static_cast<uint32_t>((i / astages) & 1), err, nullptr, kSiteDrain);
         }
     } else if (warp == 1) {
         if (lane == 0) {
             // ------------------------------------------------ MMA issuer
             // MMA A = converted weights (TMEM, 128 rows), MMA B = A' (2 mp rows)
             const uint32_t idesc = idesc_e4m3_f32(kTileN, 2 * mp);
-            int stage = 0, wb = 0, seg = 0;
-            uint32_t phase = 0, wphase = 0;
+            int as = 0, wb = 0, seg = 0;
+            uint32_t aphase = 0, wphase = 0;
             bool ok = true;
             for (int64_t u = u_begin; u < u_end && ok; ++seg) {
                 const int kb0 = static_cast<int>(u % KB);
@@ -328,25 +362,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * kAccCols;
                 for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!mbar_wait(&full[stage], phase, err, abort_flag, kSiteMmaFull) ||
+                    if (!mbar_wait(&afull[as], aphase, err, abort_flag, kSiteMmaFull) ||
                         !mbar_wait(&cready[wb], wphase, err, abort_flag, kSiteMmaFull)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t a_src = tmem_base + kWCol0 + wb * kWCols;
-                    const uint64_t bdesc0 = sdesc_kmajor_sw128(smem_u32(smem + stage * sbytes + kPackedBytes));
-                    const uint64_t bdesc1 = sdesc_kmajor_sw128(smem_u32(smem + stage * sbytes + kPackedBytes + abox));
+                    const uint64_t bdesc0 = sdesc_kmajor_sw128(smem_u32(aring + as * abytes));
+                    const uint64_t bdesc1 = sdesc_kmajor_sw128(smem_u32(aring + as * abytes + abox));
 #pragma unroll
                     for (int k = 0; k < kBK / 32; ++k) {
                         const uint64_t bdesc = (k < 4 ? bdesc0 : bdesc1) + static_cast<uint64_t>(((k & 3) * 32) >> 4);
                         mma_e4m3_ts(d_tmem, a_src + 8 * k, bdesc, idesc, (kb != kb0) || (k != 0));
                     }
-                    mma_commit(&empty[stage]);
+                    mma_commit(&aempty[as]);
                     mma_commit(&cfree[wb]);
-                    if (++stage == stages) {
-                        stage = 0;
-                        phase ^= 1u;
+                    if (++as == astages) {
+                        as = 0;
+                        aphase ^= 1u;
                     }
                     if (++wb == kWBufs) {
                         wb = 0;
@@ -369,21 +403,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int half = (warp - kFirstConvWarp) >> 2;
         const int r = q * 32 + lane;
         const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + kWCol0 + 32 * half;
-        int stage = 0, wb = 0;
+        int ws = 0, wb = 0;
         uint32_t phase = 0, wphase = 0;
         for (int64_t u = u_begin; u < u_end; ++u) {
-            if (!mbar_wait(&full[stage], phase, err, abort_flag, kSiteMmaFull) ||
+            if (!mbar_wait(&wfull[ws], phase, err, abort_flag, kSiteMmaFull) ||
                 !mbar_wait(&cfree[wb], wphase ^ 1u, err, abort_flag, kSiteProducerEmpty))
                 break;
             tc_fence_after();
-            const uint8_t *src = smem + stage * sbytes + r * 128;
+            const uint8_t *src = smem + ws * kPackedBytes + r * 128;
             uint4 w[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i)
                 w[i] = *reinterpret_cast<const uint4 *>(src + (((4 * half + i) ^ (r & 7)) << 4));
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(&empty[stage]);
+                mbar_arrive(&wempty[ws]);
             uint32_t out[32];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -400,8 +434,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&cready[wb]);
-            if (++stage == stages) {
-                stage = 0;
+            if (++ws == wstages) {
+                ws = 0;
                 phase ^= 1u;
             }
             if (++wb == kWBufs) {
@@ -548,7 +582,7 @@ cudaError_t launch_w4a8_skinny(const W4a8SkinnyArgs &a, const ErrCtx &err, cudaS
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return e;
-    const int stages = stages_for(a.mp);
+    const int wstages = w_stages_for(a.mp), astages = a_stages_for(a.mp);
     const int smem = smem_for(a.mp);
     if ((e = ensure_smem_attr(reinterpret_cast<const void *>(w4a8_skinny_kernel), smem)) != cudaSuccess)
         return e;
@@ -565,7 +599,7 @@ cudaError_t launch_w4a8_skinny(const W4a8SkinnyArgs &a, const ErrCtx &err, cudaS
     cfg.numAttrs = 1;
     note_launch();
     return cudaLaunchKernelEx(&cfg, w4a8_skinny_kernel, a.tmB, a.tmA, a.Bs, a.D, a.ldd,
-                              static_cast<const int32_t *>(a.R), a.M, a.N, a.K, a.mp, stages, err);
+                              static_cast<const int32_t *>(a.R), a.M, a.N, a.K, a.mp, wstages, astages, err);
 }
 
 }  // namespace tmg
