@@ -27,11 +27,12 @@ class Workload:
     M: int
     N: int
     K: int
-    dtype: str          # "f32", "bf16" or "mxfp4"
+    dtype: str          # "f32", "bf16", "e4m3", "mxfp4" or "w4a8"
     a_dist: str         # description of the value distribution
     b_dist: str
     epilogue: str | None = None   # fused GEMM (tmg_gemm_fused) epilogue, or None
     a_mn_major: bool = False      # A stored MN-major: the buffer is Aᵀ, (K, M) row-major
+    b_preshuffled: bool = False   # W4A8: B handed to the GEMM as its pre-shuffled image
 
     @property
     def flops(self) -> int:
@@ -56,7 +57,8 @@ WORKLOADS = {
     "w4a8_8192": Workload("w4a8_8192", 8, 8192, 8192, 8192, "w4a8", "int8 U[-128,127]",
                           "int4 U[-8,7], packed"),
     "w4a8_16x28672x8192": Workload("w4a8_16x28672x8192", 9, 16, 28672, 8192, "w4a8", "int8 U[-128,127]",
-                                   "int4 U[-8,7], packed"),
+                                   "int4 U[-8,7], packed, pre-shuffled once before timing",
+                                   b_preshuffled=True),
     # general layout: A given column-major, (M,K):(1,M)
     "bf16_4096_a_mn_major": Workload("bf16_4096_a_mn_major", 7, 4096, 4096, 4096, "bf16",
                                      "N(0,1), stored MN-major", "N(0,1)", None, True),
