@@ -176,10 +176,11 @@ __global__ void __launch_bounds__(kSplitThreads)
             if (b % KB == 0)
                 continue;                                      // the boundary is a tile start
             const int64_t t = b / KB;
-            for (int i = threadIdx.x % 32; i < M * kTileN; i += 32) {
-                const int64_t n = t * kTileN + i % kTileN;
+            for (int col = threadIdx.x % 32; col < kTileN; col += 32) {
+                const int64_t n = t * kTileN + col;
                 if (n < N)
-                    D[static_cast<int64_t>(i / kTileN) * ldd + n] = 0;
+                    for (int m = 0; m < M; ++m)
+                        D[static_cast<int64_t>(m) * ldd + n] = 0;
             }
         }
         return;
