@@ -207,3 +207,20 @@ def test_w4a8_large_sums_keep_low_bits(tmg, monkeypatch, path):
         A, B = _biased_operands(M, N, K, a_lo, a_hi, b_lo, b_hi, 751 + a_lo)
         ref = oracle.gemm_w4a8(A.numpy(), B.numpy(), M, N, K)
         assert np.array_equal(_run(tmg, A, B), ref), (path, a_lo, b_lo)
+
+
+@pytest.mark.parametrize("path", ["decode", "general"])
+def test_w4a8_misaligned_activations(tmg, monkeypatch, path):
+    """A contiguous but starting one byte past an aligned address: the
+    kernels' vector loads of A fall back to byte loads, same exact result."""
+    if path == "general":
+        monkeypatch.setenv("TMG_W4A8_PATH", "general")
+    M, N, K = 9, 300, 1056
+    A, B = inputs.random_int8(M, K, 761), inputs.random_int4_packed(N, K, 762)
+    buf = torch.empty(M * K + 16, dtype=torch.int8, device=DEV)
+    Ad = buf[1:1 + M * K].view(M, K)
+    Ad.copy_(A.to(DEV))
+    assert Ad.data_ptr() % 8 == 1
+    D = tmg.gemm_w4a8(Ad, B.to(DEV))
+    tmg.check()
+    assert np.array_equal(D.cpu().numpy().astype(np.int64), oracle.gemm_w4a8(A.numpy(), B.numpy(), M, N, K))
