@@ -130,3 +130,31 @@ def test_mn_major_workload_size_sampled(tmg):
     ref = oracle.gemm_entries(inputs.bits_of(A), oracle.make_layout((w.M, w.K), (1, w.M)), inputs.bits_of(B),
                               oracle.row_major(w.N, w.K), oracle.BF16, w.K, ms, ns)
     parity.check_bf16_values(parity.to_f64(D)[ms, ns], ref, w.K, parity.absmax(A), parity.absmax(B))
+
+
+@pytest.mark.parametrize("maj", [1, 2, 3])
+@pytest.mark.parametrize("M,N,K", [(2048, 2560, 320), (2000, 2600, 136)])
+def test_mn_major_read_in_place(tmg, monkeypatch, maj, M, N, K):
+    """Large enough for CTA pairs: MN-major A (bit 0) and/or B (bit 1) are
+    read in place by the pair kernel (64 x 64 boxes, MN-major MMA
+    descriptors) instead of being gathered; ragged M, N and K. Exact
+    agreement with the gathered path is not required (same sums, but the
+    same fp32 accumulation order, so it holds too), the oracle bound is."""
+    A, B = inputs.normal_bf16(M, K, 411), inputs.normal_bf16(N, K, 412)
+    la = ((M, K), (1, M)) if maj & 1 else ((M, K), (K, 1))
+    lb = ((N, K), (1, N)) if maj & 2 else ((N, K), (K, 1))
+    Ab = A.t().contiguous() if maj & 1 else A
+    Bb = B.t().contiguous() if maj & 2 else B
+    Ad, Bd = Ab.to(DEV), Bb.to(DEV)
+    n0 = tmg.launch_count()
+    D = tmg.gemm(Ad, Bd, M=M, N=N, K=K, layoutA=la, layoutB=lb)
+    tmg.check()
+    assert tmg.launch_count() - n0 == 1                  # the pair kernel alone: no gather
+    ref = _ref(Ab, la, Bb, lb, M, N, K)
+    parity.check_bf16(D, ref, K, parity.absmax(A), parity.absmax(B))
+    monkeypatch.setenv("TMG_NO_INPLACE_MN", "1")
+    n0 = tmg.launch_count()
+    D2 = tmg.gemm(Ad, Bd, M=M, N=N, K=K, layoutA=la, layoutB=lb)
+    tmg.check()
+    assert tmg.launch_count() - n0 >= 2                  # gathered, then the GEMM
+    assert torch.equal(D, D2)

@@ -548,6 +548,65 @@ Scratch *host_scratch(cudaStream_t s, const size_t (&bytes)[3], tmg_status *st)
     return &sc;
 }
 
+// Operands given MN-major (M or N contiguous: (rows, K):(1, ld)) read in
+// place by the pair kernel, together with K-major ones, when the problem is
+// large enough for CTA pairs and D is row-major.  Returns false when it does
+// not apply (the caller gathers instead).
+bool run_tc2_inplace(const DeviceState &ds, const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K,
+                     const tmg_layout &la, const tmg_layout &lb, const tmg_layout &ld, cudaStream_t s,
+                     tmg_status *st)
+{
+    const int64_t ldd = row_stride_if_rowmajor(ld, M, N);
+    if (ldd <= 0 || (N > 1 && ldd < N) || M < 256 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX)
+        return false;
+    const void *ops[2] = {A, B};
+    const tmg_layout *lays[2] = {&la, &lb};
+    const int64_t rows[2] = {M, N};
+    int64_t lds[2];
+    int maj = 0;
+    for (int i = 0; i < 2; ++i) {
+        lds[i] = row_stride_if_rowmajor(*lays[i], rows[i], K);
+        if (lds[i] > 0 && tma_ok(ops[i], lds[i], 2, rows[i], K))
+            continue;
+        lds[i] = col_stride_if_colmajor(*lays[i], rows[i], K);
+        if (lds[i] > 0 && lds[i] >= rows[i] && tma_ok(ops[i], lds[i], 2, K, rows[i])) {
+            maj |= 1 << i;
+            continue;
+        }
+        return false;
+    }
+    if (maj == 0)
+        return false;                                     // the ordinary dispatch covers it
+    TcArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.maj = maj;
+    a.bn = (maj & 2) ? (N >= 256 ? 256 : 128) : tc2_pick_bn(M, N, ds.num_sms);
+    if (((M + 255) / 256) * ((N + a.bn - 1) / a.bn) < ds.num_sms / 2)
+        return false;                                     // too few pair tiles
+    if ((*st = (maj & 1) ? encode_2d(&a.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, M, K, lds[0], 64, 64)
+                         : encode_2d(&a.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, K, M, lds[0], 64, 128)) != TMG_OK)
+        return true;
+    if ((*st = (maj & 2) ? encode_2d(&a.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, N, K, lds[1], 64, 64)
+                         : encode_2d(&a.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, K, N, lds[1], 64, a.bn / 2)) !=
+        TMG_OK)
+        return true;
+    a.D = D;
+    a.ldd = ldd;
+    a.M = static_cast<int>(M);
+    a.N = static_cast<int>(N);
+    a.K = static_cast<int>(K);
+    tc2_plan(a, ds.num_sms);
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if ((*st = tc2_scratch(dev, s, a)) != TMG_OK)
+        return true;
+    if ((*st = encode_d_store(a, D, M, N, ldd)) != TMG_OK)
+        return true;
+    const cudaError_t e = launch_tc2_bf16(a, ds.num_sms, err_ctx(ds), s);
+    *st = e == cudaSuccess ? TMG_OK : cuda_fail(e, "tc2_bf16 (MN-major operands) launch");
+    return true;
+}
+
 // General layouts on the tensor cores: every operand the TMA cannot read in
 // place is gathered through its layout into a dense K-major scratch copy
 // (rows padded to a multiple of 8 elements), a D that is neither row- nor
@@ -558,6 +617,8 @@ tmg_status run_packed(const DeviceState &ds, const void *A, const void *B, void 
 {
     tmg_status st;
     cudaError_t e;
+    if (!getenv("TMG_NO_INPLACE_MN") && run_tc2_inplace(ds, A, B, D, M, N, K, la, lb, ld, s, &st))
+        return st;
     const int64_t Kp = (K + 7) / 8 * 8;
     const void *ops[2] = {A, B};
     const tmg_layout *lays[2] = {&la, &lb};

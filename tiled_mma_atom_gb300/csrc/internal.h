@@ -61,6 +61,8 @@ struct TcArgs {
     int sk_tiles;      // tiles after them, run stream-K
     float *partials;   // tc2_partials_bytes()
     uint32_t *counters;  // tc2_counters_bytes(), zero on entry
+    int maj;           // pair kernel, bf16: bit 0 A MN-major (tmA over Aᵀ, box {64, 64}), bit 1 B MN-major
+                       // (tmB over Bᵀ, box {64, 64}; bn 256 or 128)
 };
 cudaError_t launch_tc_bf16(const TcArgs &a, int num_sms, const ErrCtx &err, cudaStream_t s);
 // CTA-pair variant (cta_group::2, 256 x bn tiles; bn in {256, 224, 192, 128},

@@ -64,6 +64,18 @@ cudaError_t launch_tc2_bf16(const TcArgs &a, int num_sms, const ErrCtx &err, cud
 {
     (void)num_sms;
     const Tc2Epi none{nullptr, nullptr, nullptr, kEpiNone, 0};
+    if (a.maj != 0) {
+        // MN-major operands read in place (bn 256 or 128)
+        const bool w = a.bn == 256;
+        switch (a.maj) {
+        case 1:
+            return w ? launch_pair<256, kInBf16, false, 1>(a, none, err, s) : launch_pair<128, kInBf16, false, 1>(a, none, err, s);
+        case 2:
+            return w ? launch_pair<256, kInBf16, false, 2>(a, none, err, s) : launch_pair<128, kInBf16, false, 2>(a, none, err, s);
+        default:
+            return w ? launch_pair<256, kInBf16, false, 3>(a, none, err, s) : launch_pair<128, kInBf16, false, 3>(a, none, err, s);
+        }
+    }
     switch (a.bn) {
     case 256:
         return launch_pair<256, kInBf16, false>(a, none, err, s);

@@ -86,6 +86,37 @@ struct PairCfg {
     static constexpr int SMEM = STAGES * STAGE_BYTES + STAGING_BYTES + BAR_BYTES + COLS_BYTES + 1024;
 };
 
+// Operand majorness (template parameter MAJ): bit 0 set when A is MN-major
+// (stored with M contiguous, i.e. Aᵀ row-major), bit 1 when B is (N
+// contiguous).  bf16 only.  An MN-major operand's K block lands as 64 x 64
+// boxes (64 M- or N-elements by 64 k, 128-byte swizzle): k row r of a box
+// at r * 128 bytes, 8-row groups of 1024 bytes, the next 64 M/N elements in
+// the next box 8 KB on — the canonical MN-major layout of the MMA, whose
+// descriptor takes the 8 KB step between 64-element MN chunks as its
+// leading byte offset and the 1 KB step between 8-row K groups as its
+// stride byte offset.  One MMA (K = 16) covers 16 k rows = 2048 bytes.
+constexpr int kMnBox = 64;
+constexpr int kMnBoxBytes = kMnBox * kKBlockBytes;       // 8 KB
+constexpr int kMnKStepBytes = 16 * kKBlockBytes;         // 2 KB per MMA
+
+__device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(kMnBoxBytes >> 4) << 16;
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(2) << 61;
+    return d;
+}
+
+// kind::f16 instruction descriptor with the operands' transpose bits (bit 15
+// A MN-major, bit 16 B MN-major).
+__host__ __device__ constexpr uint32_t idesc_bf16_major(int M, int N, int maj)
+{
+    return idesc_bf16_f32(M, N) | ((maj & 1) ? (1u << 15) : 0u) | ((maj & 2) ? (1u << 16) : 0u);
+}
+
 __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int &tm, int &tn)
 {
     const int group = kGroupM * tiles_n;
@@ -273,7 +304,7 @@ __device__ __forceinline__ void apply_epilogue(float (&v)[32], const Tc2Epi &e, 
     }
 }
 
-template <int BN, int IN, bool EPI>
+template <int BN, int IN, bool EPI, int MAJ = 0>
 __global__ void __launch_bounds__(tc2_threads(EPI), 1)
     tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmD, __nv_bfloat16 *__restrict__ D, int64_t ldd, int M, int N,
@@ -281,6 +312,7 @@ __global__ void __launch_bounds__(tc2_threads(EPI), 1)
                     uint32_t *__restrict__ counters, int vec_ok, int d_tma, Tc2Epi epi, ErrCtx err)
 {
     using C = PairCfg<BN, EPI>;
+    static_assert(MAJ == 0 || (IN == kInBf16 && !EPI && (BN / 2) % kMnBox == 0), "MN-major operands: plain bf16");
     constexpr int KB_ELEMS = kb_elems(IN);
     constexpr int STAGES = C::STAGES;
     constexpr uint32_t STAGE_TX = 2u * C::STAGE_BYTES;
@@ -352,8 +384,23 @@ __global__ void __launch_bounds__(tc2_threads(EPI), 1)
                     if (rank == 0)
                         mbar_arrive_expect_tx(&full[stage], STAGE_TX);
                     const uint32_t bar0 = mapa_shared(smem_u32(&full[stage]), 0);
-                    tma_load_2d_pair(sA + stage * C::A_BYTES, &tmA, bar0, kb * KB_ELEMS, tm * kBM + rank * kHalfM);
-                    tma_load_2d_pair(sB + stage * C::B_BYTES, &tmB, bar0, kb * KB_ELEMS, tn * BN + rank * (BN / 2));
+                    const int a_row = tm * kBM + rank * kHalfM, b_row = tn * BN + rank * (BN / 2);
+                    if constexpr (MAJ & 1) {
+#pragma unroll
+                        for (int j = 0; j < kHalfM / kMnBox; ++j)
+                            tma_load_2d_pair(sA + stage * C::A_BYTES + j * kMnBoxBytes, &tmA, bar0, a_row + j * kMnBox,
+                                             kb * KB_ELEMS);
+                    } else {
+                        tma_load_2d_pair(sA + stage * C::A_BYTES, &tmA, bar0, kb * KB_ELEMS, a_row);
+                    }
+                    if constexpr ((MAJ & 2) != 0) {
+#pragma unroll
+                        for (int j = 0; j < (BN / 2) / kMnBox; ++j)
+                            tma_load_2d_pair(sB + stage * C::B_BYTES + j * kMnBoxBytes, &tmB, bar0, b_row + j * kMnBox,
+                                             kb * KB_ELEMS);
+                    } else {
+                        tma_load_2d_pair(sB + stage * C::B_BYTES, &tmB, bar0, kb * KB_ELEMS, b_row);
+                    }
                     ++issued;
                     if (++stage == STAGES) {
                         stage = 0;
@@ -379,7 +426,7 @@ __global__ void __launch_bounds__(tc2_threads(EPI), 1)
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) {
             // ------------------------------------------------ MMA issuer
-            constexpr uint32_t idesc = IN == kInE4m3 ? idesc_e4m3_f32(kBM, BN) : idesc_bf16_f32(kBM, BN);
+            constexpr uint32_t idesc = IN == kInE4m3 ? idesc_e4m3_f32(kBM, BN) : idesc_bf16_major(kBM, BN, MAJ);
             int stage = 0;
             uint32_t phase = 0;
             int local = 0;
@@ -401,15 +448,18 @@ __global__ void __launch_bounds__(tc2_threads(EPI), 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(sA + stage * C::A_BYTES));
-                    const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(sB + stage * C::B_BYTES));
+                    const uint32_t a_s = smem_u32(sA + stage * C::A_BYTES), b_s = smem_u32(sB + stage * C::B_BYTES);
+                    const uint64_t adesc = (MAJ & 1) ? sdesc_mnmajor_sw128(a_s) : sdesc_kmajor_sw128(a_s);
+                    const uint64_t bdesc = (MAJ & 2) ? sdesc_mnmajor_sw128(b_s) : sdesc_kmajor_sw128(b_s);
+                    // per MMA: 32 bytes along a K-major row, or 16 k rows of an MN-major box
+                    constexpr uint64_t astep = ((MAJ & 1) ? kMnKStepBytes : 32) >> 4;
+                    constexpr uint64_t bstep = ((MAJ & 2) ? kMnKStepBytes : 32) >> 4;
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        const uint64_t koff = static_cast<uint64_t>((k * 32) >> 4);   // 32 bytes per MMA
                         if constexpr (IN == kInE4m3)
-                            mma_e4m3_pair(d_tmem, adesc + koff, bdesc + koff, idesc, (kb != kb0) || (k != 0));
+                            mma_e4m3_pair(d_tmem, adesc + k * astep, bdesc + k * bstep, idesc, (kb != kb0) || (k != 0));
                         else
-                            mma_bf16_pair(d_tmem, adesc + koff, bdesc + koff, idesc, (kb != kb0) || (k != 0));
+                            mma_bf16_pair(d_tmem, adesc + k * astep, bdesc + k * bstep, idesc, (kb != kb0) || (k != 0));
                     }
                     mma_commit_pair(&empty[stage], 0x3);
                     if (++stage == STAGES) {
@@ -603,7 +653,7 @@ __global__ void __launch_bounds__(tc2_threads(EPI), 1)
     }
 }
 
-template <int BN, int IN, bool EPI>
+template <int BN, int IN, bool EPI, int MAJ = 0>
 cudaError_t launch_pair(const TcArgs &a, const Tc2Epi &epi, const ErrCtx &err, cudaStream_t s)
 {
     using C = PairCfg<BN, EPI>;
@@ -611,7 +661,7 @@ cudaError_t launch_pair(const TcArgs &a, const Tc2Epi &epi, const ErrCtx &err, c
     static_assert(C::STAGES >= 4, "pipeline depth");
     static_assert(2 * BN <= C::TMEM_COLS, "TMEM budget");
     static_assert(C::B_BYTES % 1024 == 0, "B half must be whole 8-row swizzle atoms");
-    auto kern = tc2_gemm_kernel<BN, IN, EPI>;
+    auto kern = tc2_gemm_kernel<BN, IN, EPI, MAJ>;
     constexpr int SMEM = C::SMEM;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), SMEM);
     if (e != cudaSuccess)
