@@ -50,7 +50,7 @@ L2_BYTES = 129 * 10**6
 KERNEL_OF = {"fp32_128": "ffma_gemm_kernel", "bf16_1024": "tc_bf16_kernel",
              "bf16_4096": "tc2_gemm_kernel", "skinny_16x28672x8192": "skinny_tc_kernel",
              "mxfp4_8192": "mxfp4_pair_kernel", "e4m3_8192_bias_gelu": "tc2_gemm_kernel",
-             "bf16_4096_bias_silu": "tc2_gemm_kernel", "bf16_4096_a_mn_major": "tc2_gemm_kernel",
+             "bf16_4096_bias_silu": "tc2_gemm_kernel", "bf16_4096_a_mn_major": "tc2_gemm_kernel", "bf16_4096_b_kn": "tc2_gemm_kernel",
              "w4a8_8192": "tc2_gemm_kernel", "w4a8_16x28672x8192": "w4a8_skinny_kernel"}
 
 
@@ -213,8 +213,10 @@ def make_call(w, dev_in, out, stream):
         return lambda: tmg.gemm_fused(A, B, out, scale_a=sa, scale_b=sb, bias=bias,
                                       epilogue=w.epilogue, stream=stream)
     A, B = dev_in
-    if w.a_mn_major:
-        return lambda: tmg.gemm(A, B, out, M=w.M, N=w.N, K=w.K, layoutA=((w.M, w.K), (1, w.M)), stream=stream)
+    if w.a_mn_major or w.b_mn_major:
+        la = ((w.M, w.K), (1, w.M)) if w.a_mn_major else None
+        lb = ((w.N, w.K), (1, w.N)) if w.b_mn_major else None
+        return lambda: tmg.gemm(A, B, out, M=w.M, N=w.N, K=w.K, layoutA=la, layoutB=lb, stream=stream)
     return lambda: tmg.gemm(A, B, out, stream=stream)
 
 
@@ -305,7 +307,7 @@ def time_e2e(w, steps, dev, stream):
     host = [t.pin_memory() for t in host]
     dt = {"f32": torch.float32, "w4a8": torch.int32}.get(w.dtype, torch.bfloat16)
     out_host = torch.empty((w.M, w.N), dtype=dt).pin_memory()
-    if w.dtype in ("f32", "bf16") and w.epilogue is None and not w.a_mn_major:
+    if w.dtype in ("f32", "bf16") and w.epilogue is None and not w.a_mn_major and not w.b_mn_major:
         def step():
             tmg.gemm_host(host[0], host[1], out_host, stream=stream)
     else:
@@ -372,12 +374,13 @@ def oracle_sample(w, budget_s):
         A, B = host
         dtype = oracle.F32 if w.dtype == "f32" else oracle.BF16
         b = inputs.bits_of(B)
+        lb = oracle.make_layout((w.N, w.K), (1, w.N)) if w.b_mn_major else oracle.row_major(w.N, w.K)
         if w.a_mn_major:            # the first rows of A are the first columns of its buffer
             a, la = inputs.bits_of(A), oracle.make_layout((rows, w.K), (1, w.M))
         else:
             a, la = inputs.bits_of(A[:rows]), oracle.row_major(rows, w.K)
         t0 = time.perf_counter()
-        oracle.gemm(a, la, b, oracle.row_major(w.N, w.K), dtype, rows, w.N, w.K)
+        oracle.gemm(a, la, b, lb, dtype, rows, w.N, w.K)
         return time.perf_counter() - t0
 
     probe_rows = min(w.M, max(1, threads))

@@ -137,9 +137,9 @@ def test_mn_major_workload_size_sampled(tmg):
 def test_mn_major_read_in_place(tmg, monkeypatch, maj, M, N, K):
     """Large enough for CTA pairs: MN-major A (bit 0) and/or B (bit 1) are
     read in place by the pair kernel (64 x 64 boxes, MN-major MMA
-    descriptors) instead of being gathered; ragged M, N and K. Exact
-    agreement with the gathered path is not required (same sums, but the
-    same fp32 accumulation order, so it holds too), the oracle bound is."""
+    descriptors) instead of being gathered; ragged M, N and K.  The result
+    meets the oracle bound and equals the gathered path's bit for bit (the
+    same MMAs in the same order)."""
     A, B = inputs.normal_bf16(M, K, 411), inputs.normal_bf16(N, K, 412)
     la = ((M, K), (1, M)) if maj & 1 else ((M, K), (K, 1))
     lb = ((N, K), (1, N)) if maj & 2 else ((N, K), (K, 1))
@@ -158,3 +158,18 @@ def test_mn_major_read_in_place(tmg, monkeypatch, maj, M, N, K):
     tmg.check()
     assert tmg.launch_count() - n0 >= 2                  # gathered, then the GEMM
     assert torch.equal(D, D2)
+
+
+def test_b_kn_workload_size_sampled(tmg):
+    """The benchmark's C = A·B workload (bf16 4096³, B stored K×N row-major,
+    i.e. MN-major) at full size, sampled against the oracle."""
+    w = inputs.WORKLOADS["bf16_4096_b_kn"]
+    A, B = inputs.make_inputs(w)
+    n0 = tmg.launch_count()
+    D = tmg.gemm(A.to(DEV), B.to(DEV), M=w.M, N=w.N, K=w.K, layoutB=((w.N, w.K), (1, w.N)))
+    tmg.check()
+    assert tmg.launch_count() - n0 == 1
+    ms, ns = parity.sample_coords(w.M, w.N, 3000, seed=6)
+    ref = oracle.gemm_entries(inputs.bits_of(A), oracle.row_major(w.M, w.K), inputs.bits_of(B),
+                              oracle.make_layout((w.N, w.K), (1, w.N)), oracle.BF16, w.K, ms, ns)
+    parity.check_bf16_values(parity.to_f64(D)[ms, ns], ref, w.K, parity.absmax(A), parity.absmax(B))

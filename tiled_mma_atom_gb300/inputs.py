@@ -33,6 +33,7 @@ class Workload:
     epilogue: str | None = None   # fused GEMM (tmg_gemm_fused) epilogue, or None
     a_mn_major: bool = False      # A stored MN-major: the buffer is Aᵀ, (K, M) row-major
     b_preshuffled: bool = False   # W4A8: B handed to the GEMM as its pre-shuffled image
+    b_mn_major: bool = False      # B stored MN-major: the buffer is Bᵀ, (K, N) row-major (C = A·B)
 
     @property
     def flops(self) -> int:
@@ -62,6 +63,9 @@ WORKLOADS = {
     # general layout: A given column-major, (M,K):(1,M)
     "bf16_4096_a_mn_major": Workload("bf16_4096_a_mn_major", 7, 4096, 4096, 4096, "bf16",
                                      "N(0,1), stored MN-major", "N(0,1)", None, True),
+    # C = A·B with B stored (K, N) row-major: B is MN-major, (N,K):(1,N)
+    "bf16_4096_b_kn": Workload("bf16_4096_b_kn", 10, 4096, 4096, 4096, "bf16",
+                               "N(0,1)", "N(0,1), stored (K,N) row-major", b_mn_major=True),
 }
 
 
@@ -192,7 +196,10 @@ def make_inputs(w: Workload):
         A = normal_bf16(M, w.K, s + 0)
         if w.a_mn_major:
             A = A.t().contiguous()
-        return A, normal_bf16(w.N, w.K, s + 1, std=std_b)
+        B = normal_bf16(w.N, w.K, s + 1, std=std_b)
+        if w.b_mn_major:
+            B = B.t().contiguous()
+        return A, B
     if w.dtype == "w4a8":
         return random_int8(M, w.K, s + 0), random_int4_packed(w.N, w.K, s + 1)
     if w.dtype == "mxfp4":
