@@ -87,13 +87,18 @@ typedef enum {
  *   SKINNY_FFMA — CUDA-core split-K dot products for M <= 16, bf16, K-major;
  *   TC_SINGLE / TC_PAIR — TC restricted to one-CTA 128-row tiles or to
  *            CTA-pair (cta_group::2) 256-row tiles; TC picks between them;
- *   PACKED_TC — bf16 in any layout on the tensor cores: operands the TMA
- *            cannot read in place (MN-major, nested, strided, broadcast) are
- *            first gathered through their layouts into K-major workspace
- *            copies, a D that is neither row- nor column-major is computed
- *            into a dense workspace and scattered back.  AUTO takes it for
- *            bf16 problems with M*N*K >= 2^27 that TC cannot read in place
- *            (smaller ones go to FFMA).
+ *   PACKED_TC — bf16 in any layout on the tensor cores.  Flat MN-major
+ *            operands (A as (M,K):(1,lda), B as (N,K):(1,ldb), i.e. B stored
+ *            K x N row-major as in C = A*B; 16-byte aligned, ld a multiple
+ *            of 8) are read in place by the CTA-pair kernel when D is
+ *            row-major, M >= 256 and the pair tiles fill every pair once;
+ *            otherwise operands the TMA cannot read in place (MN-major,
+ *            nested, strided, broadcast) are first gathered through their
+ *            layouts into K-major workspace copies, and a D that is neither
+ *            row- nor column-major is computed into a dense workspace and
+ *            scattered back.  AUTO takes it for bf16 problems with
+ *            M*N*K >= 2^27 that TC cannot read in place (smaller ones go to
+ *            FFMA).
  * Forcing a family that cannot take the arguments returns UNSUPPORTED. */
 typedef enum {
     TMG_PATH_AUTO = 0,
