@@ -173,3 +173,20 @@ def test_b_kn_workload_size_sampled(tmg):
     ref = oracle.gemm_entries(inputs.bits_of(A), oracle.row_major(w.M, w.K), inputs.bits_of(B),
                               oracle.make_layout((w.N, w.K), (1, w.N)), oracle.BF16, w.K, ms, ns)
     parity.check_bf16_values(parity.to_f64(D)[ms, ns], ref, w.K, parity.absmax(A), parity.absmax(B))
+
+
+def test_mn_major_in_place_padded_leading_dimension(tmg):
+    """Column-major A inside a wider buffer (lda = M + 8) and B (K,N)
+    row-major inside one with ldb = N + 24: still read in place."""
+    M, N, K = 2048, 2560, 192
+    A, B = inputs.normal_bf16(M, K, 421), inputs.normal_bf16(N, K, 422)
+    Abuf = torch.zeros(K, M + 8, dtype=torch.bfloat16)
+    Abuf[:, :M] = A.t()
+    Bbuf = torch.zeros(K, N + 24, dtype=torch.bfloat16)
+    Bbuf[:, :N] = B.t()
+    la, lb = ((M, K), (1, M + 8)), ((N, K), (1, N + 24))
+    n0 = tmg.launch_count()
+    D = tmg.gemm(Abuf.to(DEV), Bbuf.to(DEV), M=M, N=N, K=K, layoutA=la, layoutB=lb)
+    tmg.check()
+    assert tmg.launch_count() - n0 == 1
+    parity.check_bf16(D, _ref(Abuf, la, Bbuf, lb, M, N, K), K, parity.absmax(A), parity.absmax(B))
