@@ -194,7 +194,7 @@ def accumulate_note(w):
     if w.M <= 64:
         return ("exact integer: offset-binary E4M3 weights on the fp8 tensor cores, fp32 column sums "
                 "below 2^22, int32 epilogue")
-    return "exact integer: fp32 within K segments of 4096, int32 across them"
+    return "exact integer: fp32 within K segments of 8192, int32 across them"
 
 
 def make_call(w, dev_in, out, stream):

@@ -211,8 +211,9 @@ tmg_status tmg_gemm_fused(const void *A, const void *B, void *D, int64_t M,
  *     stream);
  *   otherwise: both operands are unpacked to bf16 (exact) into workspace
  *     ((M + N) x K bf16), multiplied on the bf16 tensor cores in K segments
- *     of at most 4096 — where every fp32 partial sum is an integer below
- *     2^22, hence exact — and each segment is added into D as int32. */
+ *     of at most 8192 — where every fp32 partial sum is an integer of
+ *     magnitude at most 2^23, hence exact — and each segment is stored or
+ *     added into D as int32. */
 tmg_status tmg_gemm_w4a8(const void *A, const void *B, void *D, int64_t M,
                          int64_t N, int64_t K, void *stream);
 

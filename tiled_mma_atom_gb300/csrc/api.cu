@@ -1072,10 +1072,11 @@ tmg_status gemm_w4a8_impl(const void *A, const void *B, bool shuffled, void *D, 
         return st;
     if ((e = launch_unpack_w4a8(A, B, M, N, K, PA, PB, ldp, ds->num_sms, s, shuffled)) != cudaSuccess)
         return cuda_fail(e, "W4A8 unpack launch");
-    // K segments of at most 4096: every partial sum of a segment is an integer
-    // of magnitude <= 128 * 8 * 4096 = 2^22, exact in the fp32 accumulator;
-    // the first segment stores its int32 result, the others add to it.
-    constexpr int64_t kSeg = 4096;
+    // K segments of at most 8192: every partial sum of a segment is an integer
+    // of magnitude <= 128 * 8 * 8192 = 2^23, exact in the fp32 accumulator
+    // (integers up to 2^24 are); the first segment stores its int32 result,
+    // the others add to it.
+    constexpr int64_t kSeg = 8192;
     int dev = 0;
     cudaGetDevice(&dev);
     for (int64_t k0 = 0; k0 < K; k0 += kSeg) {

@@ -7,10 +7,10 @@
 // tensor-core MMA (tcgen05 kind::i8 is not available on sm_103a), so here
 // both operands are unpacked to bf16 — every int8 and int4 value is exact in
 // bf16 — and the product runs on the bf16 tensor cores with fp32
-// accumulation, which is exact for integer sums while they stay far below
-// 2^24: the library cuts K into segments of at most 4096 (|sum| <= 1024 *
-// 4096 = 2^22) and the GEMM epilogue adds each segment's result into the
-// int32 D (api.cu, tmg_gemm_w4a8).
+// accumulation, which is exact for integer sums below 2^24: the library
+// cuts K into segments of at most 8192 (|sum| <= 1024 * 8192 = 2^23) and the
+// GEMM epilogue stores or adds each segment's result into the int32 D
+// (api.cu, gemm_w4a8_impl).
 //
 // unpack: P[r * ldp + k] = bf16(X(r, k)) for k < K, 0 for K <= k < ldp, with
 // X either int8 (X(r, k) = A[r * K + k]) or packed int4 (two's complement
