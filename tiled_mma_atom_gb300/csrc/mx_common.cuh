@@ -117,5 +117,14 @@ __device__ __forceinline__ void tmem_cp_wide_pair(uint32_t taddr, uint64_t sdesc
     asm volatile("tcgen05.cp.cta_group::2.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
+// Programmatic dependent launch: the relayout pre-pass lets the GEMM start
+// early; the GEMM waits for the pre-pass's results only where it reads them.
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 }  // namespace mx
 }  // namespace tmg

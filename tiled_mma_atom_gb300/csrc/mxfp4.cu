@@ -76,6 +76,7 @@ struct RelayoutOperand {
 __global__ void __launch_bounds__(256)
     mx_scale_relayout_kernel(RelayoutOperand a, RelayoutOperand b, int sf_per_row, int num_kb)
 {
+    griddep_launch_dependents();
     const RelayoutOperand &o = blockIdx.y == 1 ? b : a;
     __shared__ uint32_t tile[128][17];                 // 16 words of scales per row, +1 pad
     const int kgroups = (num_kb + 7) / 8;

@@ -146,17 +146,44 @@ __global__ void __launch_bounds__(pair_threads(ACC_BUFS), 1)
     if (warp == 0) {
         if (lane == 0) {
             // ---------------------------------------------- TMA producer
+            // The kernel is a programmatic dependent launch of the scale
+            // relayout pre-pass: the first ring's worth of code tiles is
+            // requested before waiting for the pre-pass, their scale loads
+            // right after it.
             int stage = 0;
             uint32_t phase = 0;
             int64_t issued = 0;
             bool ok = true;
+            bool scales_ready = false;
+            // rows (of 256 bytes) of this CTA's relaid scales for tile t, K block kb
+            auto sfa_row = [&](int tm, int kb) {
+                return (tm * 2 + static_cast<int>(rank)) * num_kb * (C::SFA_BYTES / 256) + kb * (C::SFA_BYTES / 256);
+            };
+            auto sfb_row = [&](int tn, int kb) { return tn * num_kb * (C::SFB_BYTES / 256) + kb * (C::SFB_BYTES / 256); };
+            auto load_scales = [&](int st, int tm, int tn, int kb) {
+                const uint32_t b0 = mapa_shared(smem_u32(&full[st]), 0);
+                tma_load_2d_pair(sfA + st * C::SFA_BYTES, &tmSA, b0, 0, sfa_row(tm, kb));
+                tma_load_2d_pair(sfB + st * C::SFB_BYTES, &tmSB, b0, 0, sfb_row(tn, kb));
+            };
+            // the units issued so far are the first ones of this pair's walk,
+            // in stages 0, 1, ...: load their scales
+            auto release_deferred = [&]() {
+                griddep_wait();
+                int64_t i = 0;
+                for (int t2 = cluster; t2 < num_tiles && i < issued; t2 += nclusters) {
+                    int tm2, tn2;
+                    tile_coords(t2, tiles_m, tiles_n, tm2, tn2);
+                    for (int kb2 = 0; kb2 < num_kb && i < issued; ++kb2, ++i)
+                        load_scales(static_cast<int>(i), tm2, tn2, kb2);
+                }
+                scales_ready = true;
+            };
             for (int t = cluster; t < num_tiles && ok; t += nclusters) {
                 int tm, tn;
                 tile_coords(t, tiles_m, tiles_n, tm, tn);
-                // rows (of 256 bytes) of this CTA's / this tile's relaid scales
-                const int sfa_row0 = (tm * 2 + static_cast<int>(rank)) * num_kb * (C::SFA_BYTES / 256);
-                const int sfb_row0 = tn * num_kb * (C::SFB_BYTES / 256);
                 for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!scales_ready && issued == STAGES)
+                        release_deferred();
                     if (!mbar_wait_cluster(&empty[stage], phase ^ 1u, err, abort_flag, kSiteProducerEmpty)) {
                         ok = false;
                         break;
@@ -168,8 +195,8 @@ __global__ void __launch_bounds__(pair_threads(ACC_BUFS), 1)
                                      tm * kBM + static_cast<int>(rank) * kHalfM);
                     tma_load_2d_pair(tB + stage * C::B_BYTES, &tmB, bar0, kb * kBKBytes,
                                      tn * BN + static_cast<int>(rank) * (BN / 2));
-                    tma_load_2d_pair(sfA + stage * C::SFA_BYTES, &tmSA, bar0, 0, sfa_row0 + kb * (C::SFA_BYTES / 256));
-                    tma_load_2d_pair(sfB + stage * C::SFB_BYTES, &tmSB, bar0, 0, sfb_row0 + kb * (C::SFB_BYTES / 256));
+                    if (scales_ready)
+                        load_scales(stage, tm, tn, kb);
                     ++issued;
                     if (++stage == STAGES) {
                         stage = 0;
@@ -177,6 +204,8 @@ __global__ void __launch_bounds__(pair_threads(ACC_BUFS), 1)
                     }
                 }
             }
+            if (!scales_ready)
+                release_deferred();          // fewer units than stages, or an early stop
             for (int i = 0; i < STAGES && i < issued; ++i) {
                 int s = stage - 1 - i;
                 uint32_t ph = phase;
@@ -405,13 +434,15 @@ cudaError_t launch_pair(const Mxfp4Args &a, int num_sms, const ErrCtx &err, cuda
     cfg.blockDim = dim3(pair_threads(ACC_BUFS));
     cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // overlaps the relayout pre-pass
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     const int vec_ok = (a.N % 8 == 0) && ((reinterpret_cast<uintptr_t>(a.D) & 15u) == 0);
     note_launch();
     e = cudaLaunchKernelEx(&cfg, kern, a.tmA, a.tmB, a.tmSA, a.tmSB, static_cast<__nv_bfloat16 *>(a.D), a.M, a.N,
