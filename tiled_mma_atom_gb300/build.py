@@ -20,7 +20,7 @@ LIB = os.path.join(HERE, "libtmg.so")
 SOURCES = ["api.cu", "ffma.cu", "tc_bf16.cu", "tc2_bf16.cu", "tc2_fused.cu", "skinny.cu", "mxfp4.cu",
            "mxfp4_pair.cu", "pack.cu", "w4a8.cu", "w4a8_skinny.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
+FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-Wall",
                 "-I", CSRC, "-I", INCLUDE]
 
 

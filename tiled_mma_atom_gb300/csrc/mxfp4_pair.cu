@@ -366,37 +366,37 @@ __global__ void __launch_bounds__(pair_threads(ACC_BUFS), 1)
                         }
                     }
                 }
-                continue;
-            }
+            } else {
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld32(tbase + c * 32, v);
-                const int col0 = tn * BN + c * 32;
-                if (row < M) {
-                    if (vec_ok && col0 + 32 <= N) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(drow + col0);
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(tbase + c * 32, v);
+                    const int col0 = tn * BN + c * 32;
+                    if (row < M) {
+                        if (vec_ok && col0 + 32 <= N) {
+                            uint4 *dst = reinterpret_cast<uint4 *>(drow + col0);
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            uint4 w;
-                            w.x = pack_bf16x2(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1]));
-                            w.y = pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3]));
-                            w.z = pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5]));
-                            w.w = pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7]));
-                            dst[j] = w;
+                            for (int j = 0; j < 4; ++j) {
+                                uint4 w;
+                                w.x = pack_bf16x2(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1]));
+                                w.y = pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3]));
+                                w.z = pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5]));
+                                w.w = pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7]));
+                                dst[j] = w;
+                            }
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                if (col0 + j < N)
+                                    drow[col0 + j] = __float2bfloat16_rn(__uint_as_float(v[j]));
                         }
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (col0 + j < N)
-                                drow[col0 + j] = __float2bfloat16_rn(__uint_as_float(v[j]));
                     }
                 }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
         }
     }
 
@@ -428,8 +428,7 @@ cudaError_t launch_pair(const Mxfp4Args &a, int num_sms, const ErrCtx &err, cuda
     int clusters = num_sms / 2;
     if (tiles < clusters)
         clusters = tiles;
-    cudaLaunchConfig_t cfg;
-    std::memset(&cfg, 0, sizeof cfg);
+    cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * clusters);
     cfg.blockDim = dim3(pair_threads(ACC_BUFS));
     cfg.dynamicSmemBytes = C::SMEM;

@@ -666,8 +666,7 @@ cudaError_t launch_pair(const TcArgs &a, const Tc2Epi &epi, const ErrCtx &err, c
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), SMEM);
     if (e != cudaSuccess)
         return e;
-    cudaLaunchConfig_t cfg;
-    std::memset(&cfg, 0, sizeof cfg);
+    cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * a.pairs);
     cfg.blockDim = dim3(tc2_threads(EPI));
     cfg.dynamicSmemBytes = SMEM;
