@@ -66,7 +66,9 @@ struct MxPairCfg {
     static constexpr int SMEM_STAGES = (230 * 1024 - 2048) / STAGE_BYTES;
     static constexpr int STAGES0 = TMEM_STAGES < SMEM_STAGES ? TMEM_STAGES : SMEM_STAGES;
     static constexpr int STAGES = STAGES0 > 8 ? 8 : STAGES0;
-    static constexpr int BAR_BYTES = (3 * STAGES + 4) * 8 + 16;
+    static constexpr int CODE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int SCALE_BYTES = SFA_BYTES + SFB_BYTES;
+    static constexpr int BAR_BYTES = (4 * STAGES + 4) * 8 + 16;
     static constexpr int SMEM = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
 };
 
@@ -105,7 +107,8 @@ __global__ void __launch_bounds__(pair_threads(ACC_BUFS), 1)
     uint64_t *tfull = empty + STAGES;
     uint64_t *tempty = tfull + 2;
     uint64_t *sready = tempty + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sready + STAGES);
+    uint64_t *sfull = sready + STAGES;                 // the stage's scales have landed
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sfull + STAGES);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -120,6 +123,7 @@ __global__ void __launch_bounds__(pair_threads(ACC_BUFS), 1)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
             mbar_init(&sready[s], 1);
+            mbar_init(&sfull[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
@@ -161,7 +165,7 @@ __global__ void __launch_bounds__(pair_threads(ACC_BUFS), 1)
             };
             auto sfb_row = [&](int tn, int kb) { return tn * num_kb * (C::SFB_BYTES / 256) + kb * (C::SFB_BYTES / 256); };
             auto load_scales = [&](int st, int tm, int tn, int kb) {
-                const uint32_t b0 = mapa_shared(smem_u32(&full[st]), 0);
+                const uint32_t b0 = mapa_shared(smem_u32(&sfull[st]), 0);
                 tma_load_2d_pair(sfA + st * C::SFA_BYTES, &tmSA, b0, 0, sfa_row(tm, kb));
                 tma_load_2d_pair(sfB + st * C::SFB_BYTES, &tmSB, b0, 0, sfb_row(tn, kb));
             };
@@ -188,8 +192,12 @@ __global__ void __launch_bounds__(pair_threads(ACC_BUFS), 1)
                         ok = false;
                         break;
                     }
-                    if (rank == 0)
-                        mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
+                    if (rank == 0) {
+                        // codes and scales complete on separate barriers, so
+                        // that the scale copies need not wait for the codes
+                        mbar_arrive_expect_tx(&full[stage], 2 * C::CODE_BYTES);
+                        mbar_arrive_expect_tx(&sfull[stage], 2 * C::SCALE_BYTES);
+                    }
                     const uint32_t bar0 = mapa_shared(smem_u32(&full[stage]), 0);
                     tma_load_2d_pair(tA + stage * C::A_BYTES, &tmA, bar0, kb * kBKBytes,
                                      tm * kBM + static_cast<int>(rank) * kHalfM);
@@ -274,7 +282,7 @@ __global__ void __launch_bounds__(pair_threads(ACC_BUFS), 1)
             bool ok = true;
             for (int t = cluster; t < num_tiles && ok; t += nclusters) {
                 for (int kb = 0; kb < num_kb; ++kb) {
-                    if (!mbar_wait_cluster(&full[stage], phase, err, abort_flag, kSiteMmaFull)) {
+                    if (!mbar_wait_cluster(&sfull[stage], phase, err, abort_flag, kSiteMmaFull)) {
                         ok = false;
                         break;
                     }
