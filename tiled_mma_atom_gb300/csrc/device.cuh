@@ -360,9 +360,14 @@ __device__ __forceinline__ void cluster_sync()
 }
 
 // Arrive on an mbarrier given by its shared::cluster address (any CTA).
+// Used by epilogue warps to hand an accumulator back to the MMA issuer: what
+// they must have finished is their tcgen05.ld, which tcgen05.wait::ld has
+// already completed, so the release is CTA-scoped.  A cluster-scoped release
+// would also wait for the warp's earlier global stores to be ordered at
+// cluster scope, about a microsecond per arrive on the issuer's critical path.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
 {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+    asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                  : "memory");
 }
 
