@@ -34,11 +34,22 @@
 //
 // Warps: 0 weight producer; 1 MMA issuer and TMEM owner; 2..5 epilogue (one
 // per TMEM lane quarter); 6..13 converters (two per lane quarter, each 32 of
-// a K block's 64 weight columns); 14 A' producer.  Shared memory: a ring of
-// packed-weight slots (128-byte swizzled rows), released once the
-// converters have read them, and a ring of A' slots (two boxes each),
-// released by the MMAs.  TMEM: two accumulators (columns 0-255) and four
-// converted weight buffers (256-511).
+// a K block's 64 weight columns); 14 A' producer; 15 second MMA issuer.
+// Shared memory: a ring of packed-weight slots (128-byte swizzled rows),
+// released once the converters have read them, and a ring of A' slots (two
+// boxes each), one per converted weight buffer.  TMEM: the accumulators
+// (columns 0-255) and four converted weight buffers (256-511); unit i of a
+// CTA uses buffer and A' slot i mod 4.  The converters mark a buffer ready
+// once its weights are stored and its A' has landed; the MMA that read it
+// frees buffer and slot with one commit.
+// Two MMA issuers (when 2 mp <= 64): at these shapes an MMA takes ~25 ns
+// and a single issuing thread's per-unit wait, fence and commit leave the
+// tensor pipe idle for about as long again; with units alternating between
+// two threads, each with its own pair of accumulators, one thread's
+// bookkeeping overlaps the other's MMAs.  The epilogue adds the two
+// accumulators: each partial sum is an integer multiple of 2^-9 below 2^13
+// in magnitude, exact in fp32, and is converted to an integer before the
+// addition.
 #include <cuda_fp8.h>
 
 #include <cstring>
@@ -54,45 +65,51 @@ constexpr int kPackedBytes = kTileN * kBK / 2;    // 16 KB: 128 rows x 128 bytes
 constexpr int kABoxK = 128;                       // k (bytes) per A' box row: one 128-byte swizzle span
 constexpr int kWCols = kBK / 4;                   // TMEM columns of E4M3 weights per K block (64)
 constexpr int kWBufs = 4;
-constexpr int kAccCols = 128;                     // one accumulator: 2 mp <= 128 columns
-constexpr int kWCol0 = 2 * kAccCols;              // first weight column
+constexpr int kAccRegion = 256;                   // accumulators: 2 x 128 columns (one issuer) or 4 x 64 (two)
+constexpr int kWCol0 = kAccRegion;                // first weight column
 constexpr int kTmemCols = 512;
 constexpr int kMaxMP = 64;
 constexpr int kConvWarps = 8;
 constexpr int kFirstConvWarp = 6;
 constexpr int kAProducerWarp = kFirstConvWarp + kConvWarps;       // 14
-constexpr int kThreads = 32 * (kAProducerWarp + 1);               // 480
+constexpr int kSecondMmaWarp = kAProducerWarp + 1;                // 15
+constexpr int kThreads = 32 * (kSecondMmaWarp + 1);               // 512
 constexpr int kMaxWStages = 16;
-constexpr int kMaxAStages = 8;
 constexpr int kSmemBudget = 225 * 1024;
 
 static_assert(kWCol0 + kWBufs * kWCols <= kTmemCols, "TMEM columns");
 static_assert(kTileN == kW4TileN && kBK == kW4BK, "pre-shuffled block shape");
 
 // Two rings in shared memory: weight slots (16 KB of packed weights each),
-// freed as soon as the converters have read them, and A' slots (two boxes
-// of 2 mp rows x 128 bytes), freed when the MMAs that read them complete.
+// freed as soon as the converters have read them, and kWBufs A' slots (two
+// boxes of 2 mp rows x 128 bytes), freed with the converted weight buffer
+// of the same unit.
 __host__ __device__ constexpr int a_box_bytes(int mp) { return 2 * mp * kABoxK; }
 __host__ __device__ constexpr int a_stage_bytes(int mp) { return 2 * a_box_bytes(mp); }
-__host__ __device__ constexpr int bar_bytes() { return (2 * kMaxWStages + 2 * kMaxAStages + 2 * kWBufs + 4) * 8 + 16; }
-int a_stages_for(int mp)
-{
-    const int s = 48 * 1024 / a_stage_bytes(mp);
-    return s < 3 ? 3 : (s > kMaxAStages ? kMaxAStages : s);
-}
+__host__ __device__ constexpr int bar_bytes() { return (2 * kMaxWStages + 3 * kWBufs + 8) * 8 + 16; }
 int w_stages_for(int mp)
 {
-    const int s = (kSmemBudget - bar_bytes() - 1024 - a_stages_for(mp) * a_stage_bytes(mp)) / kPackedBytes;
+    const int s = (kSmemBudget - bar_bytes() - 1024 - kWBufs * a_stage_bytes(mp)) / kPackedBytes;
     return s > kMaxWStages ? kMaxWStages : s;
 }
 int smem_for(int mp)
 {
-    return w_stages_for(mp) * kPackedBytes + a_stages_for(mp) * a_stage_bytes(mp) + bar_bytes() + 1024;
+    return w_stages_for(mp) * kPackedBytes + kWBufs * a_stage_bytes(mp) + bar_bytes() + 1024;
 }
+// Two MMA issuers when their four accumulators (2 mp columns each) fit in
+// the accumulator region, else one with two.
+int issuers_for(int mp) { return 4 * 2 * mp <= kAccRegion ? 2 : 1; }
 
 __device__ __forceinline__ int seg_end(int kb0, int KB, int64_t left)
 {
     return left < static_cast<int64_t>(KB - kb0) ? kb0 + static_cast<int>(left) : KB;
+}
+
+// Units go to the MMA issuers by the CTA-local unit index mod niss.  Does
+// issuer j take one of the local units [i0, i1) (a non-empty range)?
+__device__ __forceinline__ bool issuer_has(int64_t i0, int64_t i1, int j, int niss)
+{
+    return niss == 1 || i1 - i0 >= 2 || static_cast<int>(i0 & 1) == j;
 }
 
 // Programmatic dependent launch: the pre-pass lets the GEMM start early;
@@ -237,7 +254,7 @@ __global__ void __launch_bounds__(kSplitThreads)
 __global__ void __launch_bounds__(kThreads, 1)
     w4a8_skinny_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmA,
                        const uint8_t *__restrict__ Bs, int32_t *__restrict__ D, int64_t ldd,
-                       const int32_t *__restrict__ R, int M, int N, int K, int mp, int wstages, int astages,
+                       const int32_t *__restrict__ R, int M, int N, int K, int mp, int wstages, int niss,
                        ErrCtx err)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -245,15 +262,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);   // weight ring
     const int abytes = a_stage_bytes(mp);
     uint8_t *aring = smem + wstages * kPackedBytes;                     // A' ring
-    uint64_t *wfull = reinterpret_cast<uint64_t *>(aring + astages * abytes);
+    uint64_t *wfull = reinterpret_cast<uint64_t *>(aring + kWBufs * abytes);
     uint64_t *wempty = wfull + kMaxWStages;
     uint64_t *afull = wempty + kMaxWStages;
-    uint64_t *aempty = afull + kMaxAStages;
-    uint64_t *cready = aempty + kMaxAStages;                   // converted weights in TMEM (converters)
-    uint64_t *cfree = cready + kWBufs;                         // converted weights consumed (MMA commit)
-    uint64_t *tfull = cfree + kWBufs;
-    uint64_t *tempty = tfull + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
+    uint64_t *cready = afull + kWBufs;                         // weights in TMEM and A' landed (converters)
+    uint64_t *cfree = cready + kWBufs;                         // buffer and A' slot consumed (MMA commit)
+    uint64_t *tfull = cfree + kWBufs;                          // per accumulator
+    uint64_t *tempty = tfull + 4;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 4);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -269,15 +285,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&wfull[s], 1);
             mbar_init(&wempty[s], kConvWarps);                 // every converter warp
         }
-        for (int s = 0; s < astages; ++s) {
-            mbar_init(&afull[s], 1);
-            mbar_init(&aempty[s], 1);                          // the MMA commit
-        }
         for (int b = 0; b < kWBufs; ++b) {
+            mbar_init(&afull[b], 1);
             mbar_init(&cready[b], kConvWarps);
-            mbar_init(&cfree[b], 1);
+            mbar_init(&cfree[b], 1);                           // the MMA commit
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < 4; ++b) {
             mbar_init(&tfull[b], 1);
             mbar_init(&tempty[b], 4);
         }
@@ -332,9 +345,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             griddep_wait();                                  // A' comes from the pre-pass
             int64_t issued = 0;
             for (int64_t i = 0; i < n_units; ++i) {
-                const int as = static_cast<int>(i % astages);
-                const uint32_t ph = static_cast<uint32_t>((i / astages) & 1);
-                if (!mbar_wait(&aempty[as], ph ^ 1u, err, abort_flag, kSiteProducerEmpty))
+                // slot i mod kWBufs is free once the MMAs of unit i - kWBufs
+                // (which used the same converted weight buffer) completed
+                const int as = static_cast<int>(i % kWBufs);
+                const uint32_t ph = static_cast<uint32_t>((i / kWBufs) & 1);
+                if (!mbar_wait(&cfree[as], ph ^ 1u, err, abort_flag, kSiteProducerEmpty))
                     break;
                 const int kb = static_cast<int>((u_begin + i) % KB);
                 uint8_t *st = aring + as * abytes;
@@ -343,54 +358,59 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_2d_hint(st + abox, &tmA, &afull[as], kb * kBK + kABoxK, 0, keep_a);
                 ++issued;
             }
-            for (int64_t i = issued - 1; i >= 0 && i >= issued - astages; --i)
-                mbar_wait(&afull[i % astages], static_cast<uint32_t>((i / astages) & 1), err, nullptr, kSiteDrain);
+            for (int64_t i = issued - 1; i >= 0 && i >= issued - kWBufs; --i)
+                mbar_wait(&afull[i % kWBufs], static_cast<uint32_t>((i / kWBufs) & 1), err, nullptr, kSiteDrain);
         }
-    } else if (warp == 1) {
-        if (lane == 0) {
-            // ------------------------------------------------ MMA issuer
-            // MMA A = converted weights (TMEM, 128 rows), MMA B = A' (2 mp rows)
+    } else if (warp == 1 || warp == kSecondMmaWarp) {
+        const int j = warp == 1 ? 0 : 1;                       // issuer index
+        if (lane == 0 && j < niss) {
+            // ------------------------------------------------ MMA issuers
+            // MMA A = converted weights (TMEM, 128 rows), MMA B = A' (2 mp
+            // rows).  Issuer j takes the units i with i mod niss = j into its
+            // accumulators 2 j, 2 j + 1 (alternating over the segments it
+            // has units in).
             const uint32_t idesc = idesc_e4m3_f32(kTileN, 2 * mp);
-            int as = 0, wb = 0, seg = 0;
-            uint32_t aphase = 0, wphase = 0;
+            const int acc_cols = kAccRegion / (2 * niss);
+            int64_t i0 = 0;                                    // local index of the segment's first unit
+            int nseg = 0;                                      // segments this issuer took part in
             bool ok = true;
-            for (int64_t u = u_begin; u < u_end && ok; ++seg) {
+            for (int64_t u = u_begin; u < u_end && ok;) {
                 const int kb0 = static_cast<int>(u % KB);
                 const int kb1 = seg_end(kb0, KB, u_end - u);
-                const int acc = seg & 1;
-                if (!mbar_wait(&tempty[acc], ((seg >> 1) & 1) ^ 1u, err, abort_flag, kSiteMmaTmemEmpty))
-                    break;
-                tc_fence_after();
-                const uint32_t d_tmem = tmem_base + acc * kAccCols;
-                for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!mbar_wait(&afull[as], aphase, err, abort_flag, kSiteMmaFull) ||
-                        !mbar_wait(&cready[wb], wphase, err, abort_flag, kSiteMmaFull)) {
-                        ok = false;
+                const int64_t i1 = i0 + (kb1 - kb0);
+                if (issuer_has(i0, i1, j, niss)) {
+                    const int acc = 2 * j + (nseg & 1);
+                    if (!mbar_wait(&tempty[acc], ((nseg >> 1) & 1) ^ 1u, err, abort_flag, kSiteMmaTmemEmpty))
                         break;
-                    }
                     tc_fence_after();
-                    const uint32_t a_src = tmem_base + kWCol0 + wb * kWCols;
-                    const uint64_t bdesc0 = sdesc_kmajor_sw128(smem_u32(aring + as * abytes));
-                    const uint64_t bdesc1 = sdesc_kmajor_sw128(smem_u32(aring + as * abytes + abox));
+                    const uint32_t d_tmem = tmem_base + acc * acc_cols;
+                    bool first = true;
+                    for (int64_t i = i0 + ((niss == 2 && static_cast<int>(i0 & 1) != j) ? 1 : 0); i < i1; i += niss) {
+                        const int wb = static_cast<int>(i % kWBufs);
+                        if (!mbar_wait(&cready[wb], static_cast<uint32_t>((i / kWBufs) & 1), err, abort_flag,
+                                       kSiteMmaFull)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t a_src = tmem_base + kWCol0 + wb * kWCols;
+                        const uint64_t bdesc0 = sdesc_kmajor_sw128(smem_u32(aring + wb * abytes));
+                        const uint64_t bdesc1 = sdesc_kmajor_sw128(smem_u32(aring + wb * abytes + abox));
 #pragma unroll
-                    for (int k = 0; k < kBK / 32; ++k) {
-                        const uint64_t bdesc = (k < 4 ? bdesc0 : bdesc1) + static_cast<uint64_t>(((k & 3) * 32) >> 4);
-                        mma_e4m3_ts(d_tmem, a_src + 8 * k, bdesc, idesc, (kb != kb0) || (k != 0));
+                        for (int k = 0; k < kBK / 32; ++k) {
+                            const uint64_t bdesc =
+                                (k < 4 ? bdesc0 : bdesc1) + static_cast<uint64_t>(((k & 3) * 32) >> 4);
+                            mma_e4m3_ts(d_tmem, a_src + 8 * k, bdesc, idesc, !first || (k != 0));
+                        }
+                        first = false;
+                        mma_commit(&cfree[wb]);
                     }
-                    mma_commit(&aempty[as]);
-                    mma_commit(&cfree[wb]);
-                    if (++as == astages) {
-                        as = 0;
-                        aphase ^= 1u;
-                    }
-                    if (++wb == kWBufs) {
-                        wb = 0;
-                        wphase ^= 1u;
-                    }
+                    if (!ok)
+                        break;
+                    mma_commit(&tfull[acc]);
+                    ++nseg;
                 }
-                if (!ok)
-                    break;
-                mma_commit(&tfull[acc]);
+                i0 = i1;
                 u += kb1 - kb0;
             }
         }
@@ -433,8 +453,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st32_wait(t_row + wb * kWCols, out);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&cready[wb]);
+            // the MMA issuer waits on this barrier alone: the unit's A'
+            // arrival is folded into it
+            int landed = 1;
+            if (lane == 0) {
+                landed = mbar_wait(&afull[wb], wphase, err, abort_flag, kSiteMmaFull) ? 1 : 0;
+                if (landed)
+                    mbar_arrive(&cready[wb]);
+            }
+            if (!__shfl_sync(0xFFFFFFFFu, landed, 0))
+                break;
             if (++ws == wstages) {
                 ws = 0;
                 phase ^= 1u;
@@ -446,44 +474,58 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // -------------------------------------------------- epilogue
-        // thread owns weight row n_local = 32 q + lane; TMEM columns m and
-        // mp + m hold the hi and lo sums of activation row m (scaled 2^-9)
+        // thread owns weight row n_local = 32 q + lane; in each accumulator
+        // TMEM columns m and mp + m hold the hi and lo sums of activation row
+        // m (scaled 2^-9); the issuers' shares of a segment are added
         const int q = warp & 3;
         const int n_local = q * 32 + lane;
+        const int acc_cols = kAccRegion / (2 * niss);
         griddep_wait();                                        // R comes from the pre-pass
-        int seg = 0;
-        for (int64_t u = u_begin; u < u_end; ++seg) {
+        int64_t i0 = 0;
+        int nseg0 = 0, nseg1 = 0;                              // segments each issuer took part in
+        bool ok = true;
+        for (int64_t u = u_begin; u < u_end && ok;) {
             const int tile = static_cast<int>(u / KB);
             const int kb0 = static_cast<int>(u % KB);
             const int kb1 = seg_end(kb0, KB, u_end - u);
+            const int64_t i1 = i0 + (kb1 - kb0);
             u += kb1 - kb0;
-            const int acc = seg & 1;
-            if (!mbar_wait(&tfull[acc], (seg >> 1) & 1, err, abort_flag, kSiteEpiTmemFull))
-                break;
-            __syncwarp();
-            tc_fence_after();
-            const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccCols;
             int32_t v[kMaxMP];
 #pragma unroll
-            for (int ch = 0; ch < kMaxMP / 16; ++ch) {
-                if (ch * 16 < mp) {
-                    uint32_t h[16], l[16];
-                    tmem_ld16(tb + ch * 16, h);
-                    tmem_ld16(tb + mp + ch * 16, l);
-#pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        v[ch * 16 + j] = 16 * __float2int_rn(__uint_as_float(h[j]) * 512.0f) +
-                                         __float2int_rn(__uint_as_float(l[j]) * 512.0f);
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        v[ch * 16 + j] = 0;
+            for (int m = 0; m < kMaxMP; ++m)
+                v[m] = 0;
+            for (int j = 0; j < niss; ++j) {
+                if (!issuer_has(i0, i1, j, niss))
+                    continue;
+                const int ns = j == 0 ? nseg0++ : nseg1++;
+                const int acc = 2 * j + (ns & 1);
+                if (!mbar_wait(&tfull[acc], (ns >> 1) & 1, err, abort_flag, kSiteEpiTmemFull)) {
+                    ok = false;
+                    break;
                 }
+                __syncwarp();
+                tc_fence_after();
+                const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * acc_cols;
+#pragma unroll
+                for (int ch = 0; ch < kMaxMP / 16; ++ch) {
+                    if (ch * 16 < mp) {
+                        uint32_t h[16], l[16];
+                        tmem_ld16(tb + ch * 16, h);
+                        tmem_ld16(tb + mp + ch * 16, l);
+#pragma unroll
+                        for (int t = 0; t < 16; ++t)
+                            v[ch * 16 + t] += 16 * __float2int_rn(__uint_as_float(h[t]) * 512.0f) +
+                                              __float2int_rn(__uint_as_float(l[t]) * 512.0f);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&tempty[acc]);
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&tempty[acc]);
+            i0 = i1;
+            if (!ok)
+                break;
 
             const int n = tile * kTileN + n_local;
             int32_t *d = D + n;
@@ -583,7 +625,7 @@ cudaError_t launch_w4a8_skinny(const W4a8SkinnyArgs &a, const ErrCtx &err, cudaS
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return e;
-    const int wstages = w_stages_for(a.mp), astages = a_stages_for(a.mp);
+    const int wstages = w_stages_for(a.mp), niss = issuers_for(a.mp);
     const int smem = smem_for(a.mp);
     if ((e = ensure_smem_attr(reinterpret_cast<const void *>(w4a8_skinny_kernel), smem)) != cudaSuccess)
         return e;
@@ -599,7 +641,7 @@ cudaError_t launch_w4a8_skinny(const W4a8SkinnyArgs &a, const ErrCtx &err, cudaS
     cfg.numAttrs = 1;
     note_launch();
     return cudaLaunchKernelEx(&cfg, w4a8_skinny_kernel, a.tmB, a.tmA, a.Bs, a.D, a.ldd,
-                              static_cast<const int32_t *>(a.R), a.M, a.N, a.K, a.mp, wstages, astages, err);
+                              static_cast<const int32_t *>(a.R), a.M, a.N, a.K, a.mp, wstages, niss, err);
 }
 
 }  // namespace tmg
