@@ -147,20 +147,21 @@ __device__ __forceinline__ void mma_e4m3_ts(uint32_t d_tmem, uint32_t a_tmem, ui
 }
 
 // registers -> TMEM: 32 lanes x 32 consecutive columns (thread i writes lane
-// base + i), then wait until the stores are done.
-__device__ __forceinline__ void tmem_st32_wait(uint32_t taddr, const uint32_t (&r)[32])
+// base + i); complete once tmem_wait_st returns.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32])
 {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
         "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
-        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};\n\t"
-        "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
         "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
         "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
         "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
         "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
         : "memory");
 }
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Position of k (mod 8) inside its group of 8 in the MMA's k order: the even
 // k first, then the odd k (the order the converters emit).
@@ -283,11 +284,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < wstages; ++s) {
             mbar_init(&wfull[s], 1);
-            mbar_init(&wempty[s], kConvWarps);                 // every converter warp
+            mbar_init(&wempty[s], kConvWarps / 2);             // the converter group of the unit
         }
         for (int b = 0; b < kWBufs; ++b) {
             mbar_init(&afull[b], 1);
-            mbar_init(&cready[b], kConvWarps);
+            mbar_init(&cready[b], kConvWarps / 2);
             mbar_init(&cfree[b], 1);                           // the MMA commit
         }
         for (int b = 0; b < 4; ++b) {
@@ -416,41 +417,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp >= kFirstConvWarp) {
         // ------------------------------------------------- converters
-        // Thread = weight row r of the tile = TMEM lane r.  Per K block it
-        // reads 4 of its row's 8 swizzled 16-byte chunks (the half `half`
-        // of the block's k), releases the staging slot, spreads the
-        // nibbles to offset-binary E4M3 bytes and stores 32 TMEM columns.
+        // Thread = weight row r of the tile = TMEM lane r.  The two groups
+        // of four warps (one per TMEM lane quarter in each) take alternate
+        // units: per unit a warp reads its row's 8 swizzled 16-byte chunks,
+        // releases the staging slot, spreads the nibbles to offset-binary
+        // E4M3 bytes and stores the unit's 64 TMEM columns of its lane
+        // quarter with one wait, so each warp's per-unit waits and store
+        // latency are paid once per two units.
         const int q = warp & 3;
-        const int half = (warp - kFirstConvWarp) >> 2;
+        const int grp = (warp - kFirstConvWarp) >> 2;
         const int r = q * 32 + lane;
-        const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + kWCol0 + 32 * half;
-        int ws = 0, wb = 0;
+        const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + kWCol0;
+        int ws = grp, wb = grp;                                // unit i: slot i mod wstages, buffer i mod kWBufs
         uint32_t phase = 0, wphase = 0;
-        for (int64_t u = u_begin; u < u_end; ++u) {
+        for (int64_t i = grp; i < n_units; i += 2) {
             if (!mbar_wait(&wfull[ws], phase, err, abort_flag, kSiteMmaFull) ||
                 !mbar_wait(&cfree[wb], wphase ^ 1u, err, abort_flag, kSiteProducerEmpty))
                 break;
             tc_fence_after();
             const uint8_t *src = smem + ws * kPackedBytes + r * 128;
-            uint4 w[4];
+            uint4 w[8];
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-                w[i] = *reinterpret_cast<const uint4 *>(src + (((4 * half + i) ^ (r & 7)) << 4));
+            for (int c = 0; c < 8; ++c)
+                w[c] = *reinterpret_cast<const uint4 *>(src + ((c ^ (r & 7)) << 4));
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&wempty[ws]);
-            uint32_t out[32];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t words[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+            for (int hh = 0; hh < 2; ++hh) {
+                uint32_t out[32];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint32_t y = words[j] ^ 0x88888888u;   // offset binary: v + 8
-                    out[8 * i + 2 * j] = y & 0x0F0F0F0Fu;       // even k
-                    out[8 * i + 2 * j + 1] = (y >> 4) & 0x0F0F0F0Fu;   // odd k
+                for (int c = 0; c < 4; ++c) {
+                    const uint4 v = w[4 * hh + c];
+                    const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const uint32_t y = words[j] ^ 0x88888888u;   // offset binary: v + 8
+                        out[8 * c + 2 * j] = y & 0x0F0F0F0Fu;       // even k
+                        out[8 * c + 2 * j + 1] = (y >> 4) & 0x0F0F0F0Fu;   // odd k
+                    }
                 }
+                tmem_st32(t_row + wb * kWCols + 32 * hh, out);
             }
-            tmem_st32_wait(t_row + wb * kWCols, out);
+            tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             // the MMA issuer waits on this barrier alone: the unit's A'
@@ -463,12 +472,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!__shfl_sync(0xFFFFFFFFu, landed, 0))
                 break;
-            if (++ws == wstages) {
-                ws = 0;
+            if ((ws += 2) >= wstages) {
+                ws -= wstages;
                 phase ^= 1u;
             }
-            if (++wb == kWBufs) {
-                wb = 0;
+            if ((wb += 2) >= kWBufs) {
+                wb -= kWBufs;
                 wphase ^= 1u;
             }
         }
