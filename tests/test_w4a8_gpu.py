@@ -81,6 +81,23 @@ def test_w4a8_decode_exact(tmg, M, N, K):
     assert np.array_equal(_run(tmg, A, B), oracle.gemm_w4a8(A.numpy(), B.numpy(), M, N, K))
 
 
+@pytest.mark.parametrize("M", [16, 17, 40])
+def test_w4a8_decode_several_units_per_cta(tmg, M):
+    """512 (tile, K block) units on 152 CTAs: each CTA's run of 3-4 units
+    crosses tile boundaries, so runs split into segments of 1 to 4 units.
+    With M <= 32 two MMA issuers take alternate units (a segment of one
+    unit leaves one of them out); with M = 40 one issuer takes all.  Exact
+    against the oracle, pre-shuffled and row-major weights alike."""
+    N, K = 2048, 8192
+    A, B = inputs.random_int8(M, K, 741), inputs.random_int4_packed(N, K, 742)
+    ref = oracle.gemm_w4a8(A.numpy(), B.numpy(), M, N, K)
+    assert np.array_equal(_run(tmg, A, B), ref)
+    Bs = tmg.w4a8_preshuffle(B.to(DEV))
+    D = tmg.gemm_w4a8_preshuffled(A.to(DEV), Bs, N)
+    tmg.check()
+    assert np.array_equal(D.cpu().numpy(), ref)
+
+
 def test_w4a8_decode_extreme_values_at_max_k(tmg):
     """K = 32768, the decode kernel's limit, with the values that drive its
     fp32 column sums furthest from zero: the kernel splits a = 16 hi + lo
