@@ -42,11 +42,12 @@
 // CTA uses buffer and A' slot i mod 4.  The converters mark a buffer ready
 // once its weights are stored and its A' has landed; the MMA that read it
 // frees buffer and slot with one commit.
-// Two MMA issuers (when 2 mp <= 64): at these shapes an MMA takes ~25 ns
-// and a single issuing thread's per-unit wait, fence and commit leave the
-// tensor pipe idle for about as long again; with units alternating between
-// two threads, each with its own pair of accumulators, one thread's
-// bookkeeping overlaps the other's MMAs.  The epilogue adds the two
+// Two MMA issuers: at these shapes an MMA takes ~25 ns and a single issuing
+// thread's per-unit wait, fence and commit leave the tensor pipe idle for
+// about as long again; with units alternating between two threads, each
+// with its own accumulators, one thread's bookkeeping overlaps the other's
+// MMAs.  Each issuer has two accumulators (alternating over segments, so
+// the epilogue of one overlaps the next) when 2 mp <= 64, else one.  The epilogue adds the two
 // accumulators: each partial sum is an integer multiple of 2^-9 below 2^13
 // in magnitude, exact in fp32, and is converted to an integer before the
 // addition.
@@ -96,21 +97,27 @@ int smem_for(int mp)
 {
     return w_stages_for(mp) * kPackedBytes + kWBufs * a_stage_bytes(mp) + bar_bytes() + 1024;
 }
-// Two MMA issuers when their four accumulators (2 mp columns each) fit in
-// the accumulator region, else one with two.
-int issuers_for(int mp) { return 4 * 2 * mp <= kAccRegion ? 2 : 1; }
+constexpr int kIssuers = 2;
+// Accumulators per MMA issuer: two when all four (2 mp columns each) fit in
+// the accumulator region, else one.
+int accs_for(int mp) { return 2 * kIssuers * 2 * mp <= kAccRegion ? 2 : 1; }
 
 __device__ __forceinline__ int seg_end(int kb0, int KB, int64_t left)
 {
     return left < static_cast<int64_t>(KB - kb0) ? kb0 + static_cast<int>(left) : KB;
 }
 
-// Units go to the MMA issuers by the CTA-local unit index mod niss.  Does
-// issuer j take one of the local units [i0, i1) (a non-empty range)?
-__device__ __forceinline__ bool issuer_has(int64_t i0, int64_t i1, int j, int niss)
+// Units go to the two MMA issuers by the parity of the CTA-local unit
+// index.  Does issuer j take one of the local units [i0, i1) (non-empty)?
+__device__ __forceinline__ bool issuer_has(int64_t i0, int64_t i1, int j)
 {
-    return niss == 1 || i1 - i0 >= 2 || static_cast<int>(i0 & 1) == j;
+    return i1 - i0 >= 2 || static_cast<int>(i0 & 1) == j;
 }
+
+// Accumulator of issuer j for the s-th segment it takes part in, and the
+// parity of that accumulator's s-th use (nacc accumulators per issuer).
+__device__ __forceinline__ int acc_index(int j, int s, int nacc) { return j * nacc + (nacc == 2 ? (s & 1) : 0); }
+__device__ __forceinline__ uint32_t acc_phase(int s, int nacc) { return static_cast<uint32_t>((nacc == 2 ? s >> 1 : s) & 1); }
 
 // Programmatic dependent launch: the pre-pass lets the GEMM start early;
 // the GEMM waits for the pre-pass's results only where it reads them.
@@ -255,7 +262,7 @@ __global__ void __launch_bounds__(kSplitThreads)
 __global__ void __launch_bounds__(kThreads, 1)
     w4a8_skinny_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmA,
                        const uint8_t *__restrict__ Bs, int32_t *__restrict__ D, int64_t ldd,
-                       const int32_t *__restrict__ R, int M, int N, int K, int mp, int wstages, int niss,
+                       const int32_t *__restrict__ R, int M, int N, int K, int mp, int wstages, int nacc,
                        ErrCtx err)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -364,14 +371,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1 || warp == kSecondMmaWarp) {
         const int j = warp == 1 ? 0 : 1;                       // issuer index
-        if (lane == 0 && j < niss) {
+        if (lane == 0) {
             // ------------------------------------------------ MMA issuers
             // MMA A = converted weights (TMEM, 128 rows), MMA B = A' (2 mp
-            // rows).  Issuer j takes the units i with i mod niss = j into its
+            // rows).  Issuer j takes the units i with i mod 2 = j into its
             // accumulators 2 j, 2 j + 1 (alternating over the segments it
             // has units in).
             const uint32_t idesc = idesc_e4m3_f32(kTileN, 2 * mp);
-            const int acc_cols = kAccRegion / (2 * niss);
+            const int acc_cols = kAccRegion / (kIssuers * nacc);
             int64_t i0 = 0;                                    // local index of the segment's first unit
             int nseg = 0;                                      // segments this issuer took part in
             bool ok = true;
@@ -379,14 +386,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int kb0 = static_cast<int>(u % KB);
                 const int kb1 = seg_end(kb0, KB, u_end - u);
                 const int64_t i1 = i0 + (kb1 - kb0);
-                if (issuer_has(i0, i1, j, niss)) {
-                    const int acc = 2 * j + (nseg & 1);
-                    if (!mbar_wait(&tempty[acc], ((nseg >> 1) & 1) ^ 1u, err, abort_flag, kSiteMmaTmemEmpty))
+                if (issuer_has(i0, i1, j)) {
+                    const int acc = acc_index(j, nseg, nacc);
+                    if (!mbar_wait(&tempty[acc], acc_phase(nseg, nacc) ^ 1u, err, abort_flag, kSiteMmaTmemEmpty))
                         break;
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + acc * acc_cols;
                     bool first = true;
-                    for (int64_t i = i0 + ((niss == 2 && static_cast<int>(i0 & 1) != j) ? 1 : 0); i < i1; i += niss) {
+                    for (int64_t i = i0 + (static_cast<int>(i0 & 1) != j ? 1 : 0); i < i1; i += kIssuers) {
                         const int wb = static_cast<int>(i % kWBufs);
                         if (!mbar_wait(&cready[wb], static_cast<uint32_t>((i / kWBufs) & 1), err, abort_flag,
                                        kSiteMmaFull)) {
@@ -488,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // m (scaled 2^-9); the issuers' shares of a segment are added
         const int q = warp & 3;
         const int n_local = q * 32 + lane;
-        const int acc_cols = kAccRegion / (2 * niss);
+        const int acc_cols = kAccRegion / (kIssuers * nacc);
         griddep_wait();                                        // R comes from the pre-pass
         int64_t i0 = 0;
         int nseg0 = 0, nseg1 = 0;                              // segments each issuer took part in
@@ -503,12 +510,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int m = 0; m < kMaxMP; ++m)
                 v[m] = 0;
-            for (int j = 0; j < niss; ++j) {
-                if (!issuer_has(i0, i1, j, niss))
+            for (int j = 0; j < kIssuers; ++j) {
+                if (!issuer_has(i0, i1, j))
                     continue;
                 const int ns = j == 0 ? nseg0++ : nseg1++;
-                const int acc = 2 * j + (ns & 1);
-                if (!mbar_wait(&tfull[acc], (ns >> 1) & 1, err, abort_flag, kSiteEpiTmemFull)) {
+                const int acc = acc_index(j, ns, nacc);
+                if (!mbar_wait(&tfull[acc], acc_phase(ns, nacc), err, abort_flag, kSiteEpiTmemFull)) {
                     ok = false;
                     break;
                 }
@@ -634,7 +641,7 @@ cudaError_t launch_w4a8_skinny(const W4a8SkinnyArgs &a, const ErrCtx &err, cudaS
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return e;
-    const int wstages = w_stages_for(a.mp), niss = issuers_for(a.mp);
+    const int wstages = w_stages_for(a.mp), nacc = accs_for(a.mp);
     const int smem = smem_for(a.mp);
     if ((e = ensure_smem_attr(reinterpret_cast<const void *>(w4a8_skinny_kernel), smem)) != cudaSuccess)
         return e;
@@ -650,7 +657,7 @@ cudaError_t launch_w4a8_skinny(const W4a8SkinnyArgs &a, const ErrCtx &err, cudaS
     cfg.numAttrs = 1;
     note_launch();
     return cudaLaunchKernelEx(&cfg, w4a8_skinny_kernel, a.tmB, a.tmA, a.Bs, a.D, a.ldd,
-                              static_cast<const int32_t *>(a.R), a.M, a.N, a.K, a.mp, wstages, niss, err);
+                              static_cast<const int32_t *>(a.R), a.M, a.N, a.K, a.mp, wstages, nacc, err);
 }
 
 }  // namespace tmg
