@@ -73,17 +73,35 @@ def build(force: bool = False, verbose: bool = False, extra: list[str] | None = 
     return LIB
 
 
+def _code_only(text: str) -> str:
+    """C++ source without its comments and blank lines: what the compiler
+    sees, so that editing a comment does not disown a profile."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    out = []
+    for line in text.splitlines():
+        # drop a // comment unless the // sits inside a string literal
+        cut = line.find("//")
+        if cut >= 0 and line.count('"', 0, cut) % 2 == 0:
+            line = line[:cut]
+        line = line.rstrip()
+        if line:
+            out.append(line)
+    return "\n".join(out)
+
+
 def source_hash(name) -> str:
-    """sha256 of csrc/<name> (a file name or a list of them) plus the shared
-    device header (identifies the kernel a profile was taken from)."""
+    """sha256 of the code (comments stripped) of csrc/<name> (a file name or a
+    list of them) plus the shared device header: identifies the kernel a
+    profile was taken from."""
     import hashlib
     h = hashlib.sha256()
     names = [name] if isinstance(name, str) else list(name)
     for f in names + ["device.cuh"]:
         p = os.path.join(CSRC, f)
         if os.path.exists(p):
-            with open(p, "rb") as fh:
-                h.update(fh.read())
+            with open(p, encoding="utf-8") as fh:
+                h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

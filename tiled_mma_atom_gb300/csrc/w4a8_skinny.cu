@@ -33,8 +33,9 @@
 // adds the row-sum correction.  No partial buffers, counters or fix-up.
 //
 // Warps: 0 weight producer; 1 MMA issuer and TMEM owner; 2..5 epilogue (one
-// per TMEM lane quarter); 6..13 converters (two per lane quarter, each 32 of
-// a K block's 64 weight columns); 14 A' producer; 15 second MMA issuer.
+// per TMEM lane quarter); 6..13 converters (two groups of four, one warp per
+// lane quarter in each, taking alternate units); 14 A' producer; 15 second
+// MMA issuer.
 // Shared memory: a ring of packed-weight slots (128-byte swizzled rows),
 // released once the converters have read them, and a ring of A' slots (two
 // boxes each), one per converted weight buffer.  TMEM: the accumulators
