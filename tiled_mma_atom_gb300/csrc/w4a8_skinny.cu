@@ -376,8 +376,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ------------------------------------------------ MMA issuers
             // MMA A = converted weights (TMEM, 128 rows), MMA B = A' (2 mp
             // rows).  Issuer j takes the units i with i mod 2 = j into its
-            // accumulators 2 j, 2 j + 1 (alternating over the segments it
-            // has units in).
+            // own accumulators (acc_index: one, or two alternating over the
+            // segments it has units in).
             const uint32_t idesc = idesc_e4m3_f32(kTileN, 2 * mp);
             const int acc_cols = kAccRegion / (kIssuers * nacc);
             int64_t i0 = 0;                                    // local index of the segment's first unit
