@@ -9,9 +9,13 @@ One step is one GEMM of the chosen workload through the library's C ABI
 synthetic data resident in HBM; before every timed step L2 is flushed (a
 512 MiB write, then a 320 MiB read so the written lines are written back
 outside the timing) unless the inputs alone exceed twice the L2, and the step
-itself is timed with CUDA events on the launching stream.  Rank 0 prints ONE JSON line.  Unless --no-extra is given, the line
-also carries a measurement of every other workload ("workloads"), each with
-its own roofline entry.
+itself is timed with CUDA events on the launching stream.  Rank 0 prints ONE
+JSON line.  Unless --no-extra is given, the line also carries a measurement
+of every other workload: the "next" rows ("workloads", each with its own
+roofline entry) and, as its last key, a compact block for the five
+configurations C1-C5 ("configs": median time, throughput, roofline fraction,
+kernel, and the CPU oracle timed on a bounded row sample of the same
+configuration on the host cores).
 
 --impl reference times the CPU oracle (oracle/, fp64, OpenMP on the host
 cores) on bounded row samples of the same workload: the reference arm.
@@ -35,6 +39,10 @@ sys.path.insert(0, ROOT)
 
 METRIC = "GEMM TFLOP/s and % of GB300 dense tensor (or HBM) roofline, 1 GPU"
 HEADLINE = "bf16_4096"
+# the five configurations the metric is quoted on, in order (C1..C5)
+CONFIGS = ("fp32_128", "bf16_1024", "bf16_4096", "skinny_16x28672x8192", "mxfp4_8192")
+# seconds of oracle work per configuration in the compact per-configuration block
+CONFIG_CPU_BUDGET = 3.0
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # nominal dense ratios fp4 : bf16 and fp8 : bf16 on GB300 (13.5, 4.5 : 2.25 PFLOP/s)
 FP4_OVER_BF16 = 13.5 / 2.25
@@ -340,6 +348,29 @@ def unit_value(w, seconds):
     return w.flops / seconds / 1e12     # TFLOP/s
 
 
+def sig(x, n=4):
+    """x rounded to n significant digits (keeps the JSON line short)."""
+    if x is None or x == 0:
+        return x
+    from math import floor, log10
+    return round(x, max(0, n - 1 - int(floor(log10(abs(x))))))
+
+
+def config_entry(w, ms_list, rl, cpu):
+    """One compact entry of the per-configuration block: GPU mean time per
+    call (the throughput and roofline fraction use it; the median is beside
+    it), plus the oracle's own timing."""
+    mean = statistics.mean(ms_list)
+    e = {"tflops": sig(unit_value(w, mean * 1e-3)), "ms": sig(mean), "ms_median": sig(statistics.median(ms_list)),
+         "bound": rl["bound"],
+         "achieved": sig(rl["achieved"]), "unit": rl["unit"], "frac": sig(rl["frac"], 3),
+         "kernel": rl["kernel"]}
+    if cpu is not None:
+        v, secs, rows, thr = cpu
+        e["cpu"] = {"tflops": sig(v, 3), "s": sig(secs, 3), "rows": f"{rows}/{w.M}", "cores": thr}
+    return e
+
+
 # ------------------------------------------------------------ CPU oracle
 
 def oracle_sample(w, budget_s):
@@ -513,28 +544,48 @@ def main():
     e2e_s, h2d, d2h = time_e2e(w, max(3, min(20, args.steps)), dev, stream)
     e2e_s = max_over_ranks(pg, e2e_s)
 
-    extra = {}
+    # the other workloads: the "next" rows first (compact), then the five
+    # configurations, each with the oracle timed on the host cores; the
+    # per-configuration block is the last key of the line
+    cpu, cpu_head = None, None
+    if rank == 0 and world == 1:
+        cpu_head = oracle_sample(w, args.cpu_budget)
+        v, secs, rows, thr = cpu_head
+        cpu = {"value": v, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+               "sample": f"first {rows} of {w.M} rows of D ({rows}x{w.N}x{w.K}) in {secs:.1f} s, fp64"}
+
+    extra, configs = {}, {}
     if not args.no_extra:
         for name, ow in inputs.WORKLOADS.items():
-            if name == w.name:
+            if name == w.name or name in CONFIGS:
                 continue
             try:
                 steps = 400 if ow.flops < 1e11 else 100
                 oms, ol, _, _, _ = time_device(ow, steps, 5, dev, stream, flush)
                 per = statistics.mean(oms)
-                extra[name] = {"value": unit_value(ow, per * 1e-3), "unit": "TFLOP/s",
-                               "ms_median": statistics.median(oms), "ms_mean": per,
-                               "l2": l2_policy(ow)[1],
-                               "launches_per_step": ol / steps,
-                               "roofline": roofline(ow, per, peaks, peak_kind, traffic)}
+                orl = roofline(ow, per, peaks, peak_kind, traffic)
+                extra[name] = {"tflops": sig(unit_value(ow, per * 1e-3)), "ms_median": sig(statistics.median(oms)),
+                               "launches_per_step": ol / steps, "flushed": l2_policy(ow)[0],
+                               "roofline": {k: sig(v) if isinstance(v, float) else v for k, v in orl.items()
+                                            if k not in ("peak_source", "nominal_peak")}}
             except Exception as e:  # report, do not hide
                 extra[name] = {"unavailable": f"{type(e).__name__}: {e}"}
-
-    cpu = None
-    if rank == 0 and world == 1:
-        v, s, rows, thr = oracle_sample(w, args.cpu_budget)
-        cpu = {"value": v, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
-               "sample": f"first {rows} of {w.M} rows of D ({rows}x{w.N}x{w.K}) in {s:.1f} s, fp64"}
+        for i, name in enumerate(CONFIGS):
+            ow = inputs.WORKLOADS[name]
+            key = f"C{i + 1}_{name}"
+            try:
+                if name == w.name:
+                    oms, orl = ms, rl
+                else:
+                    steps = 400 if ow.flops < 1e11 else 100
+                    oms, _, _, _, _ = time_device(ow, steps, 5, dev, stream, flush)
+                    orl = roofline(ow, statistics.mean(oms), peaks, peak_kind, traffic)
+                cpu_c = None
+                if rank == 0 and world == 1:
+                    cpu_c = cpu_head if name == w.name else oracle_sample(ow, CONFIG_CPU_BUDGET)
+                configs[key] = config_entry(ow, oms, orl, cpu_c)
+            except Exception as e:  # report, do not hide
+                configs[key] = {"unavailable": f"{type(e).__name__}: {e}"}
 
     if rank == 0:
         line = {
@@ -559,6 +610,7 @@ def main():
             "peaks": {"source": peak_kind, **peaks},
             "timed_wall_s": wall,
             "workloads": extra,
+            "configs": configs,
         }
         print(json.dumps(line), flush=True)
     if pg is not None:

@@ -6,12 +6,16 @@
 // r·BN/2.. of the B codes, the scales of its own 128 A rows and the scales
 // of all BN B rows (its tensor core multiplies its 128 rows by every column
 // of the tile, so it needs every B scale).  All four loads of both CTAs are
-// TMA copies completing on CTA 0's `full` barrier.  Warp roles: 0 TMA
-// producer; 1 MMA issuer (CTA 0); 2 scale copier (CTA 0), which moves each
-// stage's scales of both CTAs into their TMEM with tcgen05.cp.cta_group::2
-// copies and commits to the stage's `sready` barrier; the rest epilogue.
-// Keeping the copies out of the MMA lane's instruction stream lets it queue
-// MMAs back to back (measured on MXFP4 8192³: 218 -> 209 µs).  The scales
+// TMA copies completing on CTA 0's barriers: the codes on `full`, the scales
+// on `sfull`.  Warp roles: 0 TMA producer; 1 MMA issuer (CTA 0); 2 scale
+// copier (CTA 0), which moves each stage's scales of both CTAs into their
+// TMEM with tcgen05.cp.cta_group::2 copies and commits to the stage's `full`
+// barrier; the rest epilogue.  `full` thus completes when the code tiles
+// have landed (the producer's byte count) and the scales are in TMEM (the
+// copier's commit), and the MMA issuer waits once per K block.  Copies issued
+// from the MMA lane itself, just before the MMAs that read them, put each
+// copy's latency in front of those MMAs (MXFP4 8192³: 180 -> 248 µs); from
+// a separate warp they run ahead.  The scales
 // travel in the compact chunk order (1 KB per 128 rows and K block) and are
 // replicated across the TMEM lane quarters by the copies themselves
 // (32x128b.warpx4): a quarter of the L2 traffic and of the relayout output
@@ -19,10 +23,16 @@
 // (209 -> 197 µs).  TMEM per CTA: the accumulator(s) plus, per stage,
 // 8 columns of A scales and 8·ceil(BN/128) columns of B scales (B rows 0-127
 // in the first 4 columns of each K-block group, rows 128.. in the next 4).
-// A stage's scale columns are rewritten only after its `full` barrier
-// completes again, which needs the stage's `empty` commit — issued after
-// the MMAs that read those columns — so the copier never overwrites scales
-// still in use.
+// A stage's scale columns are rewritten only after its `sfull` barrier
+// completes again, which needs the producer to have refilled the stage after
+// its `empty` commit — issued after the MMAs that read those columns — so
+// the copier never overwrites scales still in use.
+//
+// Every role waits on its own CTA's barriers with CTA-scope acquire: a wait
+// at cluster scope cost the producer enough to slow the whole kernel (MXFP4
+// 8192³: 180 -> 172 µs).  The epilogue stores D with 32-byte vector stores
+// when rows allow it, so each store writes whole 32-byte sectors (172 ->
+// 166 µs: half-sector stores doubled the write traffic into L2).
 //
 // The FlyDSL pages express the product with scaled MFMA/WMMA atoms (E8M0
 // scale per 32 K elements: "FlyDSL Kernel Authoring Skill", §6, MX-scaled
@@ -68,7 +78,7 @@ struct MxPairCfg {
     static constexpr int STAGES = STAGES0 > 8 ? 8 : STAGES0;
     static constexpr int CODE_BYTES = A_BYTES + B_BYTES;
     static constexpr int SCALE_BYTES = SFA_BYTES + SFB_BYTES;
-    static constexpr int BAR_BYTES = (4 * STAGES + 4) * 8 + 16;
+    static constexpr int BAR_BYTES = (3 * STAGES + 4) * 8 + 16;
     static constexpr int SMEM = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
 };
 
@@ -106,8 +116,7 @@ __global__ void __launch_bounds__(pair_threads(ACC_BUFS), 1)
     uint64_t *empty = full + STAGES;
     uint64_t *tfull = empty + STAGES;
     uint64_t *tempty = tfull + 2;
-    uint64_t *sready = tempty + 2;
-    uint64_t *sfull = sready + STAGES;                 // the stage's scales have landed
+    uint64_t *sfull = tempty + 2;                      // the stage's scales have landed in shared memory
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sfull + STAGES);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -120,9 +129,8 @@ __global__ void __launch_bounds__(pair_threads(ACC_BUFS), 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&full[s], 1);
+            mbar_init(&full[s], 2);      // the producer's byte count + the copier's commit
             mbar_init(&empty[s], 1);
-            mbar_init(&sready[s], 1);
             mbar_init(&sfull[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -188,7 +196,7 @@ __global__ void __launch_bounds__(pair_threads(ACC_BUFS), 1)
                 for (int kb = 0; kb < num_kb; ++kb) {
                     if (!scales_ready && issued == STAGES)
                         release_deferred();
-                    if (!mbar_wait_cluster(&empty[stage], phase ^ 1u, err, abort_flag, kSiteProducerEmpty)) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, err, abort_flag, kSiteProducerEmpty)) {
                         ok = false;
                         break;
                     }
@@ -236,17 +244,13 @@ __global__ void __launch_bounds__(pair_threads(ACC_BUFS), 1)
             for (int t = cluster; t < num_tiles && ok; t += nclusters, ++local) {
                 const int acc = local % ACC_BUFS;
                 const uint32_t use_phase = (local / ACC_BUFS) & 1;
-                if (!mbar_wait_cluster(&tempty[acc], use_phase ^ 1u, err, abort_flag, kSiteMmaTmemEmpty))
+                if (!mbar_wait(&tempty[acc], use_phase ^ 1u, err, abort_flag, kSiteMmaTmemEmpty))
                     break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
                 for (int kb = 0; kb < num_kb; ++kb) {
-                    if (!mbar_wait_cluster(&full[stage], phase, err, abort_flag, kSiteMmaFull)) {
-                        ok = false;
-                        break;
-                    }
-                    // the stage's scales are in TMEM once `sready` completes
-                    if (!mbar_wait_cluster(&sready[stage], phase, err, abort_flag, kSiteMmaFull)) {
+                    // the stage's codes are in shared memory, its scales in TMEM
+                    if (!mbar_wait(&full[stage], phase, err, abort_flag, kSiteMmaFull)) {
                         ok = false;
                         break;
                     }
@@ -282,7 +286,7 @@ __global__ void __launch_bounds__(pair_threads(ACC_BUFS), 1)
             bool ok = true;
             for (int t = cluster; t < num_tiles && ok; t += nclusters) {
                 for (int kb = 0; kb < num_kb; ++kb) {
-                    if (!mbar_wait_cluster(&sfull[stage], phase, err, abort_flag, kSiteMmaFull)) {
+                    if (!mbar_wait(&sfull[stage], phase, err, abort_flag, kSiteMmaFull)) {
                         ok = false;
                         break;
                     }
@@ -312,7 +316,7 @@ __global__ void __launch_bounds__(pair_threads(ACC_BUFS), 1)
                                                                                    sb * kSfBlock + c * kSfChunk)));
                         }
                     }
-                    mma_commit_pair(&sready[stage], 0x1);
+                    mma_commit_pair(&full[stage], 0x1);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -356,7 +360,11 @@ __global__ void __launch_bounds__(pair_threads(ACC_BUFS), 1)
 #pragma unroll
                     for (int c = 0; c < HALF / 32; ++c) {
                         const int col0 = tn * BN + h * HALF + c * 32;
-                        if (vec_ok && col0 + 32 <= N) {
+                        if (vec_ok == 2 && col0 + 32 <= N) {
+                            const uint32_t *w = packed + c * 16;
+                            st_global_v8(drow + col0, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+                            st_global_v8(drow + col0 + 16, w[8], w[9], w[10], w[11], w[12], w[13], w[14], w[15]);
+                        } else if (vec_ok && col0 + 32 <= N) {
                             uint4 *dst = reinterpret_cast<uint4 *>(drow + col0);
 #pragma unroll
                             for (int j = 0; j < 4; ++j)
@@ -450,7 +458,9 @@ cudaError_t launch_pair(const Mxfp4Args &a, int num_sms, const ErrCtx &err, cuda
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    const int vec_ok = (a.N % 8 == 0) && ((reinterpret_cast<uintptr_t>(a.D) & 15u) == 0);
+    // row stores: 2 = 32-byte vectors (rows start on 32-byte boundaries), 1 = 16-byte vectors, 0 = scalars
+    const uintptr_t d_addr = reinterpret_cast<uintptr_t>(a.D);
+    const int vec_ok = (a.N % 16 == 0 && (d_addr & 31u) == 0) ? 2 : (a.N % 8 == 0 && (d_addr & 15u) == 0) ? 1 : 0;
     note_launch();
     e = cudaLaunchKernelEx(&cfg, kern, a.tmA, a.tmB, a.tmSA, a.tmSB, static_cast<__nv_bfloat16 *>(a.D), a.M, a.N,
                            a.K, vec_ok, err);
