@@ -62,6 +62,11 @@ KERNEL_OF = {"fp32_128": "ffma_gemm_kernel", "bf16_1024": "tc_bf16_kernel",
              "w4a8_8192": "tc2_gemm_kernel", "w4a8_16x28672x8192": "w4a8_skinny_kernel"}
 
 
+# kernel that a forced path runs (bench.py --path)
+PATH_KERNEL = {"ffma": "ffma_gemm_kernel", "skinny_ffma": "skinny_ffma_kernel", "skinny": "skinny_tc_kernel",
+               "tc_single": "tc_bf16_kernel", "tc_pair": "tc2_gemm_kernel"}
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -205,7 +210,7 @@ def accumulate_note(w):
     return "exact integer: fp32 within K segments of 8192, int32 across them"
 
 
-def make_call(w, dev_in, out, stream):
+def make_call(w, dev_in, out, stream, path="auto"):
     import tiled_mma_atom_gb300 as tmg
     if w.dtype == "mxfp4":
         A, B, sA, sB = dev_in
@@ -221,6 +226,8 @@ def make_call(w, dev_in, out, stream):
         return lambda: tmg.gemm_fused(A, B, out, scale_a=sa, scale_b=sb, bias=bias,
                                       epilogue=w.epilogue, stream=stream)
     A, B = dev_in
+    if path != "auto":
+        return lambda: tmg.gemm(A, B, out, path=path, stream=stream)
     if w.a_mn_major or w.b_mn_major:
         la = ((w.M, w.K), (1, w.M)) if w.a_mn_major else None
         lb = ((w.N, w.K), (1, w.N)) if w.b_mn_major else None
@@ -267,14 +274,15 @@ def roofline(w, ms_per_launch, peaks, peak_kind, traffic):
     return r
 
 
-def time_device(w, steps, warmup, dev, stream, flush):
-    """Per-step CUDA-event time of one library call (inputs in HBM)."""
+def time_device(w, steps, warmup, dev, stream, flush, path="auto"):
+    """Per-step CUDA-event time of one library call (inputs in HBM); `path`
+    forces a kernel family for dense f32/bf16 workloads (tmg_gemm_ex)."""
     import torch
     import tiled_mma_atom_gb300 as tmg
     host, dev_in = device_inputs(w, dev)
     dt = {"f32": torch.float32, "w4a8": torch.int32}.get(w.dtype, torch.bfloat16)
     out = torch.empty((w.M, w.N), dtype=dt, device=dev)
-    call = make_call(w, dev_in, out, stream)
+    call = make_call(w, dev_in, out, stream, path)
     do_flush, _ = l2_policy(w)
     with torch.cuda.stream(stream):
         for _ in range(warmup):
@@ -498,6 +506,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
+    ap.add_argument("--path", default="auto",
+                    help="kernel family for a dense f32/bf16 workload (auto, ffma, tc, skinny, skinny_ffma, "
+                         "tc_single, tc_pair): profiling aid, with --no-extra")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -530,7 +541,7 @@ def main():
     clocks.start()
     time.sleep(0.05)
     t_wall = time.perf_counter()
-    ms, launches, host, dev_in, out = time_device(w, args.steps, args.warmup, dev, stream, flush)
+    ms, launches, host, dev_in, out = time_device(w, args.steps, args.warmup, dev, stream, flush, args.path)
     wall = time.perf_counter() - t_wall
     torch.cuda.synchronize()
     barrier(pg)
@@ -540,6 +551,9 @@ def main():
     ms_per_step = kernel_ms_max / args.steps
     value = aggregate_tflops(world, w.flops, args.steps, kernel_ms_max)
     rl = roofline(w, kernel_ms / args.steps, peaks, peak_kind, traffic)
+    if args.path != "auto":
+        rl["kernel"] = PATH_KERNEL.get(args.path, args.path)
+        rl["traffic"] = None
 
     e2e_s, h2d, d2h = time_e2e(w, max(3, min(20, args.steps)), dev, stream)
     e2e_s = max_over_ranks(pg, e2e_s)
@@ -599,6 +613,7 @@ def main():
                        **({"epilogue": w.epilogue} if w.epilogue else {}),
                        "l2": l2_policy(w)[1],
                        "timing": "CUDA events around each library call on its stream",
+                       **({"path": args.path} if args.path != "auto" else {}),
                        "ms_median": statistics.median(ms), "ms_min": min(ms),
                        "parallelism": f"{world} independent replica(s)"},
             "roofline": rl,

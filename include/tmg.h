@@ -274,9 +274,15 @@ tmg_status tmg_gemm_mxfp4(const void *A, const void *B, const void *scaleA,
  * Its split-K partial sums and tile counters live in one 8 MiB array in the
  * library's static device memory, which every GPU that loads the library
  * holds until the process exits.  No call allocates or frees memory.  The
+ * array holds partial sums for every SM up to M = 48; for M from 49 to 64 it
+ * holds them for 127 CTAs, so those calls run on at most 127 of the SMs and
+ * split K differently from the allocating call: equal results within
+ * rounding, not bit for bit (for M <= 48 the two are bit-identical).  The
  * first call on a device looks up that array's device address (once per
- * device, with the device current); make that first call before any stream
- * capture.  Every call shares the one array and it keeps the last call's
+ * device, with the device current) and keeps it for the life of the
+ * process: make that first call before any stream capture, and do not use
+ * the library on a device after cudaDeviceReset.  Every call shares the one
+ * array and it keeps the last call's
  * contents: each call clears the counters it uses with an asynchronous
  * memset on `stream` before its kernel.  Calls whose GPU work overlaps (on
  * different streams, or from different threads) race on the array and give

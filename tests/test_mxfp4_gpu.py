@@ -76,6 +76,37 @@ def test_mxfp4_per_block_scales_bit_exact(tmg, variant):
     parity.check_exact_bf16(parity.bf16_bits(D), _ref(A, B, sA, sB, M, N, K))
 
 
+def test_mxfp4_per_block_scales_partial_scale_group(tmg, variant):
+    """K = 2560 is ten K blocks of 256: the pair kernel copies raw scales four
+    K blocks at a time, so the last copy of each tile holds two.  Per-block
+    scales 2^-1..2^1 keep the result exact (as above); ragged M and N put
+    rows past the end of both operands into the last tiles."""
+    M, N, K = 392, 328, 2560
+    A = inputs.random_fp4_codes(M, K, 13)
+    B = inputs.random_fp4_codes(N, K, 14)
+    sA = inputs.random_e8m0(M, K, 15, lo=-1, hi=1)
+    sB = inputs.random_e8m0(N, K, 16, lo=-1, hi=1)
+    D = _run(tmg, A, B, sA, sB)
+    parity.check_exact_bf16(parity.bf16_bits(D), _ref(A, B, sA, sB, M, N, K))
+
+
+@pytest.mark.parametrize("M,N,K", [(2048, 2304, 4096), (512, 640, 8192)])
+def test_mxfp4_partial_wave_exact(tmg, variant, M, N, K):
+    """Problems whose tiles do not fill whole waves of CTA pairs (fewer tiles
+    than pairs; a long K at 512 x 640 x 8192).  Unit scales keep every sum
+    exact (multiples of 1/4 of magnitude at most 36 K < 2^19), so D must
+    equal RNE_bf16 of the exact sum bit for bit, and a second call must give
+    the same bits."""
+    A = inputs.random_fp4_codes(M, K, 17)
+    B = inputs.random_fp4_codes(N, K, 18)
+    sA = torch.full((M, K // 32), 127, dtype=torch.uint8)
+    sB = torch.full((N, K // 32), 127, dtype=torch.uint8)
+    D = _run(tmg, A, B, sA, sB)
+    parity.check_exact_bf16(parity.bf16_bits(D), _ref(A, B, sA, sB, M, N, K))
+    D2 = _run(tmg, A, B, sA, sB)
+    assert torch.equal(D, D2)
+
+
 def test_mxfp4_one_hot_scale_locates_each_block(tmg, variant):
     """All codes 1.0; one row of A (or of B) gets scale 2^1 on a single K
     block.  Each output of that row (column) must be K + 32, all others K."""
@@ -97,7 +128,7 @@ def test_mxfp4_one_hot_scale_locates_each_block(tmg, variant):
         assert torch.equal(D, want), (side, idx, blk)
 
 
-@pytest.mark.parametrize("M,N,K", [(300, 200, 1024), (256, 640, 256), (520, 392, 768)])
+@pytest.mark.parametrize("M,N,K", [(300, 200, 1024), (256, 640, 256), (520, 392, 768), (512, 384, 1536)])
 def test_mxfp4_random_vs_oracle(tmg, variant, M, N, K):
     A = inputs.random_fp4_codes(M, K, 7)
     B = inputs.random_fp4_codes(N, K, 8)
