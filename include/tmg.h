@@ -40,6 +40,14 @@
  * bounded; a wait that runs out sets the device error word and the kernel
  * returns early — tmg_check() then reports TMG_ERR_TIMEOUT.
  * tmg_last_error() gives a message for the calling thread's last failure.
+ *
+ * Debug aids.  TMG_LOG=1 in the environment makes every GEMM call print the
+ * kernel family, tile and schedule it chose (one line on stderr).  The
+ * library also builds as libtmg_debug.so (same ABI; build.py
+ * --debug-bounds): there every store of D and every access to split-K
+ * scratch is checked against its buffer, an out-of-range offset skips the
+ * access and sets the device error word, and tmg_check() then reports
+ * TMG_ERR_BOUNDS.
  */
 #ifndef TMG_H
 #define TMG_H
@@ -56,7 +64,8 @@ typedef enum {
     TMG_ERR_INVALID_ARG = 1,
     TMG_ERR_UNSUPPORTED = 2,
     TMG_ERR_CUDA = 3,
-    TMG_ERR_TIMEOUT = 4
+    TMG_ERR_TIMEOUT = 4,
+    TMG_ERR_BOUNDS = 5      /* debug build only: a kernel caught an out-of-range offset */
 } tmg_status;
 
 /* Element type.  tmg_gemm: the type of A, B and D (identical), F32 or BF16.
@@ -311,6 +320,16 @@ void tmg_set_wait_budget_ns(uint64_t ns);
  * that the next tmg_check() returns TMG_ERR_TIMEOUT.  Exercises the bounded
  * wait of every kernel without any GPU fault or hang. */
 tmg_status tmg_debug_wait_timeout(uint64_t budget_ns, void *stream);
+
+/* Debug build only (libtmg_debug.so): launch one tiny kernel whose bounds
+ * check sees an offset one past the end of a buffer — it accesses nothing —
+ * so that the next tmg_check() returns TMG_ERR_BOUNDS.  Exercises the
+ * reporting of the bounds checks without any out-of-range access.  The
+ * normal build returns TMG_ERR_UNSUPPORTED. */
+tmg_status tmg_debug_bounds_probe(void *stream);
+
+/* 1 in the debug build (bounds-checked kernels), else 0. */
+int tmg_debug_build(void);
 
 /* Number of kernels the library has launched in this process. */
 uint64_t tmg_launch_count(void);

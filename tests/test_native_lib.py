@@ -147,3 +147,12 @@ def test_w4a8_preshuffle_rejects_bad_arguments_before_device_work(native):
     assert lib.tmg_gemm_w4a8_preshuffled(16, 16, 16, 4, 4, 48, None) == native.ERR_INVALID_ARG
     assert lib.tmg_gemm_w4a8_preshuffled(16, 24, 16, 4, 4, 64, None) == native.ERR_INVALID_ARG
     assert lib.tmg_gemm_w4a8_preshuffled(16, 16, 16, 0, 4, 64, None) == native.OK
+
+
+def test_normal_build_has_no_bounds_checks(native):
+    """The normal build compiles the bounds checks out: it says so, and its
+    probe entry point refuses (without touching a GPU)."""
+    L = native.lib()
+    assert L.tmg_debug_build() == 0
+    assert L.tmg_debug_bounds_probe(None) == native.ERR_UNSUPPORTED
+    assert "debug build" in L.tmg_last_error().decode()

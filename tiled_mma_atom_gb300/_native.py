@@ -11,9 +11,11 @@ import os
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libtmg.so")
+# the same library built with bounds checks in its kernels (build.py --debug-bounds)
+DEBUG_LIB_PATH = os.path.join(HERE, "libtmg_debug.so")
 
-OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = 0, 1, 2, 3, 4
-STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "CUDA", 4: "TIMEOUT"}
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_BOUNDS = 0, 1, 2, 3, 4, 5
+STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "CUDA", 4: "TIMEOUT", 5: "BOUNDS"}
 F32, BF16, E4M3 = 0, 1, 2
 EPILOGUES = {"none": 0, "bias": 1, "bias_relu": 2, "bias_silu": 3, "bias_gelu": 4}
 PATHS = {"auto": 0, "ffma": 1, "tc": 2, "skinny": 3, "skinny_ffma": 4, "tc_single": 5,
@@ -22,7 +24,8 @@ PATHS = {"auto": 0, "ffma": 1, "tc": 2, "skinny": 3, "skinny_ffma": 4, "tc_singl
 # Every function include/tmg.h declares.
 EXPORTS = ("tmg_gemm", "tmg_gemm_ex", "tmg_gemm_host", "tmg_gemm_fused", "tmg_gemm_w4a8",
            "tmg_gemm_w4a8_preshuffled", "tmg_w4a8_preshuffle", "tmg_w4a8_preshuffled_bytes", "tmg_gemm_mxfp4", "tmg_gemm_skinny_noalloc", "tmg_check", "tmg_last_error",
-           "tmg_set_wait_budget_ns", "tmg_debug_wait_timeout", "tmg_launch_count",
+           "tmg_set_wait_budget_ns", "tmg_debug_wait_timeout", "tmg_debug_bounds_probe", "tmg_debug_build",
+           "tmg_launch_count",
            "tmg_version", "tmg_shutdown")
 
 
@@ -64,6 +67,14 @@ def make_layout(shape, stride) -> Layout:
 _lib = None
 
 
+def use_library(path: str) -> None:
+    """Bind every later call to another build of the same ABI (the debug
+    build, DEBUG_LIB_PATH); the next lib() call loads it."""
+    global _lib, LIB_PATH
+    LIB_PATH = path
+    _lib = None
+
+
 def lib():
     """Load libtmg.so once; raise TmgError if it has not been built."""
     global _lib
@@ -103,6 +114,10 @@ def lib():
     L.tmg_set_wait_budget_ns.restype = None
     L.tmg_debug_wait_timeout.argtypes = [ctypes.c_uint64, P]
     L.tmg_debug_wait_timeout.restype = ctypes.c_int
+    L.tmg_debug_bounds_probe.argtypes = [P]
+    L.tmg_debug_bounds_probe.restype = ctypes.c_int
+    L.tmg_debug_build.argtypes = []
+    L.tmg_debug_build.restype = ctypes.c_int
     L.tmg_launch_count.argtypes = []
     L.tmg_launch_count.restype = ctypes.c_uint64
     L.tmg_version.argtypes = []

@@ -17,6 +17,10 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libtmg.so")
+# the debug build: every store of D and every access to split-K scratch in
+# the kernels checked against its buffer (-DTMG_DEBUG_BOUNDS)
+BUILD_DEBUG = os.path.join(HERE, "_build_debug")
+LIB_DEBUG = os.path.join(HERE, "libtmg_debug.so")
 SOURCES = ["api.cu", "ffma.cu", "tc_bf16.cu", "tc2_bf16.cu", "tc2_fused.cu", "skinny.cu", "mxfp4.cu",
            "mxfp4_pair.cu", "pack.cu", "w4a8.cu", "w4a8_skinny.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -38,22 +42,24 @@ def _deps() -> list[str]:
     return files
 
 
-def stale() -> bool:
-    if not os.path.exists(LIB):
+def stale(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(f) > t for f in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None) -> str:
-    if not force and not stale():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None,
+          debug_bounds: bool = False) -> str:
+    lib, bdir = (LIB_DEBUG, BUILD_DEBUG) if debug_bounds else (LIB, BUILD)
+    if not force and not stale(lib):
+        return lib
+    os.makedirs(bdir, exist_ok=True)
     cc = nvcc()
-    extra = extra or []
+    extra = (extra or []) + (["-DTMG_DEBUG_BOUNDS"] if debug_bounds else [])
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(bdir, src.replace(".cu", ".o"))
         cmd = [cc] + FLAGS + extra + ["-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -64,13 +70,13 @@ def build(force: bool = False, verbose: bool = False, extra: list[str] | None = 
 
     with cf.ThreadPoolExecutor(max_workers=min(len(SOURCES), os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [cc] + ARCH + ["-shared", "-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 def _code_only(text: str) -> str:
@@ -108,4 +114,4 @@ def source_hash(name) -> str:
 if __name__ == "__main__":
     v = "-v" in sys.argv
     extra = ["-Xptxas", "-v"] if "--ptxas-v" in sys.argv else None
-    print(build(force=True, verbose=v or bool(extra), extra=extra))
+    print(build(force=True, verbose=v or bool(extra), extra=extra, debug_bounds="--debug-bounds" in sys.argv))

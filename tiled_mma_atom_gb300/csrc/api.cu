@@ -77,6 +77,30 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn g_encode = nullptr;
 
+// TMG_LOG=1 (any value but "0"): one line on stderr per GEMM call naming the
+// kernel family, tile and schedule the dispatch chose.
+bool log_on()
+{
+    static const bool on = [] {
+        const char *v = getenv("TMG_LOG");
+        return v && *v && strcmp(v, "0") != 0;
+    }();
+    return on;
+}
+
+void log_choice(const char *fmt, ...) __attribute__((format(printf, 1, 2)));
+void log_choice(const char *fmt, ...)
+{
+    if (!log_on())
+        return;
+    char buf[400];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    fprintf(stderr, "tmg: %s\n", buf);
+}
+
 tmg_status fail(tmg_status st, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
 tmg_status fail(tmg_status st, const char *fmt, ...)
 {
@@ -481,6 +505,12 @@ tmg_status run_tc(const DeviceState &ds, const TcPlan &p, void *D, int64_t K, in
         if ((st = encode_d_store(a, D, p.M, p.N, p.ldd)) != TMG_OK)
             return st;
     }
+    if (pair)
+        log_choice("bf16 %dx%dx%d -> tc2_gemm_kernel (CTA pairs): 256x%d tiles, %d pairs, %d data-parallel + %d "
+                   "stream-K tiles, D stores %s", a.M, a.N, a.K, a.bn, a.pairs, a.dp_tiles, a.sk_tiles,
+                   a.d_tma ? "TMA" : "per thread");
+    else
+        log_choice("bf16 %dx%dx%d -> tc_bf16_kernel (one CTA): 128x%d tiles", a.M, a.N, a.K, a.bn);
     cudaError_t e = pair ? launch_tc2_bf16(a, ds.num_sms, err_ctx(ds), s) : launch_tc_bf16(a, ds.num_sms, err_ctx(ds), s);
     return e == cudaSuccess ? TMG_OK : cuda_fail(e, pair ? "tc2_bf16 launch" : "tc_bf16 launch");
 }
@@ -602,6 +632,10 @@ bool run_tc2_inplace(const DeviceState &ds, const void *A, const void *B, void *
         return true;
     if ((*st = encode_d_store(a, D, M, N, ldd)) != TMG_OK)
         return true;
+    log_choice("bf16 %dx%dx%d -> tc2_gemm_kernel (CTA pairs), MN-major operands read in place (A %s, B %s): "
+               "256x%d tiles, %d pairs, %d data-parallel + %d stream-K tiles", a.M, a.N, a.K,
+               (a.maj & 1) ? "MN-major" : "K-major", (a.maj & 2) ? "MN-major" : "K-major", a.bn, a.pairs, a.dp_tiles,
+               a.sk_tiles);
     const cudaError_t e = launch_tc2_bf16(a, ds.num_sms, err_ctx(ds), s);
     *st = e == cudaSuccess ? TMG_OK : cuda_fail(e, "tc2_bf16 (MN-major operands) launch");
     return true;
@@ -682,6 +716,8 @@ tmg_status run_skinny(const DeviceState &ds, const TcPlan &p, void *D, int64_t K
     a.M = static_cast<int>(p.M);
     a.N = static_cast<int>(p.N);
     a.K = static_cast<int>(K);
+    log_choice("bf16 %dx%dx%d -> skinny_tc_kernel (swap-AB, MMA N = %d): stream-K over %lld units on %d CTAs", a.M,
+               a.N, a.K, a.mp, static_cast<long long>(units), a.grid);
     cudaError_t e = launch_skinny_tc(a, err_ctx(ds), s);
     return e == cudaSuccess ? TMG_OK : cuda_fail(e, "skinny_tc launch");
 }
@@ -731,6 +767,15 @@ __global__ void wait_probe_kernel(ErrCtx err)
     __syncthreads();
     if (threadIdx.x == 0)
         mbar_wait(&bar, 0, err, nullptr, kSiteProbe);   // nothing ever arrives
+}
+
+// Checks the offset `limit` against a buffer of `limit` elements — one past
+// its end — and touches no memory either way: the debug build's check must
+// record it in the device error word.
+__global__ void bounds_probe_kernel(int64_t limit, ErrCtx err)
+{
+    if (threadIdx.x == 0)
+        (void)bounds_ok(limit, limit, err, kBndProbe);
 }
 
 }  // namespace
@@ -816,6 +861,9 @@ tmg_status tmg_gemm_ex(const void *A, const void *B, void *D, int64_t M, int64_t
         a.M = M;
         a.N = N;
         a.K = K;
+        log_choice("%s %lldx%lldx%lld -> ffma_gemm_kernel (CUDA cores, operands read through their layouts)",
+                   dt == 0 ? "f32" : "bf16", static_cast<long long>(M), static_cast<long long>(N),
+                   static_cast<long long>(K));
         cudaError_t e = launch_ffma(a, dt, ds->num_sms, err_ctx(*ds), s);
         return e == cudaSuccess ? TMG_OK : cuda_fail(e, "ffma launch");
     }
@@ -836,12 +884,17 @@ tmg_status tmg_gemm_ex(const void *A, const void *B, void *D, int64_t M, int64_t
     case TMG_PATH_PACKED_TC:
         if (dtype != TMG_BF16)
             return fail(TMG_ERR_UNSUPPORTED, "the general-layout tensor-core path takes bf16");
+        log_choice("bf16 %lldx%lldx%lld -> general layouts on the tensor cores (operands the TMA cannot read in place "
+                   "gathered through their layouts; the GEMM's own choice follows)",
+                   static_cast<long long>(M), static_cast<long long>(N), static_cast<long long>(K));
         return run_packed(*ds, A, B, D, M, N, K, la, lb, ld, s);
     case TMG_PATH_SKINNY_FFMA: {
         if (dtype != TMG_BF16 || !plan.ok || plan.M > 16 || K % 8 != 0)
             return fail(TMG_ERR_UNSUPPORTED,
                         "skinny FFMA path needs bf16, K-major A and B, K %% 8 == 0 and at most 16 rows");
         SkinnyFfmaArgs a{plan.A, plan.B, D, plan.M, plan.N, K, plan.lda, plan.ldb, plan.ldd};
+        log_choice("bf16 %lldx%lldx%lld -> skinny_ffma_kernel (CUDA cores, warp-shuffle dot products)",
+                   static_cast<long long>(plan.M), static_cast<long long>(plan.N), static_cast<long long>(K));
         cudaError_t e = launch_skinny_ffma(a, ds->num_sms, s);
         return e == cudaSuccess ? TMG_OK : cuda_fail(e, "skinny_ffma launch");
     }
@@ -993,6 +1046,9 @@ tmg_status tmg_gemm_fused(const void *A, const void *B, void *D, int64_t M, int6
         return st;
     if ((st = encode_d_store(a, D, M, N, N)) != TMG_OK)
         return st;
+    log_choice("%s %dx%dx%d fused (epilogue %d, scale_a %s, scale_b %s) -> tc2_gemm_kernel (CTA pairs): 256x%d tiles, "
+               "%d pairs, %d data-parallel + %d stream-K tiles", e4m3 ? "e4m3" : "bf16", a.M, a.N, a.K, epi.epi,
+               epi.scale_a ? "yes" : "no", epi.scale_b ? "yes" : "no", a.bn, a.pairs, a.dp_tiles, a.sk_tiles);
     cudaError_t e = launch_tc2_fused(a, epi, e4m3, err_ctx(*ds), s);
     return e == cudaSuccess ? TMG_OK : cuda_fail(e, "fused pair launch");
 }
@@ -1060,6 +1116,8 @@ tmg_status gemm_w4a8_impl(const void *A, const void *B, bool shuffled, void *D, 
         w.M = static_cast<int>(M);
         w.N = static_cast<int>(N);
         w.K = static_cast<int>(K);
+        log_choice("w4a8 %dx%dx%d -> split-activation pre-pass + w4a8_skinny_kernel (fp8 tensor cores, weights %s): "
+                   "%d CTAs", w.M, w.N, w.K, w.Bs ? "pre-shuffled" : "row-major", w.grid);
         e = launch_w4a8_skinny(w, err_ctx(*ds), s);
         return e == cudaSuccess ? TMG_OK : cuda_fail(e, "W4A8 decode launch");
     }
@@ -1100,6 +1158,9 @@ tmg_status gemm_w4a8_impl(const void *A, const void *B, bool shuffled, void *D, 
         if ((st = tc2_scratch(dev, s, a)) != TMG_OK)
             return st;
         const Tc2Epi epi{nullptr, nullptr, nullptr, kEpiNone, k0 == 0 ? 1 : 2};
+        log_choice("w4a8 %dx%dx%d, K segment at %lld -> tc2_gemm_kernel on the unpacked bf16 copies: 256x%d tiles, "
+                   "%d pairs, int32 %s", a.M, a.N, a.K, static_cast<long long>(k0), a.bn, a.pairs,
+                   k0 == 0 ? "store" : "add");
         if ((e = launch_tc2_fused(a, epi, false, err_ctx(*ds), s)) != cudaSuccess)
             return cuda_fail(e, "W4A8 GEMM launch");
     }
@@ -1232,6 +1293,10 @@ tmg_status tmg_gemm_mxfp4(const void *A, const void *B, const void *scaleA, cons
     a.M = static_cast<int>(M);
     a.N = static_cast<int>(N);
     a.K = static_cast<int>(K);
+    if (pair)
+        log_choice("mxfp4 %dx%dx%d -> scale relayout + mxfp4_pair_kernel (CTA pairs): 256x%d tiles", a.M, a.N, a.K, a.bn);
+    else
+        log_choice("mxfp4 %dx%dx%d -> scale relayout + mxfp4_kernel (one CTA): 128x128 tiles", a.M, a.N, a.K);
     cudaError_t e = pair ? launch_mxfp4_pair(a, ds->num_sms, err_ctx(*ds), s) : launch_mxfp4(a, ds->num_sms, err_ctx(*ds), s);
     return e == cudaSuccess ? TMG_OK : cuda_fail(e, pair ? "mxfp4 pair launch" : "mxfp4 launch");
 }
@@ -1298,6 +1363,8 @@ tmg_status tmg_gemm_skinny_noalloc(const void *A, const void *B, void *D, int64_
     // start at zero, the partial sums are always written before being read.
     if ((e = cudaMemsetAsync(fs.counters, 0, static_cast<size_t>(tiles) * 4 * sizeof(uint32_t), s)) != cudaSuccess)
         return cuda_fail(e, "cudaMemsetAsync(fixed skinny counters)");
+    log_choice("bf16 %dx%dx%d -> skinny_tc_kernel with the fixed scratch array (MMA N = %d) on %d CTAs", a.M, a.N,
+               a.K, a.mp, a.grid);
     e = launch_skinny_tc(a, err_ctx(*ds), s);
     return e == cudaSuccess ? TMG_OK : cuda_fail(e, "skinny_tc launch (fixed scratch)");
 }
@@ -1319,6 +1386,7 @@ tmg_status tmg_check(void *stream)
     if ((e = cudaMemcpy(&w, ds->err_word, sizeof w, cudaMemcpyDeviceToHost)) != cudaSuccess)
         return cuda_fail(e, "reading the device error word");
     if (w != 0) {
+        const bool bounds = (w & kErrBounds) != 0;
         cudaMemset(ds->err_word, 0, sizeof w);
         int dev = 0;
         cudaGetDevice(&dev);
@@ -1334,6 +1402,9 @@ tmg_status tmg_check(void *stream)
             }
         }
         cudaDeviceSynchronize();
+        if (bounds)
+            return fail(TMG_ERR_BOUNDS, "a kernel computed an offset outside its buffer and skipped the access "
+                                        "(error word 0x%08x, site %u)", w, w & 0xFFu);
         return fail(TMG_ERR_TIMEOUT, "a kernel wait ran out of its budget (error word 0x%08x, site %u)", w,
                     w & 0xFFu);
     }
@@ -1354,6 +1425,33 @@ tmg_status tmg_debug_wait_timeout(uint64_t budget_ns, void *stream)
     ErrCtx ctx{ds->err_word, budget_ns};
     cudaError_t e = launch_wait_probe(ctx, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TMG_OK : cuda_fail(e, "wait probe launch");
+}
+
+tmg_status tmg_debug_bounds_probe(void *stream)
+{
+    t_last_error.clear();
+#ifdef TMG_DEBUG_BOUNDS
+    DeviceState *ds = nullptr;
+    tmg_status st;
+    if ((st = device_state(&ds)) != TMG_OK)
+        return st;
+    note_launch();
+    bounds_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(1024, err_ctx(*ds));
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? TMG_OK : cuda_fail(e, "bounds probe launch");
+#else
+    (void)stream;
+    return fail(TMG_ERR_UNSUPPORTED, "bounds checks exist only in the debug build (libtmg_debug.so)");
+#endif
+}
+
+int tmg_debug_build(void)
+{
+#ifdef TMG_DEBUG_BOUNDS
+    return 1;
+#else
+    return 0;
+#endif
 }
 
 uint64_t tmg_launch_count(void) { return g_launches.load(); }

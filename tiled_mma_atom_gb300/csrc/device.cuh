@@ -18,6 +18,7 @@ namespace tmg {
 // Device error word codes (OR-ed into the word, high byte = kind).
 enum : uint32_t {
     kErrTimeout = 0x01000000u,
+    kErrBounds = 0x02000000u,     // debug build: an offset outside its buffer (site in the low bits)
 };
 
 // Wait-site identifiers (low bits of the error word) for diagnostics.
@@ -28,6 +29,12 @@ enum : uint32_t {
     kSiteEpiTmemFull = 4,
     kSiteDrain = 5,
     kSiteProbe = 6,
+    // bounds-check sites of the debug build
+    kBndStoreD = 16,        // a store of D
+    kBndPartials = 17,      // split-K / stream-K partial sums
+    kBndCounters = 18,      // split-K / stream-K tile counters
+    kBndScratch = 19,       // other library scratch (W4A8 split activations and row sums)
+    kBndProbe = 20,         // tmg_debug_bounds_probe
 };
 
 // Arguments every kernel receives for error reporting.
@@ -110,6 +117,39 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const 
             }
         }
     }
+}
+
+// --------------------------------------------------- debug bounds checks
+//
+// Built with -DTMG_DEBUG_BOUNDS (build.py, debug build: libtmg_debug.so),
+// every store of D and every access to split-K / stream-K scratch in the GEMM
+// kernels first checks its computed element offset against the extent of
+// its buffer: an offset outside [0, limit) ORs kErrBounds | site into the
+// device error word and the access is skipped, so tmg_check reports it
+// instead of memory being overwritten.  In the normal build the check is a
+// constant `true` and costs nothing.  (TMA loads and stores need no check:
+// the hardware clips them to the tensor map's extents.)
+__device__ __forceinline__ bool bounds_ok(int64_t off, int64_t limit, const ErrCtx &err, uint32_t site)
+{
+#ifdef TMG_DEBUG_BOUNDS
+    if (off < 0 || off >= limit) {
+        atomicOr(err.word, kErrBounds | site);
+        return false;
+    }
+#else
+    (void)off;
+    (void)limit;
+    (void)err;
+    (void)site;
+#endif
+    return true;
+}
+
+// The same for the n elements off .. off + n - 1 of one vector access (an
+// empty span, n <= 0, touches nothing).
+__device__ __forceinline__ bool span_ok(int64_t off, int n, int64_t limit, const ErrCtx &err, uint32_t site)
+{
+    return n <= 0 || (bounds_ok(off, limit, err, site) && bounds_ok(off + n - 1, limit, err, site));
 }
 
 // ------------------------------------------------------------------- TMA

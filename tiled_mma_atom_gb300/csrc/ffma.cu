@@ -59,8 +59,13 @@ constexpr int kFfmaThreads = 256;
 template <typename T, int BM, int BN, int kFfmaBK>
 __global__ void __launch_bounds__(kFfmaThreads)
     ffma_gemm_kernel(const T *__restrict__ A, const T *__restrict__ B, T *__restrict__ D,
-                     DevLayout la, DevLayout lb, DevLayout ld, int64_t M, int64_t N, int64_t K)
+                     DevLayout la, DevLayout lb, DevLayout ld, int64_t M, int64_t N, int64_t K, ErrCtx err)
 {
+#ifdef TMG_DEBUG_BOUNDS
+    const int64_t a_limit = layout_extent(la), b_limit = layout_extent(lb), d_limit = layout_extent(ld);
+#else
+    const int64_t a_limit = 0, b_limit = 0, d_limit = 0;     // unused: the checks are constant true
+#endif
     constexpr int TM = BM / 16, TN = BN / 16;
     constexpr int LA = BM * kFfmaBK / kFfmaThreads;     // elements of A each thread loads per slice
     constexpr int LB = BN * kFfmaBK / kFfmaThreads;
@@ -80,13 +85,15 @@ __global__ void __launch_bounds__(kFfmaThreads)
         for (int r = 0; r < LA; ++r) {
             const int e = tid + kFfmaThreads * r;
             const int64_t m = m0 + e / kFfmaBK, k = k0 + e % kFfmaBK;
-            ra[r] = (m < M && k < K) ? ld_elt(A, crd2idx(la, m, k)) : 0.f;
+            const int64_t off = (m < M && k < K) ? crd2idx(la, m, k) : -1;
+            ra[r] = (off >= 0 && bounds_ok(off, a_limit, err, kBndStoreD)) ? ld_elt(A, off) : 0.f;
         }
 #pragma unroll
         for (int r = 0; r < LB; ++r) {
             const int e = tid + kFfmaThreads * r;
             const int64_t n = n0 + e / kFfmaBK, k = k0 + e % kFfmaBK;
-            rb[r] = (n < N && k < K) ? ld_elt(B, crd2idx(lb, n, k)) : 0.f;
+            const int64_t off = (n < N && k < K) ? crd2idx(lb, n, k) : -1;
+            rb[r] = (off >= 0 && bounds_ok(off, b_limit, err, kBndStoreD)) ? ld_elt(B, off) : 0.f;
         }
     };
     auto stash = [&](int buf) {
@@ -146,7 +153,7 @@ __global__ void __launch_bounds__(kFfmaThreads)
 #pragma unroll
         for (int j = 0; j < TN; ++j) {
             const int64_t n = n0 + tx + 16 * j;
-            if (n < N)
+            if (n < N && bounds_ok(crd2idx(ld, m, n), d_limit, err, kBndStoreD))
                 st_elt(D, crd2idx(ld, m, n), acc[i][j]);
         }
     }
@@ -243,36 +250,36 @@ __global__ void __launch_bounds__(256)
 }
 
 template <typename T, int BM, int BN, int BK>
-cudaError_t launch_ffma_cfg(const FfmaArgs &a, cudaStream_t s)
+cudaError_t launch_ffma_cfg(const FfmaArgs &a, const ErrCtx &err, cudaStream_t s)
 {
     dim3 grid(static_cast<unsigned>((a.N + BN - 1) / BN), static_cast<unsigned>((a.M + BM - 1) / BM));
     if (grid.y > 65535u)
         return cudaErrorInvalidConfiguration;
     note_launch();
     ffma_gemm_kernel<T, BM, BN, BK><<<grid, kFfmaThreads, 0, s>>>(static_cast<const T *>(a.A), static_cast<const T *>(a.B),
-                                                                  static_cast<T *>(a.D), a.la, a.lb, a.ld, a.M, a.N, a.K);
+                                                                  static_cast<T *>(a.D), a.la, a.lb, a.ld, a.M, a.N, a.K,
+                                                                  err);
     return cudaGetLastError();
 }
 
 template <typename T>
-cudaError_t launch_ffma_t(const FfmaArgs &a, int num_sms, cudaStream_t s)
+cudaError_t launch_ffma_t(const FfmaArgs &a, int num_sms, const ErrCtx &err, cudaStream_t s)
 {
     // Latency-bound small problems: many 16x16 tiles, 128-deep K slices (one
     // global round trip per 128 k); mid-size: 32x32; large: 64x64.
     const int64_t mn = a.M * a.N;
     if (mn <= static_cast<int64_t>(num_sms) * 16 * 16 * 2)
-        return launch_ffma_cfg<T, 16, 16, 128>(a, s);
+        return launch_ffma_cfg<T, 16, 16, 128>(a, err, s);
     if (mn <= static_cast<int64_t>(num_sms) * 64 * 64)
-        return launch_ffma_cfg<T, 32, 32, 32>(a, s);
-    return launch_ffma_cfg<T, 64, 64, 32>(a, s);
+        return launch_ffma_cfg<T, 32, 32, 32>(a, err, s);
+    return launch_ffma_cfg<T, 64, 64, 32>(a, err, s);
 }
 
 }  // namespace
 
 cudaError_t launch_ffma(const FfmaArgs &a, int dtype, int num_sms, const ErrCtx &err, cudaStream_t s)
 {
-    (void)err;
-    return dtype == 0 ? launch_ffma_t<float>(a, num_sms, s) : launch_ffma_t<__nv_bfloat16>(a, num_sms, s);
+    return dtype == 0 ? launch_ffma_t<float>(a, num_sms, err, s) : launch_ffma_t<__nv_bfloat16>(a, num_sms, err, s);
 }
 
 cudaError_t launch_zero_fill(void *D, const DevLayout &ld, int64_t M, int64_t N, int dtype,

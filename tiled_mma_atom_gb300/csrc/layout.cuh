@@ -22,4 +22,15 @@ __device__ __forceinline__ int64_t crd2idx(const DevLayout &L, int64_t r, int64_
     return mode_off(L, 0, r) + mode_off(L, 1, c);
 }
 
+// Elements the layout spans: one past its largest offset (strides are >= 0,
+// checked by the host), the limit of the debug build's bounds checks.
+__device__ __forceinline__ int64_t layout_extent(const DevLayout &L)
+{
+    int64_t e = 1;
+    for (int t = 0; t < 2; ++t)
+        for (int j = 0; j < L.depth[t]; ++j)
+            e += (L.shape[t][j] - 1) * L.stride[t][j];
+    return e;
+}
+
 }  // namespace tmg

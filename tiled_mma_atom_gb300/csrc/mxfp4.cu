@@ -127,6 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                  const uint8_t *__restrict__ relA, const uint8_t *__restrict__ relB,
                  __nv_bfloat16 *__restrict__ D, int M, int N, int K, int vec_ok, ErrCtx err)
 {
+    const int64_t d_limit = static_cast<int64_t>(M) * N;     // elements of D
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -277,7 +278,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t v[32];
                 tmem_ld32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccCols + c * 32, v);
                 const int col0 = tn * kBN + c * 32;
-                if (row < M) {
+                const int64_t off = static_cast<int64_t>(row) * N + col0;
+                if (row < M && span_ok(off, min(32, N - col0), d_limit, err, kBndStoreD)) {
                     if (vec_ok && col0 + 32 <= N) {
                         uint4 *dst = reinterpret_cast<uint4 *>(drow + col0);
 #pragma unroll

@@ -105,6 +105,7 @@ __global__ void __launch_bounds__(pair_threads(ACC_BUFS), 1)
     using C = MxPairCfg<BN, ACC_BUFS>;
     constexpr int STAGES = C::STAGES;
     constexpr int NSUB = C::NSUB;
+    const int64_t d_limit = static_cast<int64_t>(M) * N;     // elements of D
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -360,6 +361,9 @@ __global__ void __launch_bounds__(pair_threads(ACC_BUFS), 1)
 #pragma unroll
                     for (int c = 0; c < HALF / 32; ++c) {
                         const int col0 = tn * BN + h * HALF + c * 32;
+                        if (col0 >= N || !span_ok(static_cast<int64_t>(row) * N + col0, min(32, N - col0), d_limit, err,
+                                                  kBndStoreD))
+                            continue;
                         if (vec_ok == 2 && col0 + 32 <= N) {
                             const uint32_t *w = packed + c * 16;
                             st_global_v8(drow + col0, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
@@ -388,7 +392,8 @@ __global__ void __launch_bounds__(pair_threads(ACC_BUFS), 1)
                     uint32_t v[32];
                     tmem_ld32(tbase + c * 32, v);
                     const int col0 = tn * BN + c * 32;
-                    if (row < M) {
+                    if (row < M && col0 < N &&
+                        span_ok(static_cast<int64_t>(row) * N + col0, min(32, N - col0), d_limit, err, kBndStoreD)) {
                         if (vec_ok && col0 + 32 <= N) {
                             uint4 *dst = reinterpret_cast<uint4 *>(drow + col0);
 #pragma unroll

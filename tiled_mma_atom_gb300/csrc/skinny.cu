@@ -81,6 +81,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int KB = (K + kBK - 1) / kBK;
     const int64_t U = static_cast<int64_t>(tiles) * KB;
     const int64_t u_begin = unit_start(c, U, G), u_end = unit_start(c + 1, U, G);
+    const int64_t d_limit = static_cast<int64_t>(M - 1) * ldd + N;                   // elements of D
+    const int64_t p_limit = static_cast<int64_t>(G) * 2 * mp * kTileN;               // floats of partials
     const uint32_t a_bytes = static_cast<uint32_t>(mp) * kBK * 2;
 
     if (threadIdx.x == 0) {
@@ -227,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (n < N) {
 #pragma unroll
                     for (int m = 0; m < kMaxMP; ++m)
-                        if (m < M)
+                        if (m < M && bounds_ok(static_cast<int64_t>(m) * ldd + n, d_limit, err, kBndStoreD))
                             D[static_cast<int64_t>(m) * ldd + n] = __float2bfloat16_rn(v[m]);
                 }
                 continue;
@@ -236,16 +238,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             // arrive for (tile, quarter) reduces them.  Warps never wait on
             // one another, so an aborted warp cannot stall the others.
             const int slot = 2 * c + (seg == 0 ? 0 : 1);
-            float *mine = partials + static_cast<int64_t>(slot) * mp * kTileN;
+            const int64_t mine_off = static_cast<int64_t>(slot) * mp * kTileN;
+            float *mine = partials + mine_off;
 #pragma unroll
             for (int m = 0; m < kMaxMP; ++m)
-                if (m < mp)
+                if (m < mp && bounds_ok(mine_off + m * kTileN + n_local, p_limit, err, kBndPartials))
                     mine[m * kTileN + n_local] = v[m];
             __threadfence();
             __syncwarp();
             const int64_t t_first = static_cast<int64_t>(tile) * KB;
             const int c_first = unit_owner(t_first, U, G);
             const int c_last = unit_owner(t_first + KB - 1, U, G);
+            if (!bounds_ok(static_cast<int64_t>(tile) * 4 + q, static_cast<int64_t>(tiles) * 4, err, kBndCounters))
+                continue;
             uint32_t old = 0;
             if (lane == 0)
                 old = atomicAdd(&counters[tile * 4 + q], 1u);
@@ -264,17 +269,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     } else {
                         const int first_tile = static_cast<int>(unit_start(cc, U, G) / KB);
                         const int s2 = 2 * cc + (first_tile == tile ? 0 : 1);
-                        const float *p = partials + static_cast<int64_t>(s2) * mp * kTileN;
+                        const int64_t p_off = static_cast<int64_t>(s2) * mp * kTileN;
+                        const float *p = partials + p_off;
 #pragma unroll
                         for (int m = 0; m < kMaxMP; ++m)
-                            if (m < mp)
+                            if (m < mp && bounds_ok(p_off + m * kTileN + n_local, p_limit, err, kBndPartials))
                                 sum[m] += __ldcg(p + m * kTileN + n_local);
                     }
                 }
                 if (n < N) {
 #pragma unroll
                     for (int m = 0; m < kMaxMP; ++m)
-                        if (m < M)
+                        if (m < M && bounds_ok(static_cast<int64_t>(m) * ldd + n, d_limit, err, kBndStoreD))
                             D[static_cast<int64_t>(m) * ldd + n] = __float2bfloat16_rn(sum[m]);
                 }
                 __syncwarp();

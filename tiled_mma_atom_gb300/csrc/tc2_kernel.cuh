@@ -313,6 +313,7 @@ __global__ void __launch_bounds__(tc2_threads(EPI), 1)
 {
     using C = PairCfg<BN, EPI>;
     static_assert(MAJ == 0 || (IN == kInBf16 && !EPI && (BN / 2) % kMnBox == 0), "MN-major operands: plain bf16");
+    const int64_t d_limit = static_cast<int64_t>(M - 1) * ldd + N;     // elements of D
     constexpr int KB_ELEMS = kb_elems(IN);
     constexpr int STAGES = C::STAGES;
     constexpr uint32_t STAGE_TX = 2u * C::STAGE_BYTES;
@@ -532,7 +533,8 @@ __global__ void __launch_bounds__(tc2_threads(EPI), 1)
                     const int row0 = row - lane;
                     if constexpr (EPI) {
                         if (epi.out_i32) {
-                            if (row < M)
+                            if (row < M && span_ok(static_cast<int64_t>(row) * ldd + col0, min(32, N - col0), d_limit,
+                                                   err, kBndStoreD))
                                 store_row_i32(reinterpret_cast<int32_t *>(D) + static_cast<int64_t>(row) * ldd, col0, N,
                                               vec_ok, v, epi.out_i32 == 2);
                             continue;
@@ -561,7 +563,8 @@ __global__ void __launch_bounds__(tc2_threads(EPI), 1)
                             bulk_commit();
                         }
                         ++nst;
-                    } else if (row < M) {
+                    } else if (row < M && span_ok(static_cast<int64_t>(row) * ldd + col0, min(32, N - col0), d_limit,
+                                                  err, kBndStoreD)) {
                         store_row_chunk(drow, col0, N, vec_ok, v);
                     }
                 }
@@ -575,16 +578,19 @@ __global__ void __launch_bounds__(tc2_threads(EPI), 1)
             // scratch, laid out [chunk][4-column group][lane][4] so each
             // store moves 512 contiguous bytes.
             const int64_t warp_elems = 32 * BN;
-            float *mine = partials + ((static_cast<int64_t>(2 * cluster + slot) * 2 + rank) * 4 + q) * warp_elems;
+            const int64_t p_limit = static_cast<int64_t>(nclusters) * 2 * 2 * 4 * warp_elems;   // floats of scratch
+            const int64_t mine_off = ((static_cast<int64_t>(2 * cluster + slot) * 2 + rank) * 4 + q) * warp_elems;
+            float *mine = partials + mine_off;
 #pragma unroll 1
             for (int c = c_begin; c < c_end; ++c) {
                 uint32_t r[32];
                 tmem_ld32(tbase + c * 32, r);
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
-                    reinterpret_cast<float4 *>(mine)[(c * 8 + j) * 32 + lane] =
-                        make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                    __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+                    if (span_ok(mine_off + ((c * 8 + j) * 32 + lane) * 4, 4, p_limit, err, kBndPartials))
+                        reinterpret_cast<float4 *>(mine)[(c * 8 + j) * 32 + lane] =
+                            make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                        __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
             }
             tc_fence_before();
             __syncwarp();
@@ -595,7 +601,10 @@ __global__ void __launch_bounds__(tc2_threads(EPI), 1)
             const int rel = tile;
             const int c_first = unit_owner(static_cast<int64_t>(rel) * num_kb, U, nclusters);
             const int c_last = unit_owner(static_cast<int64_t>(rel + 1) * num_kb - 1, U, nclusters);
-            uint32_t *counter = counters + (static_cast<int64_t>(rel) * 2 + rank) * NEPI + e;
+            const int64_t counter_idx = (static_cast<int64_t>(rel) * 2 + rank) * NEPI + e;
+            if (!bounds_ok(counter_idx, static_cast<int64_t>(sk_tiles) * 2 * NEPI, err, kBndCounters))
+                continue;
+            uint32_t *counter = counters + counter_idx;
             uint32_t old = 0;
             if (lane == 0)
                 old = atomicAdd(counter, 1u);
@@ -613,10 +622,12 @@ __global__ void __launch_bounds__(tc2_threads(EPI), 1)
                 for (int cc = c_first; cc <= c_last; ++cc) {
                     const int first_tile = static_cast<int>((U * cc / nclusters) / num_kb);
                     const int s2 = first_tile == tile ? 0 : 1;
-                    const float4 *src = reinterpret_cast<const float4 *>(
-                        partials + ((static_cast<int64_t>(2 * cc + s2) * 2 + rank) * 4 + q) * warp_elems);
+                    const int64_t src_off = ((static_cast<int64_t>(2 * cc + s2) * 2 + rank) * 4 + q) * warp_elems;
+                    const float4 *src = reinterpret_cast<const float4 *>(partials + src_off);
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
+                        if (!span_ok(src_off + ((c * 8 + j) * 32 + lane) * 4, 4, p_limit, err, kBndPartials))
+                            continue;
                         const float4 p = __ldcg(src + (c * 8 + j) * 32 + lane);
                         v[4 * j] += p.x;
                         v[4 * j + 1] += p.y;
@@ -627,13 +638,15 @@ __global__ void __launch_bounds__(tc2_threads(EPI), 1)
                 if constexpr (EPI) {
                     apply_epilogue<BN>(v, epi, sa_row, cols, c * 32);
                     if (epi.out_i32) {
-                        if (row < M)
+                        if (row < M && span_ok(static_cast<int64_t>(row) * ldd + tn * BN + c * 32,
+                                               min(32, N - tn * BN - c * 32), d_limit, err, kBndStoreD))
                             store_row_i32(reinterpret_cast<int32_t *>(D) + static_cast<int64_t>(row) * ldd,
                                           tn * BN + c * 32, N, vec_ok, v, epi.out_i32 == 2);
                         continue;
                     }
                 }
-                if (row < M)
+                if (row < M && span_ok(static_cast<int64_t>(row) * ldd + tn * BN + c * 32, min(32, N - tn * BN - c * 32),
+                                       d_limit, err, kBndStoreD))
                     store_row_chunk(drow, tn * BN + c * 32, N, vec_ok, v);
             }
             __syncwarp();

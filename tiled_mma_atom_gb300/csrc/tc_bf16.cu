@@ -64,6 +64,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    __nv_bfloat16 *__restrict__ D, int64_t ldd, int M, int N, int K, int vec_ok,
                    ErrCtx err)
 {
+    const int64_t d_limit = static_cast<int64_t>(M - 1) * ldd + N;     // elements of D
     using C = Cfg<BN, STAGES>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -209,8 +210,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t v[32];
                 tmem_ld32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + c * 32, v);
                 const int col0 = tn * BN + c * 32;
+                const int64_t off = static_cast<int64_t>(row) * ldd + col0;
                 if (row < M) {
                     if (vec_ok && col0 + 32 <= N) {
+                        if (!span_ok(off, 32, d_limit, err, kBndStoreD))
+                            continue;
                         uint4 *dst = reinterpret_cast<uint4 *>(drow + col0);
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
@@ -224,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     } else {
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
-                            if (col0 + j < N)
+                            if (col0 + j < N && bounds_ok(off + j, d_limit, err, kBndStoreD))
                                 drow[col0 + j] = __float2bfloat16_rn(__uint_as_float(v[j]));
                     }
                 }

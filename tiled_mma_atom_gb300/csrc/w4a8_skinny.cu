@@ -546,11 +546,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             const int n = tile * kTileN + n_local;
             int32_t *d = D + n;
+            const int64_t d_limit = static_cast<int64_t>(M - 1) * ldd + N;     // elements of D
             if (n < N && kb0 == 0 && kb1 == KB) {
                 // the whole tile is this CTA's: plain stores
 #pragma unroll
                 for (int m = 0; m < kMaxMP; ++m)
-                    if (m < M)
+                    if (m < M && bounds_ok(static_cast<int64_t>(m) * ldd + n, d_limit, err, kBndStoreD))
                         d[static_cast<int64_t>(m) * ldd] = v[m] - 8 * R[m];
             } else if (n < N) {
                 // a share of a tile: add into the zeroed D; the first K
@@ -558,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int corr = kb0 == 0 ? 8 : 0;
 #pragma unroll
                 for (int m = 0; m < kMaxMP; ++m)
-                    if (m < M)
+                    if (m < M && bounds_ok(static_cast<int64_t>(m) * ldd + n, d_limit, err, kBndStoreD))
                         atomicAdd(d + static_cast<int64_t>(m) * ldd, v[m] - corr * R[m]);
             }
             __syncwarp();
