@@ -438,23 +438,6 @@ tmg_status tc2_scratch(int dev, cudaStream_t s, TcArgs &a)
     return TMG_OK;
 }
 
-// Tensor map for the pair kernel's TMA stores of D (rows x cols bf16, row
-// stride ld): boxes of 32 x 32, no swizzle.  Left unused (d_tma = 0) when D
-// or its row stride is not 16-byte aligned; the kernel then stores with
-// per-thread writes.
-tmg_status encode_d_store(TcArgs &a, void *D, int64_t rows, int64_t cols, int64_t ld)
-{
-    a.d_tma = 0;
-    if (!tma_ok(D, ld, 2, rows, cols))
-        return TMG_OK;
-    tmg_status st = encode_2d(&a.tmD, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, cols, rows, ld, 32, 32,
-                              CU_TENSOR_MAP_SWIZZLE_NONE);
-    if (st != TMG_OK)
-        return st;
-    a.d_tma = 1;
-    return TMG_OK;
-}
-
 tmg_status run_tc(const DeviceState &ds, const TcPlan &p, void *D, int64_t K, int mode, cudaStream_t s)
 {
     TcArgs a;
@@ -502,13 +485,10 @@ tmg_status run_tc(const DeviceState &ds, const TcPlan &p, void *D, int64_t K, in
         cudaGetDevice(&dev);
         if ((st = tc2_scratch(dev, s, a)) != TMG_OK)
             return st;
-        if ((st = encode_d_store(a, D, p.M, p.N, p.ldd)) != TMG_OK)
-            return st;
     }
     if (pair)
         log_choice("bf16 %dx%dx%d -> tc2_gemm_kernel (CTA pairs): 256x%d tiles, %d pairs, %d data-parallel + %d "
-                   "stream-K tiles, D stores %s", a.M, a.N, a.K, a.bn, a.pairs, a.dp_tiles, a.sk_tiles,
-                   a.d_tma ? "TMA" : "per thread");
+                   "stream-K tiles", a.M, a.N, a.K, a.bn, a.pairs, a.dp_tiles, a.sk_tiles);
     else
         log_choice("bf16 %dx%dx%d -> tc_bf16_kernel (one CTA): 128x%d tiles", a.M, a.N, a.K, a.bn);
     cudaError_t e = pair ? launch_tc2_bf16(a, ds.num_sms, err_ctx(ds), s) : launch_tc_bf16(a, ds.num_sms, err_ctx(ds), s);
@@ -629,8 +609,6 @@ bool run_tc2_inplace(const DeviceState &ds, const void *A, const void *B, void *
     int dev = 0;
     cudaGetDevice(&dev);
     if ((*st = tc2_scratch(dev, s, a)) != TMG_OK)
-        return true;
-    if ((*st = encode_d_store(a, D, M, N, ldd)) != TMG_OK)
         return true;
     log_choice("bf16 %dx%dx%d -> tc2_gemm_kernel (CTA pairs), MN-major operands read in place (A %s, B %s): "
                "256x%d tiles, %d pairs, %d data-parallel + %d stream-K tiles", a.M, a.N, a.K,
@@ -1044,8 +1022,6 @@ tmg_status tmg_gemm_fused(const void *A, const void *B, void *D, int64_t M, int6
     cudaGetDevice(&dev);
     if ((st = tc2_scratch(dev, s, a)) != TMG_OK)
         return st;
-    if ((st = encode_d_store(a, D, M, N, N)) != TMG_OK)
-        return st;
     log_choice("%s %dx%dx%d fused (epilogue %d, scale_a %s, scale_b %s) -> tc2_gemm_kernel (CTA pairs): 256x%d tiles, "
                "%d pairs, %d data-parallel + %d stream-K tiles", e4m3 ? "e4m3" : "bf16", a.M, a.N, a.K, epi.epi,
                epi.scale_a ? "yes" : "no", epi.scale_b ? "yes" : "no", a.bn, a.pairs, a.dp_tiles, a.sk_tiles);
@@ -1153,7 +1129,6 @@ tmg_status gemm_w4a8_impl(const void *A, const void *B, bool shuffled, void *D, 
         a.M = static_cast<int>(M);
         a.N = static_cast<int>(N);
         a.K = static_cast<int>(kc);
-        a.d_tma = 0;
         tc2_plan(a, ds->num_sms);
         if ((st = tc2_scratch(dev, s, a)) != TMG_OK)
             return st;

@@ -196,38 +196,6 @@ __device__ __forceinline__ void tma_load_2d_hint(void *smem_dst, const CUtensorM
         : "memory");
 }
 
-// TMA tile store shared -> global (tensor map over the destination; the box
-// is read from this CTA's shared memory, rows contiguous).  Rows and columns
-// past the tensor's extents are not written.  Coordinates must be >= 0 and
-// x * element size a multiple of 16 bytes.
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *smem_src, int32_t c0, int32_t c1)
-{
-    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(smem_u32(smem_src)), "r"(c0), "r"(c1)
-                 : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-
-// Wait until at most N committed bulk groups of this thread still read
-// shared memory (their sources may then be overwritten).
-template <int N>
-__device__ __forceinline__ void bulk_wait_read()
-{
-    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-
-// Wait until every committed bulk group of this thread has completed.
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
-// Make this thread's generic-proxy shared-memory writes visible to the async
-// proxy (TMA) before a bulk operation reads them.
-__device__ __forceinline__ void fence_proxy_async_smem()
-{
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 __device__ __forceinline__ uint64_t policy_evict_first()
 {
     uint64_t p;
@@ -523,12 +491,6 @@ __device__ __forceinline__ void st_global_v8(void *p, uint32_t a0, uint32_t a1, 
     asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a0), "r"(a1), "r"(a2),
                  "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7)
                  : "memory");
-}
-
-// Named barrier among `nthreads` threads (multiple of 32), id 1..15.
-__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads)
-{
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // Two fp32 -> packed bf16x2, round to nearest even (lo in the low half).

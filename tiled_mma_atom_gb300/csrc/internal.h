@@ -48,8 +48,6 @@ cudaError_t launch_zero_fill(void *D, const DevLayout &ld, int64_t M, int64_t N,
 struct TcArgs {
     CUtensorMap tmA;   // A (M,K) bf16 K-major, box {64, 128}, 128B swizzle
     CUtensorMap tmB;   // B (N,K) bf16 K-major, box {64, BN} (pair kernel: {64, BN/2}), 128B swizzle
-    CUtensorMap tmD;   // pair kernel: D (M,N) bf16, box {32, 32}, no swizzle (valid when d_tma)
-    int d_tma;         // pair kernel: store D through tmD (16-byte aligned D and row stride)
     void *D;           // bf16 (M,N), row stride ldd elements, unit column stride
     int64_t ldd;
     int M, N, K;

@@ -67,23 +67,23 @@ constexpr int kGroupM = 8;
 // Elements per K block for an input type.
 __host__ __device__ constexpr int kb_elems(int in) { return in == kInE4m3 ? 128 : 64; }
 
-// Shared memory, in order: the ring of A / B stages; per epilogue warp two
-// 32 x 32 bf16 boxes that stage its output for TMA stores; the barriers; with
-// the fused epilogue, per epilogue warp a copy of the tile's scale_b and bias
-// columns.
+// Shared memory, in order: the ring of A / B stages; the barriers; with the
+// fused epilogue, per epilogue warp a copy of the tile's scale_b and bias
+// columns.  (The epilogue stores D straight from registers with 32-byte
+// vector stores: staging tiles in shared memory for TMA stores was no faster
+// and 16-byte stores wrote each 32-byte sector in halves — bf16 4096³:
+// 83.5 -> 81.5 µs.)
 template <int BN, bool EPI>
 struct PairCfg {
     static constexpr int A_BYTES = kHalfM * kKBlockBytes;       // 16 KB
     static constexpr int B_BYTES = (BN / 2) * kKBlockBytes;     // this CTA's half
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int BOX_BYTES = 32 * 32 * 2;                // one 32 x 32 bf16 output box
-    static constexpr int STAGING_BYTES = epi_warps(EPI) * 2 * BOX_BYTES;
     static constexpr int COLS_BYTES = EPI ? epi_warps(EPI) * 2 * BN * 4 : 0;
-    static constexpr int RING_BUDGET = 220 * 1024 - 2048 - STAGING_BYTES - COLS_BYTES;
+    static constexpr int RING_BUDGET = 220 * 1024 - 2048 - COLS_BYTES;
     static constexpr int STAGES = RING_BUDGET / STAGE_BYTES > 8 ? 8 : RING_BUDGET / STAGE_BYTES;
     static constexpr int TMEM_COLS = 512;
     static constexpr int BAR_BYTES = (2 * STAGES + 4) * 8 + 16;
-    static constexpr int SMEM = STAGES * STAGE_BYTES + STAGING_BYTES + BAR_BYTES + COLS_BYTES + 1024;
+    static constexpr int SMEM = STAGES * STAGE_BYTES + BAR_BYTES + COLS_BYTES + 1024;
 };
 
 // Operand majorness (template parameter MAJ): bit 0 set when A is MN-major
@@ -183,11 +183,21 @@ __device__ __forceinline__ int unit_owner(int64_t u, int64_t U, int P)
 }
 
 // Round 32 fp32 values of one output row to bf16 and store them at
-// drow[col0 .. col0+31] (bounded by N).
+// drow[col0 .. col0+31] (bounded by N): two 32-byte stores (whole sectors)
+// where the row segment starts on a 32-byte boundary, else four 16-byte
+// stores (vec_ok: 16-byte aligned rows), else one by one.
 __device__ __forceinline__ void store_row_chunk(__nv_bfloat16 *drow, int col0, int N, int vec_ok,
                                                 const float (&v)[32])
 {
-    if (vec_ok && col0 + 32 <= N) {
+    if (vec_ok && col0 + 32 <= N && (reinterpret_cast<uintptr_t>(drow + col0) & 31u) == 0) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+            st_global_v8(drow + col0 + 16 * j, pack_bf16x2(v[16 * j + 0], v[16 * j + 1]),
+                         pack_bf16x2(v[16 * j + 2], v[16 * j + 3]), pack_bf16x2(v[16 * j + 4], v[16 * j + 5]),
+                         pack_bf16x2(v[16 * j + 6], v[16 * j + 7]), pack_bf16x2(v[16 * j + 8], v[16 * j + 9]),
+                         pack_bf16x2(v[16 * j + 10], v[16 * j + 11]), pack_bf16x2(v[16 * j + 12], v[16 * j + 13]),
+                         pack_bf16x2(v[16 * j + 14], v[16 * j + 15]));
+    } else if (vec_ok && col0 + 32 <= N) {
         uint4 *dst = reinterpret_cast<uint4 *>(drow + col0);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -307,9 +317,9 @@ __device__ __forceinline__ void apply_epilogue(float (&v)[32], const Tc2Epi &e, 
 template <int BN, int IN, bool EPI, int MAJ = 0>
 __global__ void __launch_bounds__(tc2_threads(EPI), 1)
     tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const __grid_constant__ CUtensorMap tmD, __nv_bfloat16 *__restrict__ D, int64_t ldd, int M, int N,
-                    int K, int dp_tiles, int sk_tiles, float *__restrict__ partials,
-                    uint32_t *__restrict__ counters, int vec_ok, int d_tma, Tc2Epi epi, ErrCtx err)
+                    __nv_bfloat16 *__restrict__ D, int64_t ldd, int M, int N, int K, int dp_tiles, int sk_tiles,
+                    float *__restrict__ partials, uint32_t *__restrict__ counters, int vec_ok, Tc2Epi epi,
+                    ErrCtx err)
 {
     using C = PairCfg<BN, EPI>;
     static_assert(MAJ == 0 || (IN == kInBf16 && !EPI && (BN / 2) % kMnBox == 0), "MN-major operands: plain bf16");
@@ -322,14 +332,13 @@ __global__ void __launch_bounds__(tc2_threads(EPI), 1)
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     uint8_t *sA = smem;
     uint8_t *sB = smem + STAGES * C::A_BYTES;
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * C::STAGE_BYTES + C::STAGING_BYTES);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * C::STAGE_BYTES);
     uint64_t *empty = full + STAGES;
     uint64_t *tfull = empty + STAGES;
     uint64_t *tempty = tfull + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    uint8_t *staging = smem + STAGES * C::STAGE_BYTES;
-    float *epi_cols = reinterpret_cast<float *>(staging + C::STAGING_BYTES + C::BAR_BYTES);
+    float *epi_cols = reinterpret_cast<float *>(smem + STAGES * C::STAGE_BYTES + C::BAR_BYTES);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const uint32_t rank = cluster_ctarank();
@@ -352,8 +361,6 @@ __global__ void __launch_bounds__(tc2_threads(EPI), 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
-        if (d_tma)
-            tma_prefetch_desc(&tmD);
     }
     if (warp == 1) {
         tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
@@ -480,10 +487,6 @@ __global__ void __launch_bounds__(tc2_threads(EPI), 1)
         const int e = warp - 2;                          // epilogue warp index
         const int q = warp & 3;                          // its TMEM lane quarter
         const int c_begin = (e / 4) * CHUNKS, c_end = c_begin + CHUNKS;
-        // output staging: two 32 x 32 bf16 boxes, used alternately; `nst`
-        // counts the TMA stores this warp's lane 0 has issued
-        uint8_t *boxes = staging + e * 2 * C::BOX_BYTES;
-        int nst = 0;
         const int64_t U = static_cast<int64_t>(sk_tiles) * num_kb;
         int local = 0;
         SegWalk walk(cluster, nclusters, dp_tiles, sk_tiles, num_kb);
@@ -530,7 +533,6 @@ __global__ void __launch_bounds__(tc2_threads(EPI), 1)
                     if constexpr (EPI)
                         apply_epilogue<BN>(v, epi, sa_row, cols, c * 32);
                     const int col0 = tn * BN + c * 32;
-                    const int row0 = row - lane;
                     if constexpr (EPI) {
                         if (epi.out_i32) {
                             if (row < M && span_ok(static_cast<int64_t>(row) * ldd + col0, min(32, N - col0), d_limit,
@@ -540,33 +542,9 @@ __global__ void __launch_bounds__(tc2_threads(EPI), 1)
                             continue;
                         }
                     }
-                    if (d_tma) {
-                        // stage this warp's 32 x 32 box, then one lane stores it
-                        if (row0 >= M || col0 >= N)
-                            continue;
-                        uint8_t *box = boxes + (nst & 1) * C::BOX_BYTES;
-                        if (nst >= 2) {              // the store from this buffer two boxes ago has read it
-                            if (lane == 0)
-                                bulk_wait_read<1>();
-                            __syncwarp();
-                        }
-                        uint4 *dst = reinterpret_cast<uint4 *>(box + lane * 64);
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            dst[j] = make_uint4(pack_bf16x2(v[8 * j], v[8 * j + 1]), pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
-                                                pack_bf16x2(v[8 * j + 4], v[8 * j + 5]),
-                                                pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) {
-                            tma_store_2d(&tmD, box, col0, row0);
-                            bulk_commit();
-                        }
-                        ++nst;
-                    } else if (row < M && span_ok(static_cast<int64_t>(row) * ldd + col0, min(32, N - col0), d_limit,
-                                                  err, kBndStoreD)) {
+                    if (row < M && span_ok(static_cast<int64_t>(row) * ldd + col0, min(32, N - col0), d_limit, err,
+                                           kBndStoreD))
                         store_row_chunk(drow, col0, N, vec_ok, v);
-                    }
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -653,8 +631,6 @@ __global__ void __launch_bounds__(tc2_threads(EPI), 1)
             if (lane == 0)
                 *counter = 0;
         }
-        if (lane == 0)
-            bulk_wait_all();             // this warp's TMA stores are complete
     }
 
     __syncwarp();
@@ -693,8 +669,8 @@ cudaError_t launch_pair(const TcArgs &a, const Tc2Epi &epi, const ErrCtx &err, c
     cfg.numAttrs = 1;
     const int vec_ok = (a.ldd % 8 == 0) && ((reinterpret_cast<uintptr_t>(a.D) & 15u) == 0);
     note_launch();
-    e = cudaLaunchKernelEx(&cfg, kern, a.tmA, a.tmB, a.tmD, static_cast<__nv_bfloat16 *>(a.D), a.ldd, a.M, a.N,
-                           a.K, a.dp_tiles, a.sk_tiles, a.partials, a.counters, vec_ok, a.d_tma, epi, err);
+    e = cudaLaunchKernelEx(&cfg, kern, a.tmA, a.tmB, static_cast<__nv_bfloat16 *>(a.D), a.ldd, a.M, a.N, a.K,
+                           a.dp_tiles, a.sk_tiles, a.partials, a.counters, vec_ok, epi, err);
     if (e != cudaSuccess)
         return e;
     return cudaGetLastError();
