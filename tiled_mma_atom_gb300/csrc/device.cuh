@@ -281,28 +281,6 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N)
     return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-// D[tmem] (+)= A[smem] · B[smem]ᵀ, one tcgen05.mma of the CTA (cta_group::1).
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                         uint32_t idesc, uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// Arrive once on `bar` when every tcgen05 operation issued so far by this
-// thread has completed.
-__device__ __forceinline__ void mma_commit(uint64_t *bar)
-{
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-            smem_u32(bar))
-        : "memory");
-}
-
 // TMEM -> registers: 32 lanes x 32 consecutive 32-bit columns; thread i of
 // the warp receives lane (lane base + i).  Waits for completion before
 // returning so the registers are safe to use.
@@ -416,6 +394,12 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity
     }
 }
 
+__device__ __forceinline__ bool mbar_wait_cluster_warp(uint64_t *bar, uint32_t parity, const ErrCtx &ctx,
+                                                       volatile int *abort, uint32_t site)
+{
+    return __all_sync(0xffffffffu, mbar_wait_cluster(bar, parity, ctx, abort, site));
+}
+
 // TMA tile load into this CTA's shared memory whose completion is counted on
 // an mbarrier that may live in the peer CTA (shared::cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(void *smem_dst, const CUtensorMap *map,
@@ -447,37 +431,84 @@ __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols
                  : "memory");
 }
 
-// One pair MMA (M = 256) issued by CTA 0.
-__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                              uint32_t idesc, uint32_t accumulate)
+// ------------------------------------------------- warp-wide MMA issue
+//
+// The MMA-issuing loops run on a whole warp in warp-uniform control flow;
+// the tcgen05 instruction itself carries an elect.sync predicate, so exactly
+// one lane (the lowest, the same one every time in a converged warp) issues
+// it and no branch splits the warp.  Issued from inside a one-lane branch
+// instead, a tcgen05.mma was measured at ~70 ns apiece on this part whatever
+// its shape, against ~37 ns (N <= 128) and the pipe's own ~66 ns at N = 256
+// from the warp-wide loop: inside the branch every operand has to leave the
+// uniform datapath before each instruction.  The commits go through the same
+// elected lane, so they track exactly the MMAs it issued.
+
+// Every lane waits; the warp leaves together with one agreed result.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, const ErrCtx &ctx,
+                                               volatile int *abort, uint32_t site)
+{
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctx, abort, site));
+}
+
+// D[tmem] (+)= A[smem] · B[smem]ᵀ, one tcgen05.mma of the CTA (cta_group::1).
+__device__ __forceinline__ void mma_bf16_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate)
 {
     asm volatile(
-        "{\n\t.reg .pred p;\n\t"
+        "{\n\t.reg .pred p, e;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on `bar` when every tcgen05 operation the elected lane issued
+// so far has completed.
+__device__ __forceinline__ void mma_commit_w(uint64_t *bar)
+{
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
+        : "memory");
+}
+
+// One pair MMA (M = 256) issued by CTA 0.
+__device__ __forceinline__ void mma_bf16_pair_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
 // The same for E4M3 operands (kind::f8f6f4, K = 32 per instruction).
-__device__ __forceinline__ void mma_e4m3_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                              uint32_t idesc, uint32_t accumulate)
+__device__ __forceinline__ void mma_e4m3_pair_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                uint32_t accumulate)
 {
     asm volatile(
-        "{\n\t.reg .pred p;\n\t"
+        "{\n\t.reg .pred p, e;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
 // Arrive once on the mbarrier at this shared-memory offset in every CTA of
 // `cta_mask` when the pair's prior tcgen05 operations have completed.
-__device__ __forceinline__ void mma_commit_pair(uint64_t *bar, uint16_t cta_mask)
+__device__ __forceinline__ void mma_commit_pair_w(uint64_t *bar, uint16_t cta_mask)
 {
     asm volatile(
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(smem_u32(bar)),
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
         "h"(cta_mask)
         : "memory");
 }

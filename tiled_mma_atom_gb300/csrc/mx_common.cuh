@@ -51,48 +51,6 @@ __host__ __device__ constexpr uint32_t idesc_mxf4(int M, int N, uint32_t sf_id)
            (1u << 23) | (static_cast<uint32_t>(M >> 4) << 24) | (sf_id << 29);
 }
 
-__device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                         uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
-                                         uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %6, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X "
-        "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
-        : "memory");
-}
-
-__device__ __forceinline__ void mma_mxf4_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                              uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
-                                              uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %6, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X "
-        "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
-        : "memory");
-}
-
-// Copy one 512-byte scale chunk (32 lines x 16 bytes) from shared memory to
-// 4 TMEM columns, replicated into all four lane quarters.
-__device__ __forceinline__ void tmem_cp_chunk(uint32_t taddr, uint64_t sdesc)
-{
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
-                 : "memory");
-}
-
-// The same, issued by CTA 0 of a pair for both CTAs (each CTA's chunk at the
-// same shared-memory offset goes to that CTA's TMEM).
-__device__ __forceinline__ void tmem_cp_chunk_pair(uint32_t taddr, uint64_t sdesc)
-{
-    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
-                 : "memory");
-}
-
 // Wide copies: 128 lanes x 32 bytes (8 TMEM columns) per instruction.  Each
 // tcgen05.cp costs the tensor pipe about the same whatever its width, so the
 // pair kernel moves its scales with these: the source holds, for lane l, the
@@ -112,9 +70,60 @@ __device__ __forceinline__ uint64_t sdesc_wide_scales(uint32_t saddr)
     return d;
 }
 
-__device__ __forceinline__ void tmem_cp_wide_pair(uint32_t taddr, uint64_t sdesc)
+// Warp-wide forms (elect.sync predicate on the instruction; see the
+// warp-wide MMA issue notes beside mma_bf16_w): the issuing loops run on a
+// whole warp and one elected lane issues.
+__device__ __forceinline__ void mma_mxf4_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
 {
-    asm volatile("tcgen05.cp.cta_group::2.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X "
+        "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_mxf4_pair_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X "
+        "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Copy one 512-byte scale chunk (32 lines x 16 bytes) from shared memory to
+// 4 TMEM columns, replicated into all four lane quarters.
+__device__ __forceinline__ void tmem_cp_chunk_w(uint32_t taddr, uint64_t sdesc)
+{
+    asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+                 "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;\n\t}" ::"r"(taddr), "l"(sdesc)
+                 : "memory");
+}
+
+// The same, issued by CTA 0 of a pair for both CTAs (each CTA's chunk at the
+// same shared-memory offset goes to that CTA's TMEM).
+__device__ __forceinline__ void tmem_cp_chunk_pair_w(uint32_t taddr, uint64_t sdesc)
+{
+    asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+                 "@e tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;\n\t}" ::"r"(taddr), "l"(sdesc)
+                 : "memory");
+}
+
+// One wide copy (128 lanes x 32 bytes, the layout of sdesc_wide_scales) for
+// both CTAs of a pair.
+__device__ __forceinline__ void tmem_cp_wide_pair_w(uint32_t taddr, uint64_t sdesc)
+{
+    asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+                 "@e tcgen05.cp.cta_group::2.128x256b [%0], %1;\n\t}" ::"r"(taddr), "l"(sdesc)
+                 : "memory");
 }
 
 // Programmatic dependent launch: the relayout pre-pass lets the GEMM start

@@ -212,53 +212,52 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            // ------------------------------------------------ MMA issuer
-            int stage = 0;
-            uint32_t phase = 0;
-            int local = 0;
-            bool ok = true;
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++local) {
-                const int acc = local & 1;
-                if (!mbar_wait(&tempty[acc], ((local >> 1) & 1) ^ 1u, err, abort_flag, kSiteMmaTmemEmpty))
+        // ---------------------------------------------------- MMA issuer
+        // (the whole warp runs the loop; one elected lane issues)
+        int stage = 0;
+        uint32_t phase = 0;
+        int local = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++local) {
+            const int acc = local & 1;
+            if (!mbar_wait_warp(&tempty[acc], ((local >> 1) & 1) ^ 1u, err, abort_flag, kSiteMmaTmemEmpty))
+                break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + acc * kAccCols;
+            for (int kb = 0; kb < num_kb; ++kb) {
+                if (!mbar_wait_warp(&full[stage], phase, err, abort_flag, kSiteMmaFull)) {
+                    ok = false;
                     break;
-                tc_fence_after();
-                const uint32_t d_tmem = tmem_base + acc * kAccCols;
-                for (int kb = 0; kb < num_kb; ++kb) {
-                    if (!mbar_wait(&full[stage], phase, err, abort_flag, kSiteMmaFull)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t sf_col = tmem_base + kSfCol0 + stage * kSfColsPerStage;
-#pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        tmem_cp_chunk(sf_col + c * 4,
-                                      sdesc_noswizzle_rows16(smem_u32(sfA + stage * kSfBytes + c * kSfChunk)));
-                        tmem_cp_chunk(sf_col + 8 + c * 4,
-                                      sdesc_noswizzle_rows16(smem_u32(sfB + stage * kSfBytes + c * kSfChunk)));
-                    }
-                    const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(tA + stage * kTileBytes));
-                    const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(tB + stage * kTileBytes));
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        // 64 codes = 32 bytes per MMA; scales (k/2) chunk, id 0 or 2
-                        const uint64_t koff = static_cast<uint64_t>((k * 32) >> 4);
-                        const int c = k >> 1;
-                        const uint32_t id = (k & 1) ? 2u : 0u;
-                        mma_mxf4(d_tmem, adesc + koff, bdesc + koff, idesc_mxf4(kBM, kBN, id),
-                                 sf_col + c * 4, sf_col + 8 + c * 4, (kb | k) != 0);
-                    }
-                    mma_commit(&empty[stage]);
-                    if (++stage == kStages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
                 }
-                if (!ok)
-                    break;
-                mma_commit(&tfull[acc]);
+                tc_fence_after();
+                const uint32_t sf_col = tmem_base + kSfCol0 + stage * kSfColsPerStage;
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    tmem_cp_chunk_w(sf_col + c * 4,
+                                    sdesc_noswizzle_rows16(smem_u32(sfA + stage * kSfBytes + c * kSfChunk)));
+                    tmem_cp_chunk_w(sf_col + 8 + c * 4,
+                                    sdesc_noswizzle_rows16(smem_u32(sfB + stage * kSfBytes + c * kSfChunk)));
+                }
+                const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(tA + stage * kTileBytes));
+                const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(tB + stage * kTileBytes));
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    // 64 codes = 32 bytes per MMA; scales (k/2) chunk, id 0 or 2
+                    const uint64_t koff = static_cast<uint64_t>((k * 32) >> 4);
+                    const int c = k >> 1;
+                    const uint32_t id = (k & 1) ? 2u : 0u;
+                    mma_mxf4_w(d_tmem, adesc + koff, bdesc + koff, idesc_mxf4(kBM, kBN, id),
+                               sf_col + c * 4, sf_col + 8 + c * 4, (kb | k) != 0);
+                }
+                mma_commit_w(&empty[stage]);
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
             }
+            if (!ok)
+                break;
+            mma_commit_w(&tfull[acc]);
         }
     } else {
         // ---------------------------------------------------- epilogue

@@ -236,8 +236,10 @@ __global__ void __launch_bounds__(pair_threads(ACC_BUFS), 1)
             }
         }
     } else if (warp == 1) {
-        if (lane == 0 && rank == 0) {
-            // ------------------------------------------------ MMA issuer
+        if (rank == 0) {
+            // -------------------------------------------- MMA issuer
+            // (warp 1 and warp 2 each run their loop on the whole warp; one
+            // elected lane issues)
             int stage = 0;
             uint32_t phase = 0;
             int local = 0;
@@ -245,13 +247,13 @@ __global__ void __launch_bounds__(pair_threads(ACC_BUFS), 1)
             for (int t = cluster; t < num_tiles && ok; t += nclusters, ++local) {
                 const int acc = local % ACC_BUFS;
                 const uint32_t use_phase = (local / ACC_BUFS) & 1;
-                if (!mbar_wait(&tempty[acc], use_phase ^ 1u, err, abort_flag, kSiteMmaTmemEmpty))
+                if (!mbar_wait_warp(&tempty[acc], use_phase ^ 1u, err, abort_flag, kSiteMmaTmemEmpty))
                     break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
                 for (int kb = 0; kb < num_kb; ++kb) {
                     // the stage's codes are in shared memory, its scales in TMEM
-                    if (!mbar_wait(&full[stage], phase, err, abort_flag, kSiteMmaFull)) {
+                    if (!mbar_wait_warp(&full[stage], phase, err, abort_flag, kSiteMmaFull)) {
                         ok = false;
                         break;
                     }
@@ -265,10 +267,10 @@ __global__ void __launch_bounds__(pair_threads(ACC_BUFS), 1)
                         const uint64_t koff = static_cast<uint64_t>((k * 32) >> 4);
                         const int c = k >> 1;
                         const uint32_t id = (k & 1) ? 2u : 0u;
-                        mma_mxf4_pair(d_tmem, adesc + koff, bdesc + koff, idesc_mxf4(kBM, BN, id), sfa_col + c * 4,
+                        mma_mxf4_pair_w(d_tmem, adesc + koff, bdesc + koff, idesc_mxf4(kBM, BN, id), sfa_col + c * 4,
                                       sfb_col + c * 4 * NSUB, (kb | k) != 0);
                     }
-                    mma_commit_pair(&empty[stage], 0x3);
+                    mma_commit_pair_w(&empty[stage], 0x3);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -276,18 +278,18 @@ __global__ void __launch_bounds__(pair_threads(ACC_BUFS), 1)
                 }
                 if (!ok)
                     break;
-                mma_commit_pair(&tfull[acc], 0x3);
+                mma_commit_pair_w(&tfull[acc], 0x3);
             }
         }
     } else if (warp == 2) {
-        if (lane == 0 && rank == 0) {
+        if (rank == 0) {
             // --------------------------------------------- scale copier
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
             for (int t = cluster; t < num_tiles && ok; t += nclusters) {
                 for (int kb = 0; kb < num_kb; ++kb) {
-                    if (!mbar_wait(&sfull[stage], phase, err, abort_flag, kSiteMmaFull)) {
+                    if (!mbar_wait_warp(&sfull[stage], phase, err, abort_flag, kSiteMmaFull)) {
                         ok = false;
                         break;
                     }
@@ -298,26 +300,26 @@ __global__ void __launch_bounds__(pair_threads(ACC_BUFS), 1)
                     // then B scales per K-block group (NSUB = 2) or both
                     // groups at once (NSUB = 1)
                     if constexpr (kWideScales) {
-                        tmem_cp_wide_pair(sfa_col, sdesc_wide_scales(smem_u32(sfA + stage * C::SFA_BYTES)));
+                        tmem_cp_wide_pair_w(sfa_col, sdesc_wide_scales(smem_u32(sfA + stage * C::SFA_BYTES)));
 #pragma unroll
                         for (int p = 0; p < NSUB; ++p)
-                            tmem_cp_wide_pair(sfb_col + 8 * p,
+                            tmem_cp_wide_pair_w(sfb_col + 8 * p,
                                               sdesc_wide_scales(smem_u32(sfB + stage * C::SFB_BYTES + p * kWideSrcBytes)));
                     } else {
                         // chunk c (scale blocks 4c..4c+3) of sub-block s
                         // -> columns c * 4 * NSUB + 4 s of the group
 #pragma unroll
                         for (int c = 0; c < 2; ++c) {
-                            tmem_cp_chunk_pair(sfa_col + 4 * c,
+                            tmem_cp_chunk_pair_w(sfa_col + 4 * c,
                                                sdesc_noswizzle_rows16(smem_u32(sfA + stage * C::SFA_BYTES + c * kSfChunk)));
 #pragma unroll
                             for (int sb = 0; sb < NSUB; ++sb)
-                                tmem_cp_chunk_pair(sfb_col + c * 4 * NSUB + 4 * sb,
+                                tmem_cp_chunk_pair_w(sfb_col + c * 4 * NSUB + 4 * sb,
                                                    sdesc_noswizzle_rows16(smem_u32(sfB + stage * C::SFB_BYTES +
                                                                                    sb * kSfBlock + c * kSfChunk)));
                         }
                     }
-                    mma_commit_pair(&full[stage], 0x1);
+                    mma_commit_pair_w(&full[stage], 0x1);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;

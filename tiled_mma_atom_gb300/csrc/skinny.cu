@@ -150,45 +150,44 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            const uint32_t idesc = idesc_bf16_f32(kTileN, mp);
-            int stage = 0;
-            uint32_t phase = 0;
-            int seg = 0;
-            bool ok = true;
-            for (int64_t u = u_begin; u < u_end && ok; ++seg) {
-                const int kb0 = static_cast<int>(u % KB);
-                const int kb1 = seg_end(kb0, KB, u_end - u);
-                const int acc = seg & 1;
-                if (!mbar_wait(&tempty[acc], ((seg >> 1) & 1) ^ 1u, err, abort_flag, kSiteMmaTmemEmpty))
+        // (the whole warp runs the issue loop; one elected lane issues)
+        const uint32_t idesc = idesc_bf16_f32(kTileN, mp);
+        int stage = 0;
+        uint32_t phase = 0;
+        int seg = 0;
+        bool ok = true;
+        for (int64_t u = u_begin; u < u_end && ok; ++seg) {
+            const int kb0 = static_cast<int>(u % KB);
+            const int kb1 = seg_end(kb0, KB, u_end - u);
+            const int acc = seg & 1;
+            if (!mbar_wait_warp(&tempty[acc], ((seg >> 1) & 1) ^ 1u, err, abort_flag, kSiteMmaTmemEmpty))
+                break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + acc * kMaxMP;
+            for (int kb = kb0; kb < kb1; ++kb) {
+                if (!mbar_wait_warp(&full[stage], phase, err, abort_flag, kSiteMmaFull)) {
+                    ok = false;
                     break;
-                tc_fence_after();
-                const uint32_t d_tmem = tmem_base + acc * kMaxMP;
-                for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!mbar_wait(&full[stage], phase, err, abort_flag, kSiteMmaFull)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    uint8_t *st = smem + stage * kStageBytes;
-                    const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(st));            // MMA "A": B rows
-                    const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(st + kBBytes));  // MMA "B": A rows
-#pragma unroll
-                    for (int k = 0; k < kBK / kUmmaK; ++k) {
-                        const uint64_t koff = static_cast<uint64_t>((k * kUmmaK * 2) >> 4);
-                        mma_bf16(d_tmem, bdesc + koff, adesc + koff, idesc, (kb != kb0) || (k != 0));
-                    }
-                    mma_commit(&empty[stage]);
-                    if (++stage == kStages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
                 }
-                if (!ok)
-                    break;
-                mma_commit(&tfull[acc]);
-                u += kb1 - kb0;
+                tc_fence_after();
+                uint8_t *st = smem + stage * kStageBytes;
+                const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(st));            // MMA "A": B rows
+                const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(st + kBBytes));  // MMA "B": A rows
+#pragma unroll
+                for (int k = 0; k < kBK / kUmmaK; ++k) {
+                    const uint64_t koff = static_cast<uint64_t>((k * kUmmaK * 2) >> 4);
+                    mma_bf16_w(d_tmem, bdesc + koff, adesc + koff, idesc, (kb != kb0) || (k != 0));
+                }
+                mma_commit_w(&empty[stage]);
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
             }
+            if (!ok)
+                break;
+            mma_commit_w(&tfull[acc]);
+            u += kb1 - kb0;
         }
     } else {
         // epilogue: thread owns B row n_local = 32 q + lane of the tile

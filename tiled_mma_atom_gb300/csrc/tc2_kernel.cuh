@@ -17,7 +17,8 @@
 //                 pair's byte count); waits on its own `empty` barrier.
 //   warp 1        CTA 0 only: issues the pair MMAs and commits with a
 //                 multicast arrive on the `empty` / `tmem_full` barriers of
-//                 both CTAs.  Both CTAs' warp 1 allocate TMEM together.
+//                 both CTAs (the whole warp runs the loop, one elected lane
+//                 issues).  Both CTAs' warp 1 allocate TMEM together.
 //   warps 2..     epilogue of this CTA's 128 accumulator rows (4 warps, or
 //                 8 with the fused epilogue, two per lane quarter splitting
 //                 the columns); each warp then arrives on CTA 0's
@@ -432,8 +433,9 @@ __global__ void __launch_bounds__(tc2_threads(EPI), 1)
             }
         }
     } else if (warp == 1) {
-        if (lane == 0 && rank == 0) {
-            // ------------------------------------------------ MMA issuer
+        if (rank == 0) {
+            // -------------------------------------------- MMA issuer
+            // (the whole warp runs the loop; one elected lane issues)
             constexpr uint32_t idesc = IN == kInE4m3 ? idesc_e4m3_f32(kBM, BN) : idesc_bf16_major(kBM, BN, MAJ);
             int stage = 0;
             uint32_t phase = 0;
@@ -446,12 +448,12 @@ __global__ void __launch_bounds__(tc2_threads(EPI), 1)
                 const int acc = local & 1;
                 const uint32_t acc_phase = (local >> 1) & 1;
                 ++local;
-                if (!mbar_wait_cluster(&tempty[acc], acc_phase ^ 1u, err, abort_flag, kSiteMmaTmemEmpty))
+                if (!mbar_wait_cluster_warp(&tempty[acc], acc_phase ^ 1u, err, abort_flag, kSiteMmaTmemEmpty))
                     break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
                 for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!mbar_wait_cluster(&full[stage], phase, err, abort_flag, kSiteMmaFull)) {
+                    if (!mbar_wait_cluster_warp(&full[stage], phase, err, abort_flag, kSiteMmaFull)) {
                         ok = false;
                         break;
                     }
@@ -465,11 +467,11 @@ __global__ void __launch_bounds__(tc2_threads(EPI), 1)
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         if constexpr (IN == kInE4m3)
-                            mma_e4m3_pair(d_tmem, adesc + k * astep, bdesc + k * bstep, idesc, (kb != kb0) || (k != 0));
+                            mma_e4m3_pair_w(d_tmem, adesc + k * astep, bdesc + k * bstep, idesc, (kb != kb0) || (k != 0));
                         else
-                            mma_bf16_pair(d_tmem, adesc + k * astep, bdesc + k * bstep, idesc, (kb != kb0) || (k != 0));
+                            mma_bf16_pair_w(d_tmem, adesc + k * astep, bdesc + k * bstep, idesc, (kb != kb0) || (k != 0));
                     }
-                    mma_commit_pair(&empty[stage], 0x3);
+                    mma_commit_pair_w(&empty[stage], 0x3);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -477,7 +479,7 @@ __global__ void __launch_bounds__(tc2_threads(EPI), 1)
                 }
                 if (!ok)
                     break;
-                mma_commit_pair(&tfull[acc], 0x3);
+                mma_commit_pair_w(&tfull[acc], 0x3);
             }
         }
     } else {

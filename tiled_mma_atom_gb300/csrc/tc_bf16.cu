@@ -13,8 +13,9 @@
 //                 loads (128-byte swizzle, out-of-range rows/columns read as
 //                 zero) into a STAGES-deep shared-memory ring; mbarriers
 //                 `full`/`empty` gate each stage.
-//   warp 1        MMA issuer: one lane issues tcgen05.mma (kind::f16, 128 x BN
-//                 x 16) from shared-memory descriptors into a TMEM
+//   warp 1        MMA issuer: the warp runs the loop and one elected lane
+//                 issues tcgen05.mma (kind::f16, 128 x BN x 16) from
+//                 shared-memory descriptors into a TMEM
 //                 accumulator; tcgen05.commit releases each stage and, at
 //                 tile end, hands the accumulator to the epilogue.  Warp 1 also
 //                 allocates and frees TMEM.
@@ -152,44 +153,43 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            // ------------------------------------------------ MMA issuer
-            constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN);
-            int stage = 0;
-            uint32_t phase = 0;
-            int local = 0;
-            bool ok = true;
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++local) {
-                const int acc = local & 1;
-                const uint32_t acc_phase = (local >> 1) & 1;
-                if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, err, abort_flag, kSiteMmaTmemEmpty))
+        // ---------------------------------------------------- MMA issuer
+        // (the whole warp runs the loop; one elected lane issues)
+        constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN);
+        int stage = 0;
+        uint32_t phase = 0;
+        int local = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++local) {
+            const int acc = local & 1;
+            const uint32_t acc_phase = (local >> 1) & 1;
+            if (!mbar_wait_warp(&tempty[acc], acc_phase ^ 1u, err, abort_flag, kSiteMmaTmemEmpty))
+                break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + acc * BN;
+            for (int kb = 0; kb < num_kb; ++kb) {
+                if (!mbar_wait_warp(&full[stage], phase, err, abort_flag, kSiteMmaFull)) {
+                    ok = false;
                     break;
-                tc_fence_after();
-                const uint32_t d_tmem = tmem_base + acc * BN;
-                for (int kb = 0; kb < num_kb; ++kb) {
-                    if (!mbar_wait(&full[stage], phase, err, abort_flag, kSiteMmaFull)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(sA + stage * C::A_BYTES));
-                    const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(sB + stage * C::B_BYTES));
-#pragma unroll
-                    for (int k = 0; k < kBK / kUmmaK; ++k) {
-                        // advance 32 bytes (16 bf16) along K inside the swizzle row
-                        const uint64_t koff = static_cast<uint64_t>((k * kUmmaK * 2) >> 4);
-                        mma_bf16(d_tmem, adesc + koff, bdesc + koff, idesc, (kb | k) != 0);
-                    }
-                    mma_commit(&empty[stage]);
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
                 }
-                if (!ok)
-                    break;
-                mma_commit(&tfull[acc]);
+                tc_fence_after();
+                const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(sA + stage * C::A_BYTES));
+                const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(sB + stage * C::B_BYTES));
+#pragma unroll
+                for (int k = 0; k < kBK / kUmmaK; ++k) {
+                    // advance 32 bytes (16 bf16) along K inside the swizzle row
+                    const uint64_t koff = static_cast<uint64_t>((k * kUmmaK * 2) >> 4);
+                    mma_bf16_w(d_tmem, adesc + koff, bdesc + koff, idesc, (kb | k) != 0);
+                }
+                mma_commit_w(&empty[stage]);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
             }
+            if (!ok)
+                break;
+            mma_commit_w(&tfull[acc]);
         }
     } else {
         // ---------------------------------------------------- epilogue

@@ -143,13 +143,16 @@ __device__ __forceinline__ void bulk_load_hint(void *smem_dst, const void *gsrc,
 
 // D[tmem] (+)= A[tmem] . B[smem]^T, E4M3 operands, one CTA (kind::f8f6f4,
 // K = 32 per instruction: 8 TMEM columns of A per row).
-__device__ __forceinline__ void mma_e4m3_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                            uint32_t accumulate)
+// Issued warp-wide: the elect.sync predicate picks one lane of the issuing
+// warp, which runs its loop in warp-uniform control flow.
+__device__ __forceinline__ void mma_e4m3_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate)
 {
     asm volatile(
-        "{\n\t.reg .pred p;\n\t"
+        "{\n\t.reg .pred p, e;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
@@ -372,56 +375,55 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1 || warp == kSecondMmaWarp) {
         const int j = warp == 1 ? 0 : 1;                       // issuer index
-        if (lane == 0) {
-            // ------------------------------------------------ MMA issuers
-            // MMA A = converted weights (TMEM, 128 rows), MMA B = A' (2 mp
-            // rows).  Issuer j takes the units i with i mod 2 = j into its
-            // own accumulators (acc_index: one, or two alternating over the
-            // segments it has units in).
-            const uint32_t idesc = idesc_e4m3_f32(kTileN, 2 * mp);
-            const int acc_cols = kAccRegion / (kIssuers * nacc);
-            int64_t i0 = 0;                                    // local index of the segment's first unit
-            int nseg = 0;                                      // segments this issuer took part in
-            bool ok = true;
-            for (int64_t u = u_begin; u < u_end && ok;) {
-                const int kb0 = static_cast<int>(u % KB);
-                const int kb1 = seg_end(kb0, KB, u_end - u);
-                const int64_t i1 = i0 + (kb1 - kb0);
-                if (issuer_has(i0, i1, j)) {
-                    const int acc = acc_index(j, nseg, nacc);
-                    if (!mbar_wait(&tempty[acc], acc_phase(nseg, nacc) ^ 1u, err, abort_flag, kSiteMmaTmemEmpty))
+        // ---------------------------------------------------- MMA issuers
+        // MMA A = converted weights (TMEM, 128 rows), MMA B = A' (2 mp
+        // rows).  Issuer j takes the units i with i mod 2 = j into its
+        // own accumulators (acc_index: one, or two alternating over the
+        // segments it has units in).  The whole warp runs the loop; one
+        // elected lane issues.
+        const uint32_t idesc = idesc_e4m3_f32(kTileN, 2 * mp);
+        const int acc_cols = kAccRegion / (kIssuers * nacc);
+        int64_t i0 = 0;                                    // local index of the segment's first unit
+        int nseg = 0;                                      // segments this issuer took part in
+        bool ok = true;
+        for (int64_t u = u_begin; u < u_end && ok;) {
+            const int kb0 = static_cast<int>(u % KB);
+            const int kb1 = seg_end(kb0, KB, u_end - u);
+            const int64_t i1 = i0 + (kb1 - kb0);
+            if (issuer_has(i0, i1, j)) {
+                const int acc = acc_index(j, nseg, nacc);
+                if (!mbar_wait_warp(&tempty[acc], acc_phase(nseg, nacc) ^ 1u, err, abort_flag, kSiteMmaTmemEmpty))
+                    break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * acc_cols;
+                bool first = true;
+                for (int64_t i = i0 + (static_cast<int>(i0 & 1) != j ? 1 : 0); i < i1; i += kIssuers) {
+                    const int wb = static_cast<int>(i % kWBufs);
+                    if (!mbar_wait_warp(&cready[wb], static_cast<uint32_t>((i / kWBufs) & 1), err, abort_flag,
+                                        kSiteMmaFull)) {
+                        ok = false;
                         break;
-                    tc_fence_after();
-                    const uint32_t d_tmem = tmem_base + acc * acc_cols;
-                    bool first = true;
-                    for (int64_t i = i0 + (static_cast<int>(i0 & 1) != j ? 1 : 0); i < i1; i += kIssuers) {
-                        const int wb = static_cast<int>(i % kWBufs);
-                        if (!mbar_wait(&cready[wb], static_cast<uint32_t>((i / kWBufs) & 1), err, abort_flag,
-                                       kSiteMmaFull)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t a_src = tmem_base + kWCol0 + wb * kWCols;
-                        const uint64_t bdesc0 = sdesc_kmajor_sw128(smem_u32(aring + wb * abytes));
-                        const uint64_t bdesc1 = sdesc_kmajor_sw128(smem_u32(aring + wb * abytes + abox));
-#pragma unroll
-                        for (int k = 0; k < kBK / 32; ++k) {
-                            const uint64_t bdesc =
-                                (k < 4 ? bdesc0 : bdesc1) + static_cast<uint64_t>(((k & 3) * 32) >> 4);
-                            mma_e4m3_ts(d_tmem, a_src + 8 * k, bdesc, idesc, !first || (k != 0));
-                        }
-                        first = false;
-                        mma_commit(&cfree[wb]);
                     }
-                    if (!ok)
-                        break;
-                    mma_commit(&tfull[acc]);
-                    ++nseg;
+                    tc_fence_after();
+                    const uint32_t a_src = tmem_base + kWCol0 + wb * kWCols;
+                    const uint64_t bdesc0 = sdesc_kmajor_sw128(smem_u32(aring + wb * abytes));
+                    const uint64_t bdesc1 = sdesc_kmajor_sw128(smem_u32(aring + wb * abytes + abox));
+#pragma unroll
+                    for (int k = 0; k < kBK / 32; ++k) {
+                        const uint64_t bdesc =
+                            (k < 4 ? bdesc0 : bdesc1) + static_cast<uint64_t>(((k & 3) * 32) >> 4);
+                        mma_e4m3_ts_w(d_tmem, a_src + 8 * k, bdesc, idesc, !first || (k != 0));
+                    }
+                    first = false;
+                    mma_commit_w(&cfree[wb]);
                 }
-                i0 = i1;
-                u += kb1 - kb0;
+                if (!ok)
+                    break;
+                mma_commit_w(&tfull[acc]);
+                ++nseg;
             }
+            i0 = i1;
+            u += kb1 - kb0;
         }
     } else if (warp >= kFirstConvWarp) {
         // ------------------------------------------------- converters
