@@ -173,43 +173,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem_base = *tmem_slot;
 
     if (warp == 0) {
-        if (lane == 0) {
-            // ---------------------------------------------- producer lane
-            int stage = 0;
-            uint32_t phase = 0;
-            int64_t issued = 0;
-            bool ok = true;
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-                int tm, tn;
-                tile_coords(t, tiles_m, tiles_n, tm, tn);
-                const uint8_t *sfa_src = relA + static_cast<int64_t>(tm) * num_kb * kSfBytes;
-                const uint8_t *sfb_src = relB + static_cast<int64_t>(tn) * num_kb * kSfBytes;
-                for (int kb = 0; kb < num_kb; ++kb) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1u, err, abort_flag, kSiteProducerEmpty)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(&full[stage], 2 * kTileBytes + 2 * kSfBytes);
-                    tma_load_2d(tA + stage * kTileBytes, &tmA, &full[stage], kb * kBKBytes, tm * kBM);
-                    tma_load_2d(tB + stage * kTileBytes, &tmB, &full[stage], kb * kBKBytes, tn * kBN);
-                    bulk_load(sfA + stage * kSfBytes, sfa_src + kb * kSfBytes, kSfBytes, &full[stage]);
-                    bulk_load(sfB + stage * kSfBytes, sfb_src + kb * kSfBytes, kSfBytes, &full[stage]);
-                    ++issued;
-                    if (++stage == kStages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+        // ---------------------------------------------- producer
+        int stage = 0;
+        uint32_t phase = 0;
+        int64_t issued = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+            int tm, tn;
+            tile_coords(t, tiles_m, tiles_n, tm, tn);
+            const uint8_t *sfa_src = relA + static_cast<int64_t>(tm) * num_kb * kSfBytes;
+            const uint8_t *sfb_src = relB + static_cast<int64_t>(tn) * num_kb * kSfBytes;
+            for (int kb = 0; kb < num_kb; ++kb) {
+                if (!mbar_wait_warp(&empty[stage], phase ^ 1u, err, abort_flag, kSiteProducerEmpty)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx_w(&full[stage], 2 * kTileBytes + 2 * kSfBytes);
+                tma_load_2d_w(tA + stage * kTileBytes, &tmA, &full[stage], kb * kBKBytes, tm * kBM);
+                tma_load_2d_w(tB + stage * kTileBytes, &tmB, &full[stage], kb * kBKBytes, tn * kBN);
+                bulk_load_w(sfA + stage * kSfBytes, sfa_src + kb * kSfBytes, kSfBytes, &full[stage]);
+                bulk_load_w(sfB + stage * kSfBytes, sfb_src + kb * kSfBytes, kSfBytes, &full[stage]);
+                ++issued;
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1u;
                 }
             }
-            for (int i = 0; i < kStages && i < issued; ++i) {
-                int s = stage - 1 - i;
-                uint32_t ph = phase;
-                if (s < 0) {
-                    s += kStages;
-                    ph ^= 1u;
-                }
-                mbar_wait(&full[s], ph, err, nullptr, kSiteDrain);
+        }
+        for (int i = 0; i < kStages && i < issued; ++i) {
+            int s = stage - 1 - i;
+            uint32_t ph = phase;
+            if (s < 0) {
+                s += kStages;
+                ph ^= 1u;
             }
+            mbar_wait(&full[s], ph, err, nullptr, kSiteDrain);
         }
     } else if (warp == 1) {
         // ---------------------------------------------------- MMA issuer

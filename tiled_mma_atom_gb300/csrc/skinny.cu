@@ -111,43 +111,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem_base = *tmem_slot;
 
     if (warp == 0) {
-        if (lane == 0) {
-            const uint64_t keep_a = policy_evict_last();   // A is re-read by every CTA
-            const uint64_t stream_b = policy_evict_first(); // B is read once
-            int stage = 0;
-            uint32_t phase = 0;
-            int64_t issued = 0;
-            bool ok = true;
-            for (int64_t u = u_begin; u < u_end && ok;) {
-                const int tile = static_cast<int>(u / KB);
-                const int kb0 = static_cast<int>(u % KB);
-                const int kb1 = seg_end(kb0, KB, u_end - u);
-                for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1u, err, abort_flag, kSiteProducerEmpty)) {
-                        ok = false;
-                        break;
-                    }
-                    uint8_t *st = smem + stage * kStageBytes;
-                    mbar_arrive_expect_tx(&full[stage], kBBytes + a_bytes);
-                    tma_load_2d_hint(st, &tmB, &full[stage], kb * kBK, tile * kTileN, stream_b);
-                    tma_load_2d_hint(st + kBBytes, &tmA, &full[stage], kb * kBK, 0, keep_a);
-                    ++issued;
-                    if (++stage == kStages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+        const uint64_t keep_a = policy_evict_last();   // A is re-read by every CTA
+        const uint64_t stream_b = policy_evict_first(); // B is read once
+        int stage = 0;
+        uint32_t phase = 0;
+        int64_t issued = 0;
+        bool ok = true;
+        for (int64_t u = u_begin; u < u_end && ok;) {
+            const int tile = static_cast<int>(u / KB);
+            const int kb0 = static_cast<int>(u % KB);
+            const int kb1 = seg_end(kb0, KB, u_end - u);
+            for (int kb = kb0; kb < kb1; ++kb) {
+                if (!mbar_wait_warp(&empty[stage], phase ^ 1u, err, abort_flag, kSiteProducerEmpty)) {
+                    ok = false;
+                    break;
                 }
-                u += kb1 - kb0;
-            }
-            for (int i = 0; i < kStages && i < issued; ++i) {
-                int s = stage - 1 - i;
-                uint32_t ph = phase;
-                if (s < 0) {
-                    s += kStages;
-                    ph ^= 1u;
+                uint8_t *st = smem + stage * kStageBytes;
+                mbar_arrive_expect_tx_w(&full[stage], kBBytes + a_bytes);
+                tma_load_2d_hint_w(st, &tmB, &full[stage], kb * kBK, tile * kTileN, stream_b);
+                tma_load_2d_hint_w(st + kBBytes, &tmA, &full[stage], kb * kBK, 0, keep_a);
+                ++issued;
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1u;
                 }
-                mbar_wait(&full[s], ph, err, nullptr, kSiteDrain);
             }
+            u += kb1 - kb0;
+        }
+        for (int i = 0; i < kStages && i < issued; ++i) {
+            int s = stage - 1 - i;
+            uint32_t ph = phase;
+            if (s < 0) {
+                s += kStages;
+                ph ^= 1u;
+            }
+            mbar_wait(&full[s], ph, err, nullptr, kSiteDrain);
         }
     } else if (warp == 1) {
         // (the whole warp runs the issue loop; one elected lane issues)

@@ -17,8 +17,9 @@
 //                 pair's byte count); waits on its own `empty` barrier.
 //   warp 1        CTA 0 only: issues the pair MMAs and commits with a
 //                 multicast arrive on the `empty` / `tmem_full` barriers of
-//                 both CTAs (the whole warp runs the loop, one elected lane
-//                 issues).  Both CTAs' warp 1 allocate TMEM together.
+//                 both CTAs.  Both CTAs' warp 1 allocate TMEM together.
+//                 Warps 0 and 1 run their loops on all 32 lanes; one elected
+//                 lane issues each copy, MMA and commit.
 //   warps 2..     epilogue of this CTA's 128 accumulator rows (4 warps, or
 //                 8 with the fused epilogue, two per lane quarter splitting
 //                 the columns); each warp then arrives on CTA 0's
@@ -373,64 +374,62 @@ __global__ void __launch_bounds__(tc2_threads(EPI), 1)
     const uint32_t tmem_base = *tmem_slot;
 
     if (warp == 0) {
-        if (lane == 0) {
-            // ---------------------------------------------- TMA producer
-            int stage = 0;
-            uint32_t phase = 0;
-            int64_t issued = 0;
-            bool ok = true;
-            SegWalk walk(cluster, nclusters, dp_tiles, sk_tiles, num_kb);
-            int tile, kb0, kb1, slot;
-            bool partial;
-            while (ok && walk.next(tile, kb0, kb1, partial, slot)) {
-                int tm, tn;
-                tile_coords(tile, tiles_m, tiles_n, tm, tn);
-                for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!mbar_wait_cluster(&empty[stage], phase ^ 1u, err, abort_flag, kSiteProducerEmpty)) {
-                        ok = false;
-                        break;
-                    }
-                    if (rank == 0)
-                        mbar_arrive_expect_tx(&full[stage], STAGE_TX);
-                    const uint32_t bar0 = mapa_shared(smem_u32(&full[stage]), 0);
-                    const int a_row = tm * kBM + rank * kHalfM, b_row = tn * BN + rank * (BN / 2);
-                    if constexpr (MAJ & 1) {
-#pragma unroll
-                        for (int j = 0; j < kHalfM / kMnBox; ++j)
-                            tma_load_2d_pair(sA + stage * C::A_BYTES + j * kMnBoxBytes, &tmA, bar0, a_row + j * kMnBox,
-                                             kb * KB_ELEMS);
-                    } else {
-                        tma_load_2d_pair(sA + stage * C::A_BYTES, &tmA, bar0, kb * KB_ELEMS, a_row);
-                    }
-                    if constexpr ((MAJ & 2) != 0) {
-#pragma unroll
-                        for (int j = 0; j < (BN / 2) / kMnBox; ++j)
-                            tma_load_2d_pair(sB + stage * C::B_BYTES + j * kMnBoxBytes, &tmB, bar0, b_row + j * kMnBox,
-                                             kb * KB_ELEMS);
-                    } else {
-                        tma_load_2d_pair(sB + stage * C::B_BYTES, &tmB, bar0, kb * KB_ELEMS, b_row);
-                    }
-                    ++issued;
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-            }
-            // Tail: wait until the MMA has released every stage this CTA
-            // filled (so no multicast arrive is still on its way here), and
-            // in CTA 0 until every load of the pair has landed.
-            for (int i = 0; i < STAGES && i < issued; ++i) {
-                int s = stage - 1 - i;
-                uint32_t ph = phase;
-                if (s < 0) {
-                    s += STAGES;
-                    ph ^= 1u;
+        // ---------------------------------------------- TMA producer
+        int stage = 0;
+        uint32_t phase = 0;
+        int64_t issued = 0;
+        bool ok = true;
+        SegWalk walk(cluster, nclusters, dp_tiles, sk_tiles, num_kb);
+        int tile, kb0, kb1, slot;
+        bool partial;
+        while (ok && walk.next(tile, kb0, kb1, partial, slot)) {
+            int tm, tn;
+            tile_coords(tile, tiles_m, tiles_n, tm, tn);
+            for (int kb = kb0; kb < kb1; ++kb) {
+                if (!mbar_wait_cluster_warp(&empty[stage], phase ^ 1u, err, abort_flag, kSiteProducerEmpty)) {
+                    ok = false;
+                    break;
                 }
                 if (rank == 0)
-                    mbar_wait_cluster(&full[s], ph, err, abort_flag, kSiteDrain);
-                mbar_wait_cluster(&empty[s], ph, err, abort_flag, kSiteDrain);
+                    mbar_arrive_expect_tx_w(&full[stage], STAGE_TX);
+                const uint32_t bar0 = mapa_shared(smem_u32(&full[stage]), 0);
+                const int a_row = tm * kBM + rank * kHalfM, b_row = tn * BN + rank * (BN / 2);
+                if constexpr (MAJ & 1) {
+#pragma unroll
+                    for (int j = 0; j < kHalfM / kMnBox; ++j)
+                        tma_load_2d_pair_w(sA + stage * C::A_BYTES + j * kMnBoxBytes, &tmA, bar0, a_row + j * kMnBox,
+                                           kb * KB_ELEMS);
+                } else {
+                    tma_load_2d_pair_w(sA + stage * C::A_BYTES, &tmA, bar0, kb * KB_ELEMS, a_row);
+                }
+                if constexpr ((MAJ & 2) != 0) {
+#pragma unroll
+                    for (int j = 0; j < (BN / 2) / kMnBox; ++j)
+                        tma_load_2d_pair_w(sB + stage * C::B_BYTES + j * kMnBoxBytes, &tmB, bar0, b_row + j * kMnBox,
+                                           kb * KB_ELEMS);
+                } else {
+                    tma_load_2d_pair_w(sB + stage * C::B_BYTES, &tmB, bar0, kb * KB_ELEMS, b_row);
+                }
+                ++issued;
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
             }
+        }
+        // Tail: wait until the MMA has released every stage this CTA
+        // filled (so no multicast arrive is still on its way here), and
+        // in CTA 0 until every load of the pair has landed.
+        for (int i = 0; i < STAGES && i < issued; ++i) {
+            int s = stage - 1 - i;
+            uint32_t ph = phase;
+            if (s < 0) {
+                s += STAGES;
+                ph ^= 1u;
+            }
+            if (rank == 0)
+                mbar_wait_cluster(&full[s], ph, err, abort_flag, kSiteDrain);
+            mbar_wait_cluster(&empty[s], ph, err, abort_flag, kSiteDrain);
         }
     } else if (warp == 1) {
         if (rank == 0) {

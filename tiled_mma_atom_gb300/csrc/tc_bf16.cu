@@ -9,19 +9,21 @@
 // overlap the MFMAs of step k (§3 "Runtime Loops with Loop-Carried Values"),
 // and a direct row-major or LDS-shuffled epilogue.  On sm_103a the same roles
 // map onto dedicated hardware:
-//   warp 0        TMA producer: one lane issues cp.async.bulk.tensor tile
-//                 loads (128-byte swizzle, out-of-range rows/columns read as
-//                 zero) into a STAGES-deep shared-memory ring; mbarriers
-//                 `full`/`empty` gate each stage.
-//   warp 1        MMA issuer: the warp runs the loop and one elected lane
-//                 issues tcgen05.mma (kind::f16, 128 x BN x 16) from
-//                 shared-memory descriptors into a TMEM
+//   warp 0        TMA producer: one elected lane issues cp.async.bulk.tensor
+//                 tile loads (128-byte swizzle, out-of-range rows/columns
+//                 read as zero) into a STAGES-deep shared-memory ring;
+//                 mbarriers `full`/`empty` gate each stage.
+//   warp 1        MMA issuer: one elected lane issues tcgen05.mma
+//                 (kind::f16, 128 x BN x 16) from shared-memory descriptors
+//                 into a TMEM
 //                 accumulator; tcgen05.commit releases each stage and, at
 //                 tile end, hands the accumulator to the epilogue.  Warp 1 also
 //                 allocates and frees TMEM.
 //   warps 2..5    epilogue: tcgen05.ld TMEM -> registers (warp w reads TMEM
 //                 lanes 32(w%4)..32(w%4)+31 = tile rows), fp32 -> bf16 round to
 //                 nearest even, 16-byte stores.
+// Warps 0 and 1 run their loops on all 32 lanes in warp-uniform control flow;
+// each TMA copy, tcgen05.mma and commit carries an elect.sync predicate.
 // Two TMEM accumulators (2 x BN columns) let the epilogue of tile i overlap
 // the mainloop of tile i+1.  The grid is one CTA per SM; CTA c takes tiles
 // c, c + grid, ... in a grouped order (8 M-tiles per group) so concurrently
@@ -110,47 +112,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem_base = *tmem_slot;
 
     if (warp == 0) {
-        if (lane == 0) {
-            // ---------------------------------------------- TMA producer
-            int stage = 0;
-            uint32_t phase = 0;
-            bool ok = true;
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-                int tm, tn;
-                tile_coords(t, tiles_m, tiles_n, tm, tn);
-                for (int kb = 0; kb < num_kb; ++kb) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1u, err, abort_flag, kSiteProducerEmpty)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-                    tma_load_2d(sA + stage * C::A_BYTES, &tmA, &full[stage], kb * kBK, tm * kBM);
-                    tma_load_2d(sB + stage * C::B_BYTES, &tmB, &full[stage], kb * kBK, tn * BN);
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-            }
-            // Drain: every load issued must have landed before the CTA may
-            // exit.  On the normal path the MMA warp consumed them all and
-            // these waits return at once.
-            for (int i = 0; i < STAGES; ++i) {
-                // the stage before `stage` in ring order, walking backwards
-                int s = stage - 1 - i;
-                uint32_t ph = phase;
-                if (s < 0) {
-                    s += STAGES;
-                    ph ^= 1u;
-                }
-                // only stages that were ever filled
-                const int64_t issued = static_cast<int64_t>(num_kb) *
-                                       ((num_tiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
-                                        static_cast<int>(gridDim.x));
-                if (i >= issued)
+        // ---------------------------------------------- TMA producer
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+            int tm, tn;
+            tile_coords(t, tiles_m, tiles_n, tm, tn);
+            for (int kb = 0; kb < num_kb; ++kb) {
+                if (!mbar_wait_warp(&empty[stage], phase ^ 1u, err, abort_flag, kSiteProducerEmpty)) {
+                    ok = false;
                     break;
-                mbar_wait(&full[s], ph, err, nullptr, kSiteDrain);
+                }
+                mbar_arrive_expect_tx_w(&full[stage], C::STAGE_BYTES);
+                tma_load_2d_w(sA + stage * C::A_BYTES, &tmA, &full[stage], kb * kBK, tm * kBM);
+                tma_load_2d_w(sB + stage * C::B_BYTES, &tmB, &full[stage], kb * kBK, tn * BN);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
             }
+        }
+        // Drain: every load issued must have landed before the CTA may
+        // exit.  On the normal path the MMA warp consumed them all and
+        // these waits return at once.
+        for (int i = 0; i < STAGES; ++i) {
+            // the stage before `stage` in ring order, walking backwards
+            int s = stage - 1 - i;
+            uint32_t ph = phase;
+            if (s < 0) {
+                s += STAGES;
+                ph ^= 1u;
+            }
+            // only stages that were ever filled
+            const int64_t issued = static_cast<int64_t>(num_kb) *
+                                   ((num_tiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                                    static_cast<int>(gridDim.x));
+            if (i >= issued)
+                break;
+            mbar_wait(&full[s], ph, err, nullptr, kSiteDrain);
         }
     } else if (warp == 1) {
         // ---------------------------------------------------- MMA issuer
