@@ -62,8 +62,10 @@ def test_debug_build_runs_every_family_clean(dbg, monkeypatch):
     # bf16 tensor cores: one CTA, CTA pairs with a stream-K tail, skinny
     _bf16_case(t, 200, 300, 136, 3, path="tc_single")
     monkeypatch.setenv("TMG_TC_PAIR_BN", "128")
+    monkeypatch.setenv("TMG_TC_PAIR_SCHED", "sk")
     _bf16_case(t, 520, 600, 256, 5, path="tc_pair")
     monkeypatch.delenv("TMG_TC_PAIR_BN")
+    monkeypatch.delenv("TMG_TC_PAIR_SCHED")
     _bf16_case(t, 24, 3000, 1000, 7, path="skinny")
     # MXFP4 on CTA pairs and on one CTA
     for kernel in ("pair", "single"):

@@ -61,12 +61,17 @@ def test_fused_vs_oracle(tmg, kind, epi):
                               float(sa.max()), float(sb.max()))
 
 
+@pytest.mark.parametrize("width", [224, 256])
 @pytest.mark.parametrize("kind", sorted(KINDS))
-def test_fused_integer_exact_through_stream_k(tmg, kind):
+def test_fused_integer_exact_through_stream_k(tmg, kind, width, monkeypatch):
     """Integer inputs, power-of-two scales, integer bias, relu: every step is
     exact in fp32, so D must be the bf16 rounding of the exact value, bit for
     bit.  2048 x 2560 leaves a partial last wave: its tiles are summed from
-    stream-K partials before the epilogue.  Twice: the counters reset."""
+    stream-K partials before the epilogue (224-wide tiles: the epilogue warps
+    of a lane quarter split 7 column chunks 4 + 3).  Twice: the counters
+    reset."""
+    monkeypatch.setenv("TMG_TC_PAIR_BN", str(width))
+    monkeypatch.setenv("TMG_TC_PAIR_SCHED", "sk")
     _, dt, odt = KINDS[kind]
     M, N, K = 2048, 2560, 1024
     A = inputs.integer_valued(M, K, 311, dtype=dt)

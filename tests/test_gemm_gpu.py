@@ -205,12 +205,15 @@ def test_tc_pair_each_tile_width_vs_oracle(tmg, shape, width):
     parity.check_bf16(D, parity.ref_full(A, B, oracle.BF16), K, parity.absmax(A), parity.absmax(B))
 
 
+@pytest.mark.parametrize("sched", ["sk", "dp"])
 @pytest.mark.parametrize("width", [128, 192, 224, 256])
-def test_tc_pair_stream_k_tail_exact(tmg, width, monkeypatch):
-    """2048 x 2560 leaves a partial last wave for every pair tile width, so
-    the last tiles run stream-K and are summed from fp32 partials.  Integer
-    inputs: bit-exact; twice in a row (the tile counters reset themselves)."""
+def test_tc_pair_stream_k_tail_exact(tmg, width, sched, monkeypatch):
+    """2048 x 2560 leaves a partial last wave for every pair tile width: with
+    a stream-K tail the last tiles are summed from fp32 partials, data-parallel
+    the last wave leaves pairs idle.  Integer inputs: bit-exact; twice in a row
+    (the tile counters reset themselves)."""
     monkeypatch.setenv("TMG_TC_PAIR_BN", str(width))
+    monkeypatch.setenv("TMG_TC_PAIR_SCHED", sched)
     M, N, K = 2048, 2560, 1024
     A = inputs.integer_valued(M, K, 200 + width)
     B = inputs.integer_valued(N, K, 201 + width)
@@ -222,9 +225,11 @@ def test_tc_pair_stream_k_tail_exact(tmg, width, monkeypatch):
     parity.check_exact_bf16(parity.bf16_bits(D2), parity.ref_full(A, B, oracle.BF16))
 
 
-def test_tc_pair_stream_k_random_vs_oracle(tmg):
+def test_tc_pair_stream_k_random_vs_oracle(tmg, monkeypatch):
     """Random inputs through the stream-K tail (4096 x 4096 has 256 tiles of
     256 columns over 76 pairs); sampled outputs in the split tiles' region."""
+    monkeypatch.setenv("TMG_TC_PAIR_BN", "256")
+    monkeypatch.setenv("TMG_TC_PAIR_SCHED", "sk")
     M, N, K = 4096, 4096, 512
     A = inputs.normal_bf16(M, K, 211)
     B = inputs.normal_bf16(N, K, 212)

@@ -438,6 +438,18 @@ tmg_status tc2_scratch(int dev, cudaStream_t s, TcArgs &a)
     return TMG_OK;
 }
 
+// Testing aid: TMG_TC_PAIR_BN = 128 | 192 | 224 | 256 forces the pair-tile
+// width of the plain and fused pair kernels.
+int pair_bn_override(int bn)
+{
+    if (const char *f = getenv("TMG_TC_PAIR_BN")) {
+        const int v = atoi(f);
+        if (v == 128 || v == 192 || v == 224 || v == 256)
+            return v;
+    }
+    return bn;
+}
+
 tmg_status run_tc(const DeviceState &ds, const TcPlan &p, void *D, int64_t K, int mode, cudaStream_t s)
 {
     TcArgs a;
@@ -446,17 +458,12 @@ tmg_status run_tc(const DeviceState &ds, const TcPlan &p, void *D, int64_t K, in
     // smaller problems keep more SMs busy with one-CTA 128-row tiles.
     bool pair = mode == 2;
     if (mode == 0 && p.M >= 256) {
-        const int bn2 = tc2_pick_bn(p.M, p.N, ds.num_sms);
+        const int bn2 = tc2_pick_bn(p.M, p.N, K, ds.num_sms);
         pair = ((p.M + 255) / 256) * ((p.N + bn2 - 1) / bn2) >= ds.num_sms / 2;
     }
     int box_b;
     if (pair) {
-        a.bn = tc2_pick_bn(p.M, p.N, ds.num_sms);
-        if (const char *f = getenv("TMG_TC_PAIR_BN")) {      // testing aid: 128 | 192 | 224 | 256
-            const int v = atoi(f);
-            if (v == 128 || v == 192 || v == 224 || v == 256)
-                a.bn = v;
-        }
+        a.bn = pair_bn_override(tc2_pick_bn(p.M, p.N, K, ds.num_sms));
         box_b = a.bn / 2;
     } else {
         // widest tile that still gives every SM work; 64 for small problems
@@ -590,7 +597,9 @@ bool run_tc2_inplace(const DeviceState &ds, const void *A, const void *B, void *
     TcArgs a;
     std::memset(&a, 0, sizeof a);
     a.maj = maj;
-    a.bn = (maj & 2) ? (N >= 256 ? 256 : 128) : tc2_pick_bn(M, N, ds.num_sms);
+    // the MN-major kernels are built at widths 256 and 128 only
+    static const int kMnWidths[2] = {256, 128};
+    a.bn = (maj & 2) ? (N >= 256 ? 256 : 128) : tc2_pick_bn_of(M, N, K, 64, ds.num_sms, kMnWidths, 2);
     if (((M + 255) / 256) * ((N + a.bn - 1) / a.bn) < ds.num_sms / 2)
         return false;                                     // too few pair tiles
     if ((*st = (maj & 1) ? encode_2d(&a.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, M, K, lds[0], 64, 64)
@@ -1005,8 +1014,8 @@ tmg_status tmg_gemm_fused(const void *A, const void *B, void *D, int64_t M, int6
                     "a multiple of 16)", elem);
     TcArgs a;
     std::memset(&a, 0, sizeof a);
-    a.bn = tc2_fused_pick_bn(N);
     a.kb_elems = e4m3 ? 128 : 64;
+    a.bn = pair_bn_override(tc2_pick_bn_of(M, N, K, a.kb_elems, ds->num_sms, kTc2FusedWidths, 4));
     const CUtensorMapDataType dt = e4m3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     if ((st = encode_2d(&a.tmA, dt, elem, A, K, M, K, a.kb_elems, 128)) != TMG_OK)
         return st;
@@ -1117,8 +1126,8 @@ tmg_status gemm_w4a8_impl(const void *A, const void *B, bool shuffled, void *D, 
         const int64_t kc = K - k0 < kSeg ? K - k0 : kSeg;
         TcArgs a;
         std::memset(&a, 0, sizeof a);
-        a.bn = tc2_fused_pick_bn(N);
         a.kb_elems = 64;
+        a.bn = tc2_pick_bn_of(M, N, kc, 64, ds->num_sms, kTc2FusedWidths, 4);
         const uint16_t *pa = static_cast<const uint16_t *>(PA) + k0, *pb = static_cast<const uint16_t *>(PB) + k0;
         if ((st = encode_2d(&a.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pa, kc, M, ldp, 64, 128)) != TMG_OK)
             return st;

@@ -66,8 +66,12 @@ cudaError_t launch_tc_bf16(const TcArgs &a, int num_sms, const ErrCtx &err, cuda
 // CTA-pair variant (cta_group::2, 256 x bn tiles; bn in {256, 224, 192, 128},
 // tmB box {64, bn/2}).  Call tc2_plan first, then provide the scratch.
 cudaError_t launch_tc2_bf16(const TcArgs &a, int num_sms, const ErrCtx &err, cudaStream_t s);
-// Pair-tile width for an M x N output.
-int tc2_pick_bn(int64_t M, int64_t N, int num_sms);
+// Pair-tile width for an M x N x K product (64-element K blocks), from the
+// widths 256 / 224 / 192 / 128; tc2_pick_bn_of chooses among `cands` for
+// K blocks of kb_elems elements.  The same cost model decides, in
+// tc2_plan, between a data-parallel schedule and a stream-K tail.
+int tc2_pick_bn(int64_t M, int64_t N, int64_t K, int num_sms);
+int tc2_pick_bn_of(int64_t M, int64_t N, int64_t K, int kb_elems, int num_sms, const int *cands, int nc);
 
 // Fused epilogue of the pair kernel: D = bf16(act(acc * scale_a[m] *
 // scale_b[n] + bias[n])); scale_a / scale_b may be null (factor 1), bias is
@@ -82,10 +86,11 @@ struct Tc2Epi {
 };
 // Pair kernel with the fused epilogue (tc2_fused.cu); bf16 or E4M3 inputs
 // (tmA/tmB over bytes for E4M3, box {128, rows}; a.kb_elems = 128);
-// a.bn in {256, 128}.  Call tc2_plan first, then provide the scratch.
+// a.bn one of kTc2FusedWidths.  Call tc2_plan first, then provide the
+// scratch.
 cudaError_t launch_tc2_fused(const TcArgs &a, const Tc2Epi &e, bool in_e4m3, const ErrCtx &err,
                              cudaStream_t s);
-int tc2_fused_pick_bn(int64_t N);
+extern const int kTc2FusedWidths[4];
 // W4A8 operands: A (M, K) int8 and B (N, K/2) packed int4 unpacked to bf16
 // (M, ldp) and (N, ldp), zero-padded past K; ldp a multiple of 8.
 cudaError_t launch_unpack_w4a8(const void *A, const void *B, int64_t M, int64_t N, int64_t K, void *PA, void *PB,
@@ -128,7 +133,8 @@ cudaError_t launch_w4a8_skinny(const W4a8SkinnyArgs &a, const ErrCtx &err, cudaS
 
 // D[m,n] = bf16(act(bias[n])) (or 0 without a bias): the fused GEMM at K = 0.
 cudaError_t launch_fused_k0(void *D, int64_t M, int64_t N, const Tc2Epi &e, cudaStream_t s);
-// Fill pairs / dp_tiles / sk_tiles for a.M, a.N, a.K, a.bn.
+// Fill pairs / dp_tiles / sk_tiles for a.M, a.N, a.K, a.bn: data-parallel,
+// or a stream-K tail where the cost model expects it to pay.
 void tc2_plan(TcArgs &a, int num_sms);
 size_t tc2_partials_bytes(const TcArgs &a);
 size_t tc2_counters_bytes(const TcArgs &a);

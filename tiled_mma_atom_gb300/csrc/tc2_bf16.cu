@@ -1,9 +1,61 @@
 // tc2_bf16.cu — the bf16 GEMM on CTA pairs (kernel in tc2_kernel.cuh):
 // the launches of the plain bf16 kernels, the schedule plan (data-parallel
 // tiles and the stream-K tail) and the tile-width choice.
+#include <algorithm>
+#include <cstdlib>
+
 #include "tc2_kernel.cuh"
 
 namespace tmg {
+
+// Estimated time of the pair kernel in ns (up to a constant) for 256 x bn
+// tiles over `pairs` CTA pairs, data-parallel (each pair takes whole tiles,
+// the last wave possibly partial) or with a stream-K tail (the last full
+// wave and the partial one split into equal runs of K blocks, summed from
+// fp32 partials).  Per K block of one tile, measured on GB300 (bf16, L2
+// flushed, sweep of M 2048-8192, N 1024-8192, K 2048-4096): 204 / 244 / 281
+// / 320 ns at widths 128 / 192 / 224 / 256; a stream-K tail adds about 10 us
+// (the partials' traffic and the ordered fix-up), so it pays only where a
+// data-parallel last wave would leave many pairs idle for many K blocks.
+static double tc2_kb_cost(int bn)
+{
+    return bn <= 128 ? 204.0 : bn <= 192 ? 244.0 : bn <= 224 ? 281.0 : 320.0;
+}
+
+static bool tc2_sk_possible(int64_t tiles, int num_kb, int pairs)
+{
+    if (tiles % pairs == 0)
+        return false;
+    const int64_t full_waves = tiles / pairs;
+    const int64_t sk = tiles - (full_waves > 0 ? full_waves - 1 : 0) * pairs;
+    return sk * num_kb >= pairs;
+}
+
+static double tc2_est(int64_t M, int64_t N, int num_kb, int bn, int pairs, bool sk)
+{
+    const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + bn - 1) / bn);
+    const double c = tc2_kb_cost(bn) * num_kb;
+    if (sk && tc2_sk_possible(tiles, num_kb, pairs))
+        return static_cast<double>(tiles) / pairs * c + 10000.0;
+    return static_cast<double>((tiles + pairs - 1) / pairs) * c;
+}
+
+static int tc2_best_bn(int64_t M, int64_t N, int64_t K, int kb_elems, int num_sms, const int *cands, int nc)
+{
+    const int pairs = num_sms / 2;
+    const int num_kb = static_cast<int>((K + kb_elems - 1) / kb_elems);
+    int best = cands[0];
+    double best_t = -1.0;
+    for (int i = 0; i < nc; ++i) {
+        const double t = std::min(tc2_est(M, N, num_kb, cands[i], pairs, false),
+                                  tc2_est(M, N, num_kb, cands[i], pairs, true));
+        if (best_t < 0.0 || t < best_t) {
+            best_t = t;
+            best = cands[i];
+        }
+    }
+    return best;
+}
 
 void tc2_plan(TcArgs &a, int num_sms)
 {
@@ -11,21 +63,19 @@ void tc2_plan(TcArgs &a, int num_sms)
     const int tiles = ((a.M + kBM - 1) / kBM) * ((a.N + a.bn - 1) / a.bn);
     const int kbe = a.kb_elems > 0 ? a.kb_elems : 64;
     const int num_kb = (a.K + kbe - 1) / kbe;
-    const int full_waves = tiles / pairs;
-    int dp = tiles, sk = 0;
-    if (tiles % pairs != 0) {
-        // the last full wave and the partial one run stream-K, provided
-        // every pair gets at least one K block
+    bool sk = tc2_est(a.M, a.N, num_kb, a.bn, pairs, true) < tc2_est(a.M, a.N, num_kb, a.bn, pairs, false);
+    if (const char *f = getenv("TMG_TC_PAIR_SCHED"))        // testing aid: "sk" | "dp"
+        sk = f[0] == 's';
+    int dp = tiles, skt = 0;
+    if (sk && tc2_sk_possible(tiles, num_kb, pairs)) {
+        // the last full wave and the partial one run stream-K
+        const int full_waves = tiles / pairs;
         dp = (full_waves > 0 ? full_waves - 1 : 0) * pairs;
-        sk = tiles - dp;
-        if (static_cast<int64_t>(sk) * num_kb < pairs) {
-            dp = tiles;
-            sk = 0;
-        }
+        skt = tiles - dp;
     }
     a.dp_tiles = dp;
-    a.sk_tiles = sk;
-    a.pairs = sk > 0 ? pairs : (tiles < pairs ? tiles : pairs);
+    a.sk_tiles = skt;
+    a.pairs = skt > 0 ? pairs : (tiles < pairs ? tiles : pairs);
 }
 
 size_t tc2_partials_bytes(const TcArgs &a)
@@ -39,25 +89,15 @@ size_t tc2_counters_bytes(const TcArgs &a)
     return static_cast<size_t>(a.sk_tiles) * 2 * epi_warps(true) * sizeof(uint32_t);
 }
 
-int tc2_pick_bn(int64_t M, int64_t N, int num_sms)
+int tc2_pick_bn(int64_t M, int64_t N, int64_t K, int num_sms)
 {
-    (void)M;
-    (void)num_sms;
-    // A pair MMA costs about the same at any width, so pick the width with
-    // the least total cost over the column tiles: roughly (2000 + width) per
-    // tile column (measured: 256-wide tiles do 14% more work than 224-wide
-    // ones in the same time).
     static const int cands[] = {256, 224, 192, 128};
-    int best = 256;
-    int64_t best_cost = -1;
-    for (int bn : cands) {
-        const int64_t cost = ((N + bn - 1) / bn) * (2000 + bn);
-        if (best_cost < 0 || cost < best_cost) {
-            best_cost = cost;
-            best = bn;
-        }
-    }
-    return best;
+    return tc2_best_bn(M, N, K, 64, num_sms, cands, 4);
+}
+
+int tc2_pick_bn_of(int64_t M, int64_t N, int64_t K, int kb_elems, int num_sms, const int *cands, int nc)
+{
+    return tc2_best_bn(M, N, K, kb_elems, num_sms, cands, nc);
 }
 
 cudaError_t launch_tc2_bf16(const TcArgs &a, int num_sms, const ErrCtx &err, cudaStream_t s)
@@ -66,6 +106,8 @@ cudaError_t launch_tc2_bf16(const TcArgs &a, int num_sms, const ErrCtx &err, cud
     const Tc2Epi none{nullptr, nullptr, nullptr, kEpiNone, 0};
     if (a.maj != 0) {
         // MN-major operands read in place (bn 256 or 128)
+        if (a.bn != 256 && a.bn != 128)
+            return cudaErrorInvalidValue;
         const bool w = a.bn == 256;
         switch (a.maj) {
         case 1:
@@ -83,8 +125,10 @@ cudaError_t launch_tc2_bf16(const TcArgs &a, int num_sms, const ErrCtx &err, cud
         return launch_pair<224, kInBf16, false>(a, none, err, s);
     case 192:
         return launch_pair<192, kInBf16, false>(a, none, err, s);
-    default:
+    case 128:
         return launch_pair<128, kInBf16, false>(a, none, err, s);
+    default:
+        return cudaErrorInvalidValue;     // a width no kernel is built for
     }
 }
 

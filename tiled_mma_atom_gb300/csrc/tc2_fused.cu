@@ -6,19 +6,28 @@
 
 namespace tmg {
 
-int tc2_fused_pick_bn(int64_t N)
+const int kTc2FusedWidths[4] = {256, 224, 192, 128};
+
+template <int IN>
+static cudaError_t launch_fused_in(const TcArgs &a, const Tc2Epi &e, const ErrCtx &err, cudaStream_t s)
 {
-    // same cost model as tc2_pick_bn, over the two widths built here
-    const int64_t c256 = ((N + 255) / 256) * (2000 + 256);
-    const int64_t c128 = ((N + 127) / 128) * (2000 + 128);
-    return c128 < c256 ? 128 : 256;
+    switch (a.bn) {
+    case 128:
+        return launch_pair<128, IN, true>(a, e, err, s);
+    case 192:
+        return launch_pair<192, IN, true>(a, e, err, s);
+    case 224:
+        return launch_pair<224, IN, true>(a, e, err, s);
+    case 256:
+        return launch_pair<256, IN, true>(a, e, err, s);
+    default:
+        return cudaErrorInvalidValue;     // a width no kernel is built for
+    }
 }
 
 cudaError_t launch_tc2_fused(const TcArgs &a, const Tc2Epi &e, bool in_e4m3, const ErrCtx &err, cudaStream_t s)
 {
-    if (in_e4m3)
-        return a.bn == 128 ? launch_pair<128, kInE4m3, true>(a, e, err, s) : launch_pair<256, kInE4m3, true>(a, e, err, s);
-    return a.bn == 128 ? launch_pair<128, kInBf16, true>(a, e, err, s) : launch_pair<256, kInBf16, true>(a, e, err, s);
+    return in_e4m3 ? launch_fused_in<kInE4m3>(a, e, err, s) : launch_fused_in<kInBf16>(a, e, err, s);
 }
 
 namespace {

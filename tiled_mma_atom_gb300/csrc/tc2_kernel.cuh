@@ -484,10 +484,13 @@ __global__ void __launch_bounds__(tc2_threads(EPI), 1)
     } else {
         // ---------------------------------------------------- epilogue
         constexpr int NEPI = epi_warps(EPI);
-        constexpr int CHUNKS = BN / 32 / (NEPI / 4);     // 32-column chunks per warp
+        // 32-column chunks per warp: the warps sharing a lane quarter split
+        // the tile's BN / 32 chunks, the first ones taking one more when
+        // the count is odd (224-wide tiles: 4 + 3)
+        constexpr int CHUNKS = (BN / 32 + NEPI / 4 - 1) / (NEPI / 4);
         const int e = warp - 2;                          // epilogue warp index
         const int q = warp & 3;                          // its TMEM lane quarter
-        const int c_begin = (e / 4) * CHUNKS, c_end = c_begin + CHUNKS;
+        const int c_begin = (e / 4) * CHUNKS, c_end = min(BN / 32, c_begin + CHUNKS);
         const int64_t U = static_cast<int64_t>(sk_tiles) * num_kb;
         int local = 0;
         SegWalk walk(cluster, nclusters, dp_tiles, sk_tiles, num_kb);
