@@ -139,7 +139,10 @@ def test_mn_major_read_in_place(tmg, monkeypatch, maj, M, N, K):
     read in place by the pair kernel (64 x 64 boxes, MN-major MMA
     descriptors) instead of being gathered; ragged M, N and K.  The result
     meets the oracle bound and equals the gathered path's bit for bit (the
-    same MMAs in the same order)."""
+    same MMAs in the same order: the tile width and schedule are pinned, as
+    the two paths choose among different widths when B is MN-major)."""
+    monkeypatch.setenv("TMG_TC_PAIR_BN", "256")
+    monkeypatch.setenv("TMG_TC_PAIR_SCHED", "sk")
     A, B = inputs.normal_bf16(M, K, 411), inputs.normal_bf16(N, K, 412)
     la = ((M, K), (1, M)) if maj & 1 else ((M, K), (K, 1))
     lb = ((N, K), (1, N)) if maj & 2 else ((N, K), (K, 1))
@@ -157,6 +160,29 @@ def test_mn_major_read_in_place(tmg, monkeypatch, maj, M, N, K):
     D2 = tmg.gemm(Ad, Bd, M=M, N=N, K=K, layoutA=la, layoutB=lb)
     tmg.check()
     assert tmg.launch_count() - n0 >= 2                  # gathered, then the GEMM
+    assert torch.equal(D, D2)
+
+
+@pytest.mark.parametrize("width", [128, 192, 224, 256])
+def test_mn_major_a_in_place_every_width(tmg, monkeypatch, width):
+    """A column-major read in place at every pair-tile width (its boxes do
+    not depend on the width), data-parallel with a partial last wave:
+    equal to the gathered path at the same width and schedule."""
+    monkeypatch.setenv("TMG_TC_PAIR_BN", str(width))
+    monkeypatch.setenv("TMG_TC_PAIR_SCHED", "dp")
+    M, N, K = 2048, 2600, 200
+    A, B = inputs.normal_bf16(M, K, 431), inputs.normal_bf16(N, K, 432)
+    la = ((M, K), (1, M))
+    Ad, Bd = A.t().contiguous().to(DEV), B.to(DEV)
+    n0 = tmg.launch_count()
+    D = tmg.gemm(Ad, Bd, M=M, N=N, K=K, layoutA=la)
+    tmg.check()
+    assert tmg.launch_count() - n0 == 1
+    parity.check_bf16(D, _ref(A.t().contiguous(), la, B, ((N, K), (K, 1)), M, N, K), K, parity.absmax(A),
+                      parity.absmax(B))
+    monkeypatch.setenv("TMG_NO_INPLACE_MN", "1")
+    D2 = tmg.gemm(Ad, Bd, M=M, N=N, K=K, layoutA=la)
+    tmg.check()
     assert torch.equal(D, D2)
 
 

@@ -597,9 +597,15 @@ bool run_tc2_inplace(const DeviceState &ds, const void *A, const void *B, void *
     TcArgs a;
     std::memset(&a, 0, sizeof a);
     a.maj = maj;
-    // the MN-major kernels are built at widths 256 and 128 only
-    static const int kMnWidths[2] = {256, 128};
-    a.bn = (maj & 2) ? (N >= 256 ? 256 : 128) : tc2_pick_bn_of(M, N, K, 64, ds.num_sms, kMnWidths, 2);
+    // an MN-major B is read in 64-column boxes: widths 256 and 128 only
+    static const int kBMnWidths[2] = {256, 128};
+    if (maj & 2) {
+        a.bn = tc2_pick_bn_of(M, N, K, 64, ds.num_sms, kBMnWidths, 2);
+        const int f = pair_bn_override(a.bn);
+        a.bn = (f == 256 || f == 128) ? f : a.bn;
+    } else {
+        a.bn = pair_bn_override(tc2_pick_bn(M, N, K, ds.num_sms));
+    }
     if (((M + 255) / 256) * ((N + a.bn - 1) / a.bn) < ds.num_sms / 2)
         return false;                                     // too few pair tiles
     if ((*st = (maj & 1) ? encode_2d(&a.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, M, K, lds[0], 64, 64)

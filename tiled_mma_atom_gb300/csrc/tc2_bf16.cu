@@ -104,14 +104,27 @@ cudaError_t launch_tc2_bf16(const TcArgs &a, int num_sms, const ErrCtx &err, cud
 {
     (void)num_sms;
     const Tc2Epi none{nullptr, nullptr, nullptr, kEpiNone, 0};
+    if (a.maj == 1) {
+        // MN-major A read in place (any width: its boxes do not depend on it)
+        switch (a.bn) {
+        case 256:
+            return launch_pair<256, kInBf16, false, 1>(a, none, err, s);
+        case 224:
+            return launch_pair<224, kInBf16, false, 1>(a, none, err, s);
+        case 192:
+            return launch_pair<192, kInBf16, false, 1>(a, none, err, s);
+        case 128:
+            return launch_pair<128, kInBf16, false, 1>(a, none, err, s);
+        default:
+            return cudaErrorInvalidValue;
+        }
+    }
     if (a.maj != 0) {
-        // MN-major operands read in place (bn 256 or 128)
+        // MN-major B read in place: 64-column boxes, so bn 256 or 128
         if (a.bn != 256 && a.bn != 128)
             return cudaErrorInvalidValue;
         const bool w = a.bn == 256;
         switch (a.maj) {
-        case 1:
-            return w ? launch_pair<256, kInBf16, false, 1>(a, none, err, s) : launch_pair<128, kInBf16, false, 1>(a, none, err, s);
         case 2:
             return w ? launch_pair<256, kInBf16, false, 2>(a, none, err, s) : launch_pair<128, kInBf16, false, 2>(a, none, err, s);
         default:

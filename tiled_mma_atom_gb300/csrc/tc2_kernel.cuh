@@ -324,7 +324,8 @@ __global__ void __launch_bounds__(tc2_threads(EPI), 1)
                     ErrCtx err)
 {
     using C = PairCfg<BN, EPI>;
-    static_assert(MAJ == 0 || (IN == kInBf16 && !EPI && (BN / 2) % kMnBox == 0), "MN-major operands: plain bf16");
+    static_assert(MAJ == 0 || (IN == kInBf16 && !EPI && ((MAJ & 2) == 0 || (BN / 2) % kMnBox == 0)),
+                  "MN-major operands: plain bf16; an MN-major B needs whole 64-column boxes per CTA");
     const int64_t d_limit = static_cast<int64_t>(M - 1) * ldd + N;     // elements of D
     constexpr int KB_ELEMS = kb_elems(IN);
     constexpr int STAGES = C::STAGES;
