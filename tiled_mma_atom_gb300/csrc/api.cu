@@ -454,26 +454,22 @@ tmg_status run_tc(const DeviceState &ds, const TcPlan &p, void *D, int64_t K, in
 {
     TcArgs a;
     std::memset(&a, 0, sizeof a);
-    // Pairs pay off once their tiles fill every SM pair at least once;
-    // smaller problems keep more SMs busy with one-CTA 128-row tiles.
+    // CTA pairs or one-CTA tiles, whichever the cost model expects to be
+    // faster: pairs halve the B traffic per SM, one-CTA tiles come in twice
+    // as many per wave.
     bool pair = mode == 2;
+    double est1 = 0.0, est2 = 0.0;
+    const int bn1 = tc_pick_bn(p.M, p.N, K, ds.num_sms, &est1);
     if (mode == 0 && p.M >= 256) {
-        const int bn2 = tc2_pick_bn(p.M, p.N, K, ds.num_sms);
-        pair = ((p.M + 255) / 256) * ((p.N + bn2 - 1) / bn2) >= ds.num_sms / 2;
+        tc2_pick_bn(p.M, p.N, K, ds.num_sms, &est2);
+        pair = est2 < est1;
     }
     int box_b;
     if (pair) {
         a.bn = pair_bn_override(tc2_pick_bn(p.M, p.N, K, ds.num_sms));
         box_b = a.bn / 2;
     } else {
-        // widest tile that still gives every SM work; 64 for small problems
-        const int64_t rows = (p.M + 127) / 128;
-        if (rows * ((p.N + 255) / 256) >= ds.num_sms)
-            a.bn = 256;
-        else if (rows * ((p.N + 127) / 128) >= ds.num_sms / 2)
-            a.bn = 128;
-        else
-            a.bn = 64;
+        a.bn = bn1;
         box_b = a.bn;
     }
     tmg_status st;

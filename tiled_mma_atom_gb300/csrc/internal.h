@@ -63,6 +63,9 @@ struct TcArgs {
                        // (tmB over Bᵀ, box {64, 64}; bn 256 or 128)
 };
 cudaError_t launch_tc_bf16(const TcArgs &a, int num_sms, const ErrCtx &err, cudaStream_t s);
+// One-CTA tile width (64, 128 or 256) for an M x N x K product and its
+// estimated time in ns, on the same footing as tc2_pick_bn's estimate.
+int tc_pick_bn(int64_t M, int64_t N, int64_t K, int num_sms, double *est_ns);
 // CTA-pair variant (cta_group::2, 256 x bn tiles; bn in {256, 224, 192, 128},
 // tmB box {64, bn/2}).  Call tc2_plan first, then provide the scratch.
 cudaError_t launch_tc2_bf16(const TcArgs &a, int num_sms, const ErrCtx &err, cudaStream_t s);
@@ -70,7 +73,7 @@ cudaError_t launch_tc2_bf16(const TcArgs &a, int num_sms, const ErrCtx &err, cud
 // widths 256 / 224 / 192 / 128; tc2_pick_bn_of chooses among `cands` for
 // K blocks of kb_elems elements.  The same cost model decides, in
 // tc2_plan, between a data-parallel schedule and a stream-K tail.
-int tc2_pick_bn(int64_t M, int64_t N, int64_t K, int num_sms);
+int tc2_pick_bn(int64_t M, int64_t N, int64_t K, int num_sms, double *est_ns = nullptr);
 int tc2_pick_bn_of(int64_t M, int64_t N, int64_t K, int kb_elems, int num_sms, const int *cands, int nc);
 
 // Fused epilogue of the pair kernel: D = bf16(act(acc * scale_a[m] *

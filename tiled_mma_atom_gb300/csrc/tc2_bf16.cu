@@ -40,7 +40,8 @@ static double tc2_est(int64_t M, int64_t N, int num_kb, int bn, int pairs, bool 
     return static_cast<double>((tiles + pairs - 1) / pairs) * c;
 }
 
-static int tc2_best_bn(int64_t M, int64_t N, int64_t K, int kb_elems, int num_sms, const int *cands, int nc)
+static int tc2_best_bn(int64_t M, int64_t N, int64_t K, int kb_elems, int num_sms, const int *cands, int nc,
+                       double *est = nullptr)
 {
     const int pairs = num_sms / 2;
     const int num_kb = static_cast<int>((K + kb_elems - 1) / kb_elems);
@@ -54,6 +55,8 @@ static int tc2_best_bn(int64_t M, int64_t N, int64_t K, int kb_elems, int num_sm
             best = cands[i];
         }
     }
+    if (est)
+        *est = best_t;
     return best;
 }
 
@@ -89,10 +92,10 @@ size_t tc2_counters_bytes(const TcArgs &a)
     return static_cast<size_t>(a.sk_tiles) * 2 * epi_warps(true) * sizeof(uint32_t);
 }
 
-int tc2_pick_bn(int64_t M, int64_t N, int64_t K, int num_sms)
+int tc2_pick_bn(int64_t M, int64_t N, int64_t K, int num_sms, double *est_ns)
 {
     static const int cands[] = {256, 224, 192, 128};
-    return tc2_best_bn(M, N, K, 64, num_sms, cands, 4);
+    return tc2_best_bn(M, N, K, 64, num_sms, cands, 4, est_ns);
 }
 
 int tc2_pick_bn_of(int64_t M, int64_t N, int64_t K, int kb_elems, int num_sms, const int *cands, int nc)

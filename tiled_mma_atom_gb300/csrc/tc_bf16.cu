@@ -269,6 +269,30 @@ cudaError_t launch_cfg(const TcArgs &a, int num_sms, const ErrCtx &err, cudaStre
 
 }  // namespace
 
+int tc_pick_bn(int64_t M, int64_t N, int64_t K, int num_sms, double *est_ns)
+{
+    // Per K block of one 128 x bn tile, measured on GB300 (bf16, L2 flushed,
+    // M, N 1024-3072, K 1024-4096): 173 / 223 / 367 ns at widths 64 / 128 /
+    // 256; whole waves of num_sms tiles.
+    static const int widths[3] = {64, 128, 256};
+    static const double cost[3] = {173.0, 223.0, 367.0};
+    const int64_t num_kb = (K + kBK - 1) / kBK;
+    const int64_t rows = (M + kBM - 1) / kBM;
+    int best = 128;
+    double best_t = -1.0;
+    for (int i = 0; i < 3; ++i) {
+        const int64_t tiles = rows * ((N + widths[i] - 1) / widths[i]);
+        const double t = static_cast<double>((tiles + num_sms - 1) / num_sms) * num_kb * cost[i];
+        if (best_t < 0.0 || t < best_t) {
+            best_t = t;
+            best = widths[i];
+        }
+    }
+    if (est_ns)
+        *est_ns = best_t;
+    return best;
+}
+
 cudaError_t launch_tc_bf16(const TcArgs &a, int num_sms, const ErrCtx &err, cudaStream_t s)
 {
     if (a.bn == 256)
