@@ -126,3 +126,28 @@ def test_log_names_the_chosen_kernel():
     quiet = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300, cwd=ROOT,
                            env=dict(os.environ, TMG_LOG="0"))
     assert quiet.returncode == 0 and "tmg: " not in quiet.stderr
+
+
+def test_log_shows_the_cost_model_choices():
+    """The cost model's choices for three shapes, as TMG_LOG reports them:
+    bf16 4096^3 on 224-wide pair tiles in four whole data-parallel waves
+    (16 x 19 = 304 tiles on 76 pairs), 1024^3 on one-CTA 128x64 tiles, and
+    2048^3 at K = 4096 on 256-wide pair tiles in one partial wave (64 of the
+    76 pairs) rather than one-CTA tiles in two waves."""
+    code = ("import torch, tiled_mma_atom_gb300 as t\n"
+            "for (M, N, K) in ((4096, 4096, 4096), (1024, 1024, 1024), (2048, 2048, 4096)):\n"
+            "    A = torch.randn(M, K, dtype=torch.bfloat16, device='cuda')\n"
+            "    B = torch.randn(N, K, dtype=torch.bfloat16, device='cuda')\n"
+            "    t.gemm(A, B)\n"
+            "t.check()\n")
+    env = dict(os.environ, TMG_LOG="1")
+    env.pop("TMG_TC_PAIR_BN", None)
+    env.pop("TMG_TC_PAIR_SCHED", None)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300, cwd=ROOT, env=env)
+    assert r.returncode == 0, r.stderr
+    lines = [ln for ln in r.stderr.splitlines() if ln.startswith("tmg: ")]
+    assert len(lines) == 3, r.stderr
+    assert "tc2_gemm_kernel" in lines[0] and "256x224 tiles" in lines[0] and "304 data-parallel + 0 stream-K" in lines[0]
+    assert "tc_bf16_kernel" in lines[1] and "128x64 tiles" in lines[1]
+    assert "tc2_gemm_kernel" in lines[2] and "256x256 tiles" in lines[2] and "+ 0 stream-K" in lines[2]
+
