@@ -61,7 +61,7 @@ def test_fused_vs_oracle(tmg, kind, epi):
                               float(sa.max()), float(sb.max()))
 
 
-@pytest.mark.parametrize("width", [224, 256])
+@pytest.mark.parametrize("width", [128, 192, 224, 256])
 @pytest.mark.parametrize("kind", sorted(KINDS))
 def test_fused_integer_exact_through_stream_k(tmg, kind, width, monkeypatch):
     """Integer inputs, power-of-two scales, integer bias, relu: every step is

@@ -225,6 +225,21 @@ def test_tc_pair_stream_k_tail_exact(tmg, width, sched, monkeypatch):
     parity.check_exact_bf16(parity.bf16_bits(D2), parity.ref_full(A, B, oracle.BF16))
 
 
+@pytest.mark.parametrize("width", [128, 224, 256])
+def test_tc_pair_fewer_tiles_than_pairs_exact(tmg, width, monkeypatch):
+    """Data-parallel with fewer tiles than CTA pairs (1024 x 2048: 32 tiles
+    at width 256, 36 at 224, 64 at 128, on 76 pairs): only that many pairs
+    are launched.  Ragged N and K; integer inputs, bit-exact."""
+    monkeypatch.setenv("TMG_TC_PAIR_BN", str(width))
+    monkeypatch.setenv("TMG_TC_PAIR_SCHED", "dp")
+    M, N, K = 1024, 2000, 520
+    A = inputs.integer_valued(M, K, 220 + width)
+    B = inputs.integer_valued(N, K, 221 + width)
+    D = tmg.gemm(*_gpu(A, B), path="tc_pair")
+    tmg.check()
+    parity.check_exact_bf16(parity.bf16_bits(D), parity.ref_full(A, B, oracle.BF16))
+
+
 def test_tc_pair_stream_k_random_vs_oracle(tmg, monkeypatch):
     """Random inputs through the stream-K tail (4096 x 4096 has 256 tiles of
     256 columns over 76 pairs); sampled outputs in the split tiles' region."""
