@@ -159,30 +159,6 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
-// 2-D tiled bulk tensor copy global -> shared, completion counted in bytes on
-// `bar`.  c0 is the innermost (contiguous) coordinate in elements.
-__device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *map,
-                                            uint64_t *bar, int32_t c0, int32_t c1)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(smem_dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
-        : "memory");
-}
-
-// Contiguous bulk copy global -> shared (`bytes` a multiple of 16, both
-// addresses 16-byte aligned), completion counted in bytes on `bar`.
-__device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint32_t bytes,
-                                          uint64_t *bar)
-{
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-            "r"(smem_u32(smem_dst)),
-        "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
-        : "memory");
-}
-
 // Same, with an L2 eviction-priority hint (createpolicy result).
 __device__ __forceinline__ void tma_load_2d_hint(void *smem_dst, const CUtensorMap *map,
                                                  uint64_t *bar, int32_t c0, int32_t c1,
@@ -400,18 +376,6 @@ __device__ __forceinline__ bool mbar_wait_cluster_warp(uint64_t *bar, uint32_t p
     return __all_sync(0xffffffffu, mbar_wait_cluster(bar, parity, ctx, abort, site));
 }
 
-// TMA tile load into this CTA's shared memory whose completion is counted on
-// an mbarrier that may live in the peer CTA (shared::cluster address).
-__device__ __forceinline__ void tma_load_2d_pair(void *smem_dst, const CUtensorMap *map,
-                                                 uint32_t bar_cluster_addr, int32_t c0, int32_t c1)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(smem_dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster_addr), "r"(c0), "r"(c1)
-        : "memory");
-}
-
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t *slot, uint32_t ncols)
 {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -523,6 +487,8 @@ __device__ __forceinline__ void mbar_arrive_expect_tx_w(uint64_t *bar, uint32_t 
                  : "memory");
 }
 
+// 2-D tiled bulk tensor copy global -> shared, completion counted in bytes on
+// `bar`; c0 is the innermost (contiguous) coordinate in elements.
 __device__ __forceinline__ void tma_load_2d_w(void *smem_dst, const CUtensorMap *map, uint64_t *bar, int32_t c0,
                                               int32_t c1)
 {
@@ -534,6 +500,8 @@ __device__ __forceinline__ void tma_load_2d_w(void *smem_dst, const CUtensorMap 
         : "memory");
 }
 
+// The same into this CTA's shared memory, completion counted on an mbarrier
+// that may live in the peer CTA of a pair (shared::cluster address).
 __device__ __forceinline__ void tma_load_2d_pair_w(void *smem_dst, const CUtensorMap *map, uint32_t bar_cluster_addr,
                                                    int32_t c0, int32_t c1)
 {
@@ -556,6 +524,8 @@ __device__ __forceinline__ void tma_load_2d_hint_w(void *smem_dst, const CUtenso
         : "memory");
 }
 
+// Contiguous bulk copy global -> shared (`bytes` a multiple of 16, both
+// addresses 16-byte aligned), completion counted in bytes on `bar`.
 __device__ __forceinline__ void bulk_load_w(void *smem_dst, const void *gsrc, uint32_t bytes, uint64_t *bar)
 {
     asm volatile(
