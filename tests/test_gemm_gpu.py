@@ -279,6 +279,25 @@ def test_tc_single_and_pair_agree(tmg):
     assert torch.equal(D1, D2)
 
 
+def test_auto_dispatch_random_shapes(tmg):
+    """Shapes drawn at random (seeded) through the auto dispatch, which picks
+    one-CTA or pair kernels, tile widths and schedules from its cost model:
+    every choice it makes on them must give the oracle's values (sampled
+    entries, including the corners and the last row and column)."""
+    rng = np.random.default_rng(2024)
+    for i in range(16):
+        M = int(rng.integers(65, 3200))
+        N = int(rng.integers(16, 5200))
+        K = 8 * int(rng.integers(1, 320))
+        A = inputs.normal_bf16(M, K, 600 + 2 * i)
+        B = inputs.normal_bf16(N, K, 601 + 2 * i)
+        D = tmg.gemm(*_gpu(A, B))
+        tmg.check()
+        ms, ns = parity.sample_coords(M, N, 600, seed=i)
+        ref = parity.ref_entries(A, B, oracle.BF16, ms, ns)
+        parity.check_bf16_values(parity.to_f64(D)[ms, ns], ref, K, parity.absmax(A), parity.absmax(B))
+
+
 def test_tc_deterministic(tmg):
     A = inputs.normal_bf16(512, 768, 81)
     B = inputs.normal_bf16(640, 768, 82)
