@@ -133,9 +133,11 @@ def test_log_shows_the_cost_model_choices():
     bf16 4096^3 on 224-wide pair tiles in four whole data-parallel waves
     (16 x 19 = 304 tiles on 76 pairs), 1024^3 on one-CTA 128x64 tiles, and
     2048^3 at K = 4096 on 256-wide pair tiles in one partial wave (64 of the
-    76 pairs) rather than one-CTA tiles in two waves."""
+    76 pairs) rather than one-CTA tiles in two waves.  The pair tiles run in
+    groups of 16 M-tiles while sixteen 256-row A panels take at most 32 MB
+    (K = 4096 bf16: 2 MB each) and in groups of 8 beyond (K = 8192)."""
     code = ("import torch, tiled_mma_atom_gb300 as t\n"
-            "for (M, N, K) in ((4096, 4096, 4096), (1024, 1024, 1024), (2048, 2048, 4096)):\n"
+            "for (M, N, K) in ((4096, 4096, 4096), (1024, 1024, 1024), (2048, 2048, 4096), (2048, 2048, 8192)):\n"
             "    A = torch.randn(M, K, dtype=torch.bfloat16, device='cuda')\n"
             "    B = torch.randn(N, K, dtype=torch.bfloat16, device='cuda')\n"
             "    t.gemm(A, B)\n"
@@ -146,8 +148,11 @@ def test_log_shows_the_cost_model_choices():
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300, cwd=ROOT, env=env)
     assert r.returncode == 0, r.stderr
     lines = [ln for ln in r.stderr.splitlines() if ln.startswith("tmg: ")]
-    assert len(lines) == 3, r.stderr
+    assert len(lines) == 4, r.stderr
     assert "tc2_gemm_kernel" in lines[0] and "256x224 tiles" in lines[0] and "304 data-parallel + 0 stream-K" in lines[0]
+    assert "groups of 16 M-tiles" in lines[0]
     assert "tc_bf16_kernel" in lines[1] and "128x64 tiles" in lines[1]
     assert "tc2_gemm_kernel" in lines[2] and "256x256 tiles" in lines[2] and "+ 0 stream-K" in lines[2]
+    assert "groups of 16 M-tiles" in lines[2]
+    assert "tc2_gemm_kernel" in lines[3] and "groups of 8 M-tiles" in lines[3]
 

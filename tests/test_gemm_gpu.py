@@ -266,6 +266,18 @@ def test_tc_pair_ragged_integer_exact(tmg, M, N, K):
     parity.check_exact_bf16(parity.bf16_bits(D), parity.ref_full(A, B, oracle.BF16))
 
 
+@pytest.mark.parametrize("M,N,K", [(4648, 600, 256), (2856, 300, 4160)])
+def test_tc_pair_ragged_tile_groups_exact(tmg, M, N, K):
+    """The pair kernel's tile order runs groups of 16 M-tiles at K = 256
+    (19 M-tiles: one group of 16 and a ragged group of 3) and groups of 8
+    at K = 4160 (12 M-tiles: 8 and a ragged 4).  Integer inputs: bit-exact."""
+    A = inputs.integer_valued(M, K, 160 + M)
+    B = inputs.integer_valued(N, K, 161 + N)
+    D = tmg.gemm(*_gpu(A, B), path="tc_pair")
+    tmg.check()
+    parity.check_exact_bf16(parity.bf16_bits(D), parity.ref_full(A, B, oracle.BF16))
+
+
 def test_tc_single_and_pair_agree(tmg):
     """One-CTA and CTA-pair kernels on the same inputs: integer inputs make
     both exact, so they must agree bit for bit."""

@@ -491,7 +491,7 @@ tmg_status run_tc(const DeviceState &ds, const TcPlan &p, void *D, int64_t K, in
     }
     if (pair)
         log_choice("bf16 %dx%dx%d -> tc2_gemm_kernel (CTA pairs): 256x%d tiles, %d pairs, %d data-parallel + %d "
-                   "stream-K tiles", a.M, a.N, a.K, a.bn, a.pairs, a.dp_tiles, a.sk_tiles);
+                   "stream-K tiles, groups of %d M-tiles", a.M, a.N, a.K, a.bn, a.pairs, a.dp_tiles, a.sk_tiles, a.group_m);
     else
         log_choice("bf16 %dx%dx%d -> tc_bf16_kernel (one CTA): 128x%d tiles", a.M, a.N, a.K, a.bn);
     cudaError_t e = pair ? launch_tc2_bf16(a, ds.num_sms, err_ctx(ds), s) : launch_tc_bf16(a, ds.num_sms, err_ctx(ds), s);
@@ -622,9 +622,9 @@ bool run_tc2_inplace(const DeviceState &ds, const void *A, const void *B, void *
     if ((*st = tc2_scratch(dev, s, a)) != TMG_OK)
         return true;
     log_choice("bf16 %dx%dx%d -> tc2_gemm_kernel (CTA pairs), MN-major operands read in place (A %s, B %s): "
-               "256x%d tiles, %d pairs, %d data-parallel + %d stream-K tiles", a.M, a.N, a.K,
+               "256x%d tiles, %d pairs, %d data-parallel + %d stream-K tiles, groups of %d M-tiles", a.M, a.N, a.K,
                (a.maj & 1) ? "MN-major" : "K-major", (a.maj & 2) ? "MN-major" : "K-major", a.bn, a.pairs, a.dp_tiles,
-               a.sk_tiles);
+               a.sk_tiles, a.group_m);
     const cudaError_t e = launch_tc2_bf16(a, ds.num_sms, err_ctx(ds), s);
     *st = e == cudaSuccess ? TMG_OK : cuda_fail(e, "tc2_bf16 (MN-major operands) launch");
     return true;
@@ -1034,8 +1034,9 @@ tmg_status tmg_gemm_fused(const void *A, const void *B, void *D, int64_t M, int6
     if ((st = tc2_scratch(dev, s, a)) != TMG_OK)
         return st;
     log_choice("%s %dx%dx%d fused (epilogue %d, scale_a %s, scale_b %s) -> tc2_gemm_kernel (CTA pairs): 256x%d tiles, "
-               "%d pairs, %d data-parallel + %d stream-K tiles", e4m3 ? "e4m3" : "bf16", a.M, a.N, a.K, epi.epi,
-               epi.scale_a ? "yes" : "no", epi.scale_b ? "yes" : "no", a.bn, a.pairs, a.dp_tiles, a.sk_tiles);
+               "%d pairs, %d data-parallel + %d stream-K tiles, groups of %d M-tiles", e4m3 ? "e4m3" : "bf16", a.M, a.N,
+               a.K, epi.epi, epi.scale_a ? "yes" : "no", epi.scale_b ? "yes" : "no", a.bn, a.pairs, a.dp_tiles,
+               a.sk_tiles, a.group_m);
     cudaError_t e = launch_tc2_fused(a, epi, e4m3, err_ctx(*ds), s);
     return e == cudaSuccess ? TMG_OK : cuda_fail(e, "fused pair launch");
 }
@@ -1145,8 +1146,8 @@ tmg_status gemm_w4a8_impl(const void *A, const void *B, bool shuffled, void *D, 
             return st;
         const Tc2Epi epi{nullptr, nullptr, nullptr, kEpiNone, k0 == 0 ? 1 : 2};
         log_choice("w4a8 %dx%dx%d, K segment at %lld -> tc2_gemm_kernel on the unpacked bf16 copies: 256x%d tiles, "
-                   "%d pairs, int32 %s", a.M, a.N, a.K, static_cast<long long>(k0), a.bn, a.pairs,
-                   k0 == 0 ? "store" : "add");
+                   "%d pairs, groups of %d M-tiles, int32 %s", a.M, a.N, a.K, static_cast<long long>(k0), a.bn, a.pairs,
+                   a.group_m, k0 == 0 ? "store" : "add");
         if ((e = launch_tc2_fused(a, epi, false, err_ctx(*ds), s)) != cudaSuccess)
             return cuda_fail(e, "W4A8 GEMM launch");
     }

@@ -57,6 +57,7 @@ struct TcArgs {
     int pairs;         // clusters launched
     int dp_tiles;      // tiles run data-parallel
     int sk_tiles;      // tiles after them, run stream-K
+    int group_m;       // M-tiles per group of the tile order (8 or 16)
     float *partials;   // tc2_partials_bytes()
     uint32_t *counters;  // tc2_counters_bytes(), zero on entry
     int maj;           // pair kernel, bf16: bit 0 A MN-major (tmA over Aᵀ, box {64, 64}), bit 1 B MN-major

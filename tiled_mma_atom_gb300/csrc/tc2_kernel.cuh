@@ -64,7 +64,6 @@ constexpr int kKBlockBytes = 128;  // bytes of each operand row per K block (one
 // the whole kernel.
 __host__ __device__ constexpr int epi_warps(bool epi) { return epi ? 8 : 4; }
 __host__ __device__ constexpr int tc2_threads(bool epi) { return 64 + 32 * epi_warps(epi); }
-constexpr int kGroupM = 8;
 
 // Elements per K block for an input type.
 __host__ __device__ constexpr int kb_elems(int in) { return in == kInE4m3 ? 128 : 64; }
@@ -119,11 +118,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16_major(int M, int N, int maj)
     return idesc_bf16_f32(M, N) | ((maj & 1) ? (1u << 15) : 0u) | ((maj & 2) ? (1u << 16) : 0u);
 }
 
-__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int &tm, int &tn)
+// Tiles run in groups of group_m M-tiles, M-tile fastest within a group
+// (the host's tc2_plan picks group_m).
+__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int group_m, int &tm, int &tn)
 {
-    const int group = kGroupM * tiles_n;
-    const int first_m = (t / group) * kGroupM;
-    const int gm = min(tiles_m - first_m, kGroupM);
+    const int group = group_m * tiles_n;
+    const int first_m = (t / group) * group_m;
+    const int gm = min(tiles_m - first_m, group_m);
     const int r = t % group;
     tm = first_m + r % gm;
     tn = r / gm;
@@ -320,7 +321,7 @@ template <int BN, int IN, bool EPI, int MAJ = 0>
 __global__ void __launch_bounds__(tc2_threads(EPI), 1)
     tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     __nv_bfloat16 *__restrict__ D, int64_t ldd, int M, int N, int K, int dp_tiles, int sk_tiles,
-                    float *__restrict__ partials, uint32_t *__restrict__ counters, int vec_ok, Tc2Epi epi,
+                    int group_m, float *__restrict__ partials, uint32_t *__restrict__ counters, int vec_ok, Tc2Epi epi,
                     ErrCtx err)
 {
     using C = PairCfg<BN, EPI>;
@@ -385,7 +386,7 @@ __global__ void __launch_bounds__(tc2_threads(EPI), 1)
         bool partial;
         while (ok && walk.next(tile, kb0, kb1, partial, slot)) {
             int tm, tn;
-            tile_coords(tile, tiles_m, tiles_n, tm, tn);
+            tile_coords(tile, tiles_m, tiles_n, group_m, tm, tn);
             for (int kb = kb0; kb < kb1; ++kb) {
                 if (!mbar_wait_cluster_warp(&empty[stage], phase ^ 1u, err, abort_flag, kSiteProducerEmpty)) {
                     ok = false;
@@ -499,7 +500,7 @@ __global__ void __launch_bounds__(tc2_threads(EPI), 1)
         bool partial;
         while (walk.next(tile, kb0, kb1, partial, slot)) {
             int tm, tn;
-            tile_coords(tile, tiles_m, tiles_n, tm, tn);
+            tile_coords(tile, tiles_m, tiles_n, group_m, tm, tn);
             const int acc = local & 1;
             const uint32_t acc_phase = (local >> 1) & 1;
             ++local;
@@ -655,6 +656,8 @@ cudaError_t launch_pair(const TcArgs &a, const Tc2Epi &epi, const ErrCtx &err, c
     static_assert(C::STAGES >= 4, "pipeline depth");
     static_assert(2 * BN <= C::TMEM_COLS, "TMEM budget");
     static_assert(C::B_BYTES % 1024 == 0, "B half must be whole 8-row swizzle atoms");
+    if (a.group_m < 1)          // tc2_plan not called
+        return cudaErrorInvalidValue;
     auto kern = tc2_gemm_kernel<BN, IN, EPI, MAJ>;
     constexpr int SMEM = C::SMEM;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), SMEM);
@@ -675,7 +678,7 @@ cudaError_t launch_pair(const TcArgs &a, const Tc2Epi &epi, const ErrCtx &err, c
     const int vec_ok = (a.ldd % 8 == 0) && ((reinterpret_cast<uintptr_t>(a.D) & 15u) == 0);
     note_launch();
     e = cudaLaunchKernelEx(&cfg, kern, a.tmA, a.tmB, static_cast<__nv_bfloat16 *>(a.D), a.ldd, a.M, a.N, a.K,
-                           a.dp_tiles, a.sk_tiles, a.partials, a.counters, vec_ok, epi, err);
+                           a.dp_tiles, a.sk_tiles, a.group_m, a.partials, a.counters, vec_ok, epi, err);
     if (e != cudaSuccess)
         return e;
     return cudaGetLastError();
