@@ -85,7 +85,7 @@ def test_reference_arm_prints_one_line_on_cpu():
 def test_config_block_is_last_and_fits_a_short_tail():
     """The five configurations' compact entries close the JSON line, so a
     reader that keeps only the last 1,500 characters still sees C1-C5 with
-    their oracle timings.  Built from realistic values through the same
+    their oracle timings and their warm (back-to-back) times.  Built from realistic values through the same
     helpers bench.py uses."""
     sys.path.insert(0, ROOT)
     import bench
@@ -96,7 +96,7 @@ def test_config_block_is_last_and_fits_a_short_tail():
         w = inputs.WORKLOADS[name]
         ms = [0.0123456789, 0.0823456789, 0.1823456789]
         rl = bench.roofline(w, sum(ms) / 3, peaks, "measured", {})
-        configs[f"C{i + 1}_{name}"] = bench.config_entry(w, ms, rl, (0.0461234, 2.98765, 935, 16))
+        configs[f"C{i + 1}_{name}"] = bench.config_entry(w, ms, rl, (0.0461234, 2.98765, 935, 16), 0.0712345678)
     line = {"metric": bench.METRIC, "value": 1613.6, "workloads": {"x": {"tflops": 1.0}}, "configs": configs}
     text = json.dumps(line)
     tail = text[-1500:]
@@ -107,4 +107,5 @@ def test_config_block_is_last_and_fits_a_short_tail():
     assert c5["bound"] == "tensor" and c5["kernel"] == "mxfp4_pair_kernel"
     assert c5["cpu"]["cores"] == 16 and c5["cpu"]["rows"] == "935/8192"
     assert configs["C4_skinny_16x28672x8192"]["unit"] == "GB/s"
+    assert c5["ms_warm"] == 0.07123 and c5["ms"] == 0.09235
     assert bench.sig(0.0823456789) == 0.08235 and bench.sig(1613.61) == 1614.0
