@@ -55,7 +55,7 @@ NOMINAL = {"bf16": 2250.0, "e4m3": 4500.0, "mxfp4": 13500.0, "w4a8": 2250.0, "hb
 L2_FLUSH_BYTES = 512 << 20
 L2_CLEAN_BYTES = 320 << 20
 L2_BYTES = 129 * 10**6
-KERNEL_OF = {"fp32_128": "ffma_gemm_kernel", "bf16_1024": "tc_bf16_kernel",
+KERNEL_OF = {"fp32_128": "ffma_dense_kernel", "bf16_1024": "tc_bf16_kernel",
              "bf16_4096": "tc2_gemm_kernel", "skinny_16x28672x8192": "skinny_tc_kernel",
              "mxfp4_8192": "mxfp4_pair_kernel", "e4m3_8192_bias_gelu": "tc2_gemm_kernel",
              "bf16_4096_bias_silu": "tc2_gemm_kernel", "bf16_4096_a_mn_major": "tc2_gemm_kernel", "bf16_4096_b_kn": "tc2_gemm_kernel",
@@ -63,7 +63,7 @@ KERNEL_OF = {"fp32_128": "ffma_gemm_kernel", "bf16_1024": "tc_bf16_kernel",
 
 
 # kernel that a forced path runs (bench.py --path)
-PATH_KERNEL = {"ffma": "ffma_gemm_kernel", "skinny_ffma": "skinny_ffma_kernel", "skinny": "skinny_tc_kernel",
+PATH_KERNEL = {"ffma": "ffma_dense_kernel", "skinny_ffma": "skinny_ffma_kernel", "skinny": "skinny_tc_kernel",
                "tc_single": "tc_bf16_kernel", "tc_pair": "tc2_gemm_kernel"}
 
 

@@ -75,6 +75,32 @@ def test_ffma_fp32_ragged_and_general_layouts(tmg):
     parity.check_fp32(D2, ref)
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("M,N,K", [(128, 128, 128), (300, 700, 264), (1000, 900, 200), (70, 33, 136)])
+def test_ffma_dense_and_general_kernels_agree(tmg, dtype, M, N, K):
+    """Row-major operands with 16-byte rows take the dense CUDA-core kernel;
+    the same values read through a padded row stride (K + 1, not a multiple
+    of the vector) take the general crd2idx kernel.  Both use the same tiles
+    and k order, so they agree bit for bit; both match the oracle.  The
+    shapes cover the three tile configurations (16x16 with 128-deep K
+    slices, 32x32, 64x64) and ragged edges."""
+    if dtype == "f32":
+        A, B = inputs.uniform_f32(M, K, 41), inputs.uniform_f32(N, K, 42)
+    else:
+        A, B = inputs.normal_bf16(M, K, 43), inputs.normal_bf16(N, K, 44)
+    Apad = torch.zeros(M, K + 1, dtype=A.dtype)
+    Apad[:, :K] = A
+    dA, dB, dApad = _gpu(A, B, Apad)
+    D1 = tmg.gemm(dA, dB, path="ffma").clone()
+    D2 = tmg.gemm(dApad, dB, M=M, N=N, K=K, layoutA=((M, K), (K + 1, 1)), path="ffma")
+    tmg.check()
+    assert torch.equal(D1, D2)
+    if dtype == "f32":
+        parity.check_fp32(D1, parity.ref_full(A, B, oracle.F32))
+    else:
+        parity.check_bf16(D1, parity.ref_full(A, B, oracle.BF16), K, parity.absmax(A), parity.absmax(B))
+
+
 def test_ffma_broadcast_operand(tmg):
     """A zero stride broadcasts one row of B to every n."""
     M, N, K = 20, 30, 40

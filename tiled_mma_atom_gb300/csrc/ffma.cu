@@ -10,7 +10,9 @@
 //    32x32) output tile in shared memory, prefetching the next slice into
 //    registers (the prologue / loop-carried prefetch of §3 "Runtime Loops with
 //    Loop-Carried Values"), and each thread accumulates a register tile,
-//    summing k in increasing order.
+//    summing k in increasing order.  Row-major operands with 16-byte rows
+//    take ffma_dense_kernel: the same tiles and k order with 16-byte vector
+//    loads at plain row-major addresses.
 //
 // 2. skinny_ffma: M <= 16 decode-shaped GEMM with K-major bf16 operands.  A
 //    warp streams four rows of B with 128-bit loads, lanes splitting K, and
@@ -159,6 +161,138 @@ __global__ void __launch_bounds__(kFfmaThreads)
     }
 }
 
+// 16 bytes of T as fp32 values (exact for fp32 and bf16).
+__device__ __forceinline__ void vec_to_f32(const uint4 &v, float (&f)[4])
+{
+    f[0] = __uint_as_float(v.x);
+    f[1] = __uint_as_float(v.y);
+    f[2] = __uint_as_float(v.z);
+    f[3] = __uint_as_float(v.w);
+}
+__device__ __forceinline__ void vec_to_f32(const uint4 &v, float (&f)[8])
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+
+// Dense operands: A (M,K), B (N,K) and D (M,N) row-major (unit stride along
+// the second coordinate), A and B rows 16-byte aligned, K a multiple of the
+// 16-byte vector.  The tiles, thread map and k order are those of
+// ffma_gemm_kernel (so the results are the same bits); the operands arrive
+// as 16-byte vectors at plain row-major addresses.  A small problem runs
+// this code once per thread and fetches it from L2 or DRAM as it goes, so
+// its length is its time: the general kernel's per-element address
+// arithmetic, straight-line, keeps the warps waiting on instruction fetch
+// for several microseconds at 128^3.
+template <typename T, int BM, int BN, int BK>
+__global__ void __launch_bounds__(kFfmaThreads)
+    ffma_dense_kernel(const T *__restrict__ A, const T *__restrict__ B, T *__restrict__ D, int64_t lda,
+                      int64_t ldb, int64_t ldd, int M, int N, int K)
+{
+    constexpr int VEC = 16 / static_cast<int>(sizeof(T));
+    constexpr int KV = BK / VEC;                          // vectors per tile row and K slice
+    constexpr int NVA = BM * KV, NVB = BN * KV;
+    constexpr int RA = (NVA + kFfmaThreads - 1) / kFfmaThreads, RB = (NVB + kFfmaThreads - 1) / kFfmaThreads;
+    constexpr int TM = BM / 16, TN = BN / 16;
+    __shared__ float As[2][BK][BM + 1];
+    __shared__ float Bs[2][BK][BN + 1];
+
+    const int tid = threadIdx.x;
+    const int tx = tid % 16, ty = tid / 16;
+    const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+
+    uint4 ra[RA], rb[RB];
+    auto load = [&](int k0) {
+#pragma unroll
+        for (int r = 0; r < RA; ++r) {
+            const int v = tid + kFfmaThreads * r, m = m0 + v / KV, k = k0 + (v % KV) * VEC;
+            ra[r] = (v < NVA && m < M && k < K) ? __ldg(reinterpret_cast<const uint4 *>(A + m * lda + k))
+                                                 : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int r = 0; r < RB; ++r) {
+            const int v = tid + kFfmaThreads * r, n = n0 + v / KV, k = k0 + (v % KV) * VEC;
+            rb[r] = (v < NVB && n < N && k < K) ? __ldg(reinterpret_cast<const uint4 *>(B + n * ldb + k))
+                                                 : make_uint4(0, 0, 0, 0);
+        }
+    };
+    auto stash = [&](int buf) {
+#pragma unroll
+        for (int r = 0; r < RA; ++r) {
+            const int v = tid + kFfmaThreads * r;
+            if (v < NVA) {
+                float f[VEC];
+                vec_to_f32(ra[r], f);
+#pragma unroll
+                for (int j = 0; j < VEC; ++j)
+                    As[buf][(v % KV) * VEC + j][v / KV] = f[j];
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < RB; ++r) {
+            const int v = tid + kFfmaThreads * r;
+            if (v < NVB) {
+                float f[VEC];
+                vec_to_f32(rb[r], f);
+#pragma unroll
+                for (int j = 0; j < VEC; ++j)
+                    Bs[buf][(v % KV) * VEC + j][v / KV] = f[j];
+            }
+        }
+    };
+
+    float acc[TM][TN];
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j)
+            acc[i][j] = 0.f;
+
+    load(0);
+    stash(0);
+    __syncthreads();
+    int buf = 0;
+    for (int k0 = 0; k0 < K; k0 += BK) {
+        const bool more = k0 + BK < K;
+        if (more)
+            load(k0 + BK);
+#pragma unroll 
+        for (int kk = 0; kk < BK; ++kk) {
+            float a[TM], b[TN];
+#pragma unroll
+            for (int i = 0; i < TM; ++i)
+                a[i] = As[buf][kk][ty + 16 * i];
+#pragma unroll
+            for (int j = 0; j < TN; ++j)
+                b[j] = Bs[buf][kk][tx + 16 * j];
+#pragma unroll
+            for (int i = 0; i < TM; ++i)
+#pragma unroll
+                for (int j = 0; j < TN; ++j)
+                    acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        }
+        if (more)
+            stash(buf ^ 1);
+        __syncthreads();
+        buf ^= 1;
+    }
+
+#pragma unroll
+    for (int i = 0; i < TM; ++i) {
+        const int m = m0 + ty + 16 * i;
+#pragma unroll
+        for (int j = 0; j < TN; ++j) {
+            const int n = n0 + tx + 16 * j;
+            if (m < M && n < N)
+                st_elt(D, m * ldd + n, acc[i][j]);
+        }
+    }
+}
+
 template <typename T>
 __global__ void zero_fill_kernel(T *D, DevLayout ld, int64_t M, int64_t N)
 {
@@ -255,6 +389,21 @@ cudaError_t launch_ffma_cfg(const FfmaArgs &a, const ErrCtx &err, cudaStream_t s
     dim3 grid(static_cast<unsigned>((a.N + BN - 1) / BN), static_cast<unsigned>((a.M + BM - 1) / BM));
     if (grid.y > 65535u)
         return cudaErrorInvalidConfiguration;
+    // dense operands take the short kernel
+    constexpr int64_t VEC = 16 / sizeof(T);
+    const DevLayout &la = a.la, &lb = a.lb, &ld = a.ld;
+    const bool dense = la.depth[0] == 1 && la.depth[1] == 1 && la.stride[1][0] == 1 && la.stride[0][0] % VEC == 0 &&
+                       lb.depth[0] == 1 && lb.depth[1] == 1 && lb.stride[1][0] == 1 && lb.stride[0][0] % VEC == 0 &&
+                       ld.depth[0] == 1 && ld.depth[1] == 1 && ld.stride[1][0] == 1 && a.K % VEC == 0 &&
+                       (reinterpret_cast<uintptr_t>(a.A) & 15u) == 0 && (reinterpret_cast<uintptr_t>(a.B) & 15u) == 0 &&
+                       a.M < (int64_t{1} << 31) && a.N < (int64_t{1} << 31) && a.K < (int64_t{1} << 31);
+    if (dense) {
+        note_launch();
+        ffma_dense_kernel<T, BM, BN, BK><<<grid, kFfmaThreads, 0, s>>>(
+            static_cast<const T *>(a.A), static_cast<const T *>(a.B), static_cast<T *>(a.D), la.stride[0][0],
+            lb.stride[0][0], ld.stride[0][0], static_cast<int>(a.M), static_cast<int>(a.N), static_cast<int>(a.K));
+        return cudaGetLastError();
+    }
     note_launch();
     ffma_gemm_kernel<T, BM, BN, BK><<<grid, kFfmaThreads, 0, s>>>(static_cast<const T *>(a.A), static_cast<const T *>(a.B),
                                                                   static_cast<T *>(a.D), a.la, a.lb, a.ld, a.M, a.N, a.K,
