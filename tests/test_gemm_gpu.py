@@ -80,7 +80,8 @@ def test_ffma_fp32_ragged_and_general_layouts(tmg):
 def test_ffma_dense_and_general_kernels_agree(tmg, dtype, M, N, K):
     """Row-major operands with 16-byte rows take the dense CUDA-core kernel;
     the same values read through a padded row stride (K + 1, not a multiple
-    of the vector) take the general crd2idx kernel.  Both use the same tiles
+    of the vector), or from a pointer 4 bytes past a 16-byte boundary, take
+    the general crd2idx kernel.  Both use the same tiles
     and k order, so they agree bit for bit; both match the oracle.  The
     shapes cover the three tile configurations (16x16 with 128-deep K
     slices, 32x32, 64x64) and ragged edges."""
@@ -95,6 +96,13 @@ def test_ffma_dense_and_general_kernels_agree(tmg, dtype, M, N, K):
     D2 = tmg.gemm(dApad, dB, M=M, N=N, K=K, layoutA=((M, K), (K + 1, 1)), path="ffma")
     tmg.check()
     assert torch.equal(D1, D2)
+    # the same row-major values four bytes past a 16-byte boundary: general kernel
+    flat = torch.zeros(M * K + 8, dtype=A.dtype, device=DEV)
+    Aoff = flat[4 // A.element_size():][:M * K].view(M, K)
+    Aoff.copy_(dA)
+    D3 = tmg.gemm(Aoff, dB, path="ffma")
+    tmg.check()
+    assert torch.equal(D1, D3)
     if dtype == "f32":
         parity.check_fp32(D1, parity.ref_full(A, B, oracle.F32))
     else:
