@@ -401,6 +401,25 @@ def test_skinny_tc_integer_exact_and_repeatable(tmg):
     parity.check_exact_bf16(parity.bf16_bits(D2), ref)
 
 
+@pytest.mark.parametrize("N", [19456, 25600, 38952])
+def test_skinny_tc_whole_and_split_tiles_exact(tmg, N):
+    """The skinny kernel's schedule: tiles // G whole tiles per CTA and the
+    remaining tiles shared out as stream-K runs.  On 152 SMs: 152 tiles (all
+    whole, nothing split), 200 tiles (one whole tile each, 48 split), and
+    305 tiles with a ragged last one (two whole tiles each, one tile split
+    over more CTAs than it has K blocks, so most CTAs have no stream-K
+    units).  Integer inputs: bit-exact, twice in a row."""
+    M, K = 16, 1024
+    A = inputs.integer_valued(M, K, 111)
+    B = inputs.integer_valued(N, K, 112 + N)
+    dA, dB = _gpu(A, B)
+    D1 = tmg.gemm(dA, dB, path="skinny").clone()
+    D2 = tmg.gemm(dA, dB, path="skinny")
+    tmg.check()
+    assert torch.equal(D1, D2)
+    parity.check_exact_bf16(parity.bf16_bits(D2), parity.ref_full(A, B, oracle.BF16))
+
+
 def test_workload_skinny_sampled(tmg):
     """16x28672x8192 decode GEMM, the benchmark's launch (auto -> skinny)."""
     w = inputs.WORKLOADS["skinny_16x28672x8192"]
