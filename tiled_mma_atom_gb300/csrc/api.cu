@@ -758,6 +758,7 @@ __global__ void wait_probe_kernel(ErrCtx err)
         mbar_wait(&bar, 0, err, nullptr, kSiteProbe);   // nothing ever arrives
 }
 
+#ifdef TMG_DEBUG_BOUNDS
 // Checks the offset `limit` against a buffer of `limit` elements — one past
 // its end — and touches no memory either way: the debug build's check must
 // record it in the device error word.
@@ -766,6 +767,7 @@ __global__ void bounds_probe_kernel(int64_t limit, ErrCtx err)
     if (threadIdx.x == 0)
         (void)bounds_ok(limit, limit, err, kBndProbe);
 }
+#endif
 
 }  // namespace
 
