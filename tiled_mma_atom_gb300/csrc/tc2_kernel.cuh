@@ -69,8 +69,10 @@ __host__ __device__ constexpr int tc2_threads(bool epi) { return 64 + 32 * epi_w
 __host__ __device__ constexpr int kb_elems(int in) { return in == kInE4m3 ? 128 : 64; }
 
 // Shared memory, in order: the ring of A / B stages; the barriers; with the
-// fused epilogue, per epilogue warp a copy of the tile's scale_b and bias
-// columns.  (The epilogue stores D straight from registers with 32-byte
+// fused epilogue, per epilogue warp a copy of the scale_b and bias columns
+// of its own chunks of the tile (copies of the whole tile's columns cost the
+// 224-wide kernel its seventh stage: bf16 4096^3 with the fused epilogue
+// but no operation took 78.5 instead of 76.5 us).  (The epilogue stores D straight from registers with 32-byte
 // vector stores: staging tiles in shared memory for TMA stores was no faster
 // and 16-byte stores wrote each 32-byte sector in halves — bf16 4096³:
 // 83.5 -> 81.5 µs.)
@@ -79,7 +81,10 @@ struct PairCfg {
     static constexpr int A_BYTES = kHalfM * kKBlockBytes;       // 16 KB
     static constexpr int B_BYTES = (BN / 2) * kKBlockBytes;     // this CTA's half
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int COLS_BYTES = EPI ? epi_warps(EPI) * 2 * BN * 4 : 0;
+    // each epilogue warp's copy of the scale_b and bias columns of its own
+    // chunks of the tile (the warps sharing a lane quarter split the chunks)
+    static constexpr int COLW = EPI ? ((BN / 32 + epi_warps(EPI) / 4 - 1) / (epi_warps(EPI) / 4)) * 32 : 0;
+    static constexpr int COLS_BYTES = epi_warps(EPI) * 2 * COLW * 4;
     static constexpr int RING_BUDGET = 220 * 1024 - 2048 - COLS_BYTES;
     static constexpr int STAGES = RING_BUDGET / STAGE_BYTES > 8 ? 8 : RING_BUDGET / STAGE_BYTES;
     static constexpr int TMEM_COLS = 512;
@@ -271,7 +276,7 @@ __device__ __forceinline__ float gelu_as(float y)
 // slow the whole kernel 2-4x).  SiLU uses the fast exponential and division
 // intrinsics, GELU the erfc formula above: their errors (a few fp32 ulp,
 // 1.5e-7) are far below the bf16 rounding that follows.
-template <int BN>
+template <int COLW>
 __device__ __forceinline__ void apply_epilogue(float (&v)[32], const Tc2Epi &e, float sa_row, const float *cols,
                                                int cl)
 {
@@ -292,7 +297,7 @@ __device__ __forceinline__ void apply_epilogue(float (&v)[32], const Tc2Epi &e, 
         }
     }
     if (e.epi >= kEpiBias) {
-        const float4 *w = reinterpret_cast<const float4 *>(cols + BN + cl);
+        const float4 *w = reinterpret_cast<const float4 *>(cols + COLW + cl);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const float4 t = w[j];
@@ -507,7 +512,7 @@ __global__ void __launch_bounds__(tc2_threads(EPI), 1)
             const int row = tm * kBM + static_cast<int>(rank) * kHalfM + q * 32 + lane;
             // this warp's copy of the tile's scale_b / bias columns, staged
             // while the accumulator is still being computed
-            float *cols = epi_cols + e * 2 * BN;
+            float *cols = epi_cols + e * 2 * C::COLW;
             float sa_row = 1.f;
             if constexpr (EPI) {
                 if (epi.scale_a && row < M)
@@ -516,10 +521,10 @@ __global__ void __launch_bounds__(tc2_threads(EPI), 1)
                 const int c0 = tn * BN;
                 if (epi.scale_b)
                     for (int i = c_begin * 32 + lane; i < c_end * 32; i += 32)
-                        cols[i] = c0 + i < N ? __ldg(epi.scale_b + c0 + i) : 0.f;
+                        cols[i - c_begin * 32] = c0 + i < N ? __ldg(epi.scale_b + c0 + i) : 0.f;
                 if (epi.epi >= kEpiBias)
                     for (int i = c_begin * 32 + lane; i < c_end * 32; i += 32)
-                        cols[BN + i] = c0 + i < N ? __ldg(epi.bias + c0 + i) : 0.f;
+                        cols[C::COLW + i - c_begin * 32] = c0 + i < N ? __ldg(epi.bias + c0 + i) : 0.f;
                 __syncwarp();
             }
             if (!mbar_wait_cluster(&tfull[acc], acc_phase, err, abort_flag, kSiteEpiTmemFull))
@@ -537,7 +542,7 @@ __global__ void __launch_bounds__(tc2_threads(EPI), 1)
                     for (int j = 0; j < 32; ++j)
                         v[j] = __uint_as_float(r[j]);
                     if constexpr (EPI)
-                        apply_epilogue<BN>(v, epi, sa_row, cols, c * 32);
+                        apply_epilogue<C::COLW>(v, epi, sa_row, cols, (c - c_begin) * 32);
                     const int col0 = tn * BN + c * 32;
                     if constexpr (EPI) {
                         if (epi.out_i32) {
@@ -620,7 +625,7 @@ __global__ void __launch_bounds__(tc2_threads(EPI), 1)
                     }
                 }
                 if constexpr (EPI) {
-                    apply_epilogue<BN>(v, epi, sa_row, cols, c * 32);
+                    apply_epilogue<C::COLW>(v, epi, sa_row, cols, (c - c_begin) * 32);
                     if (epi.out_i32) {
                         if (row < M && span_ok(static_cast<int64_t>(row) * ldd + tn * BN + c * 32,
                                                min(32, N - tn * BN - c * 32), d_limit, err, kBndStoreD))
