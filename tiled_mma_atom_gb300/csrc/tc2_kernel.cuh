@@ -26,16 +26,17 @@
 //                 `tmem_empty` barrier (count: the epilogue warps of both
 //                 CTAs).
 //
-// Schedule.  A pair MMA costs nearly the same whatever its width, so tiles
-// are as wide as possible (BN = 256 unless the last column tile would be
-// mostly empty).  When the tile count is not a multiple of the P pairs, 1-2
-// waves' worth of tiles run stream-K — their (tile, K block) units cut into
-// P equal contiguous runs, one per pair — and the rest data-parallel (pair c
-// takes c, c + P, ...); each pair does its stream-K run first.  A tile split
-// across pairs leaves fp32 partial sums in scratch; the last pair to finish
-// a piece of it (a counter per tile, CTA and epilogue warp) adds the
-// partials in pair order — a fixed order, so the result does not depend on
-// timing — applies the epilogue, rounds to bf16 and resets the counter.
+// Schedule (planned on the host by tc2_plan).  The tile width (256, 224,
+// 192 or 128) and the schedule come from a cost model of measured per-K-block
+// tile times: whole data-parallel waves (pair c takes tiles c, c + P, ...),
+// or, where a partial last wave would leave most pairs idle, the last full
+// wave and the partial one run stream-K — their (tile, K block) units cut
+// into P equal contiguous runs, one per pair, each pair doing its run first.
+// A tile split across pairs leaves fp32 partial sums in scratch; the last
+// pair to finish a piece of it (a counter per tile, CTA and epilogue warp)
+// adds the partials in pair order — a fixed order, so the result does not
+// depend on timing — applies the epilogue, rounds to bf16 and resets the
+// counter.  Tiles are visited in groups of group_m M-tiles.
 //
 // The fused epilogue follows the options of the preshuffle GEMM in "Kernel
 // authoring guide", §11 "Complete example: Preshuffle GEMM" (scale_a,
