@@ -100,6 +100,20 @@ def test_w4a8_decode_several_units_per_cta(tmg, M):
     assert np.array_equal(D.cpu().numpy(), ref)
 
 
+@pytest.mark.parametrize("shuffled", [False, True])
+@pytest.mark.parametrize("N,K", [(25600, 2048), (38952, 1024), (19496, 2048)])
+def test_w4a8_decode_many_tiles_exact(tmg, N, K, shuffled):
+    """Decode shapes with more 128-row tiles than SMs (200, 153 and 305
+    tiles, the last ragged), so every CTA's stream-K run spans whole and
+    shared tiles (red.adds into zeroed D).  Row-major and pre-shuffled
+    weights; bit-exact."""
+    M = 16
+    A, B = inputs.random_int8(M, K, 751), inputs.random_int4_packed(N, K, 752)
+    ref = oracle.gemm_w4a8(A.numpy(), B.numpy(), M, N, K)
+    got = _run_shuffled(tmg, A, B) if shuffled else _run(tmg, A, B)
+    assert np.array_equal(got, ref)
+
+
 def test_w4a8_decode_extreme_values_at_max_k(tmg):
     """K = 32768, the decode kernel's limit, with the values that drive its
     fp32 column sums furthest from zero: the kernel splits a = 16 hi + lo
